@@ -1,0 +1,348 @@
+// ftd_api.cu -- the C ABI declared in include/ftd.h.
+//
+// Host side only: argument checks, the single pool allocation made at init
+// (the pre-allocated KV-cache buffer of "FasterTransformer source analysis",
+// framerc.cn, section 3.2), kernel selection and launch.  Every step of the
+// decode path itself runs in the kernels of ftd_decode_splitk.cuh.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+
+#include "../../include/ftd.h"
+#include "ftd_decode_splitk.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+ftd_status fail(ftd_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+ftd_status fail(ftd_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+ftd_status cuda_fail(cudaError_t e, const char* what) {
+    if (e == cudaErrorMemoryAllocation) return fail(FTD_ERR_OOM, "%s: %s", what, cudaGetErrorString(e));
+    return fail(FTD_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int elem_bytes(ftd_dtype d) {
+    switch (d) {
+        case FTD_F32: return 4;
+        case FTD_F16: return 2;
+        case FTD_BF16: return 2;
+        case FTD_I8: return 1;
+    }
+    return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct ftd_ctx {
+    ftd_config cfg;
+    int device = 0;
+    int grid = 0;
+    int G = 1, nhb = 1;
+    ftd::KernelInfo ki{};
+    float qscale = 0.f;
+    void* pool = nullptr;
+    size_t pool_bytes = 0;
+    unsigned char* k_cache = nullptr;
+    unsigned char* v_cache = nullptr;
+    float* scales = nullptr;
+    float* ws = nullptr;
+    uint32_t* counters = nullptr;
+    size_t n_counters = 0;
+    uint32_t* err = nullptr;
+    void* st_q = nullptr;
+    void* st_k = nullptr;
+    void* st_v = nullptr;
+    void* st_bias = nullptr;
+    int32_t* st_lens = nullptr;
+    float* st_out = nullptr;
+    size_t q_bytes = 0, kv_new_bytes = 0, bias_bytes = 0, out_bytes = 0;
+    cudaStream_t last_stream = nullptr;
+};
+
+extern "C" {
+
+const char* ftd_status_str(ftd_status s) {
+    switch (s) {
+        case FTD_OK: return "FTD_OK";
+        case FTD_ERR_INVALID_ARG: return "FTD_ERR_INVALID_ARG";
+        case FTD_ERR_UNSUPPORTED: return "FTD_ERR_UNSUPPORTED";
+        case FTD_ERR_OOM: return "FTD_ERR_OOM";
+        case FTD_ERR_CUDA: return "FTD_ERR_CUDA";
+        case FTD_ERR_SEQ_OVERFLOW: return "FTD_ERR_SEQ_OVERFLOW";
+        case FTD_ERR_DEVICE_TIMEOUT: return "FTD_ERR_DEVICE_TIMEOUT";
+    }
+    return "FTD_ERR_UNKNOWN";
+}
+
+const char* ftd_last_error(void) { return g_last_error.c_str(); }
+
+uint64_t ftd_kernel_launches(void) { return g_launches.load(); }
+
+ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
+    g_last_error.clear();
+    if (!out) return fail(FTD_ERR_INVALID_ARG, "ftd_init: out is NULL");
+    *out = nullptr;
+    if (!cfg) return fail(FTD_ERR_INVALID_ARG, "ftd_init: cfg is NULL");
+    const ftd_config c = *cfg;
+    if (c.max_batch < 1 || c.max_batch > ftd::kMaxBatch)
+        return fail(FTD_ERR_INVALID_ARG, "max_batch %d outside 1..%d", c.max_batch, ftd::kMaxBatch);
+    if (c.n_kv_heads < 1 || c.n_q_heads < c.n_kv_heads || c.n_q_heads % c.n_kv_heads != 0)
+        return fail(FTD_ERR_INVALID_ARG, "n_q_heads %d must be a positive multiple of n_kv_heads %d",
+                    c.n_q_heads, c.n_kv_heads);
+    if (c.max_len < 16 || c.max_len % 16 != 0)
+        return fail(FTD_ERR_INVALID_ARG, "max_len %d must be a positive multiple of 16", c.max_len);
+    if (c.head_dim <= 0) return fail(FTD_ERR_INVALID_ARG, "head_dim %d", c.head_dim);
+    if (c.head_dim != 64 && c.head_dim != 128)
+        return fail(FTD_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", c.head_dim);
+    if (c.qkv_dtype != FTD_F32 && c.qkv_dtype != FTD_F16 && c.qkv_dtype != FTD_BF16)
+        return fail(FTD_ERR_UNSUPPORTED, "qkv_dtype %d (F32, F16 or BF16)", static_cast<int>(c.qkv_dtype));
+    if (c.cache_dtype != FTD_F32 && c.cache_dtype != FTD_F16 && c.cache_dtype != FTD_BF16 &&
+        c.cache_dtype != FTD_I8)
+        return fail(FTD_ERR_UNSUPPORTED, "cache_dtype %d", static_cast<int>(c.cache_dtype));
+    if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale))
+        return fail(FTD_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+
+    const int g = c.n_q_heads / c.n_kv_heads;
+    int G = 8;
+    while (g % G) G >>= 1;
+    const int nhb = g / G;
+
+    ftd::KernelInfo ki{};
+    switch (c.cache_dtype) {
+        case FTD_F32: ki = ftd::select_f32(c.head_dim, G); break;
+        case FTD_F16: ki = ftd::select_f16(c.head_dim, G); break;
+        case FTD_BF16: ki = ftd::select_bf16(c.head_dim, G); break;
+        case FTD_I8: ki = ftd::select_i8(c.head_dim, G); break;
+    }
+    if (!ki.fn) return fail(FTD_ERR_UNSUPPORTED, "no kernel for this configuration");
+
+    const long long tiles_per_seq = (c.max_len + ki.T - 1) / ki.T;
+    const long long max_tiles = static_cast<long long>(c.max_batch) * c.n_kv_heads * nhb * tiles_per_seq;
+    if (max_tiles >= (1LL << 31)) return fail(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit tile indices");
+
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+
+    const int grid = sms;  // one persistent CTA of 8 worker warps per SM
+    const size_t B = c.max_batch, Hq = c.n_q_heads, Hkv = c.n_kv_heads, D = c.head_dim, L = c.max_len;
+    const size_t cache_bytes = B * Hkv * L * D * elem_bytes(c.cache_dtype);
+    const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * B * Hkv * L * sizeof(float) : 0;
+    const size_t n_seg = B * Hkv * nhb;
+    const size_t n_slots = n_seg + static_cast<size_t>(grid) * ftd::kWarps;
+    const size_t ws_bytes = n_slots * ki.slot_floats * sizeof(float);
+    const int qeb = elem_bytes(c.qkv_dtype);
+
+    ftd_ctx* ctx = new (std::nothrow) ftd_ctx();
+    if (!ctx) return fail(FTD_ERR_OOM, "host allocation of the context failed");
+    ctx->cfg = c;
+    ctx->device = dev;
+    ctx->grid = grid;
+    ctx->G = G;
+    ctx->nhb = nhb;
+    ctx->ki = ki;
+    const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf(static_cast<float>(D));
+    ctx->qscale = scale * 1.4426950408889634f;
+    ctx->q_bytes = B * Hq * D * qeb;
+    ctx->kv_new_bytes = B * Hkv * D * qeb;
+    ctx->bias_bytes = (Hq + 2 * Hkv) * D * qeb;
+    ctx->out_bytes = B * Hq * D * sizeof(float);
+    ctx->n_counters = n_seg;
+
+    size_t off = 0;
+    auto carve = [&](size_t bytes) {
+        const size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    const size_t o_k = carve(cache_bytes), o_v = carve(cache_bytes), o_s = carve(scale_bytes);
+    const size_t o_cnt = carve(n_seg * sizeof(uint32_t)), o_err = carve(sizeof(uint32_t));
+    const size_t zero_end = off;  // caches, scales, counters and the error word start at zero
+    const size_t o_ws = carve(ws_bytes);
+    const size_t o_q = carve(ctx->q_bytes), o_kn = carve(ctx->kv_new_bytes), o_vn = carve(ctx->kv_new_bytes);
+    const size_t o_b = carve(ctx->bias_bytes), o_l = carve(B * sizeof(int32_t)), o_o = carve(ctx->out_bytes);
+    ctx->pool_bytes = off;
+
+    e = cudaMalloc(&ctx->pool, ctx->pool_bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete ctx;
+        return cuda_fail(e, "cudaMalloc of the cache pool");
+    }
+    unsigned char* base = static_cast<unsigned char*>(ctx->pool);
+    ctx->k_cache = base + o_k;
+    ctx->v_cache = base + o_v;
+    ctx->scales = scale_bytes ? reinterpret_cast<float*>(base + o_s) : nullptr;
+    ctx->counters = reinterpret_cast<uint32_t*>(base + o_cnt);
+    ctx->err = reinterpret_cast<uint32_t*>(base + o_err);
+    ctx->ws = reinterpret_cast<float*>(base + o_ws);
+    ctx->st_q = base + o_q;
+    ctx->st_k = base + o_kn;
+    ctx->st_v = base + o_vn;
+    ctx->st_bias = base + o_b;
+    ctx->st_lens = reinterpret_cast<int32_t*>(base + o_l);
+    ctx->st_out = reinterpret_cast<float*>(base + o_o);
+    ctx->last_stream = static_cast<cudaStream_t>(stream);
+
+    e = cudaMemsetAsync(ctx->pool, 0, zero_end, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaFree(ctx->pool);
+        delete ctx;
+        return cuda_fail(e, "cudaMemsetAsync of the cache pool");
+    }
+    *out = ctx;
+    return FTD_OK;
+}
+
+ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** scales) {
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_cache_ptrs: ctx is NULL");
+    if (k_cache) *k_cache = ctx->k_cache;
+    if (v_cache) *v_cache = ctx->v_cache;
+    if (scales) *scales = ctx->scales;
+    return FTD_OK;
+}
+
+static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                                const void* bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
+                                float* scales, float* out, cudaStream_t stream) {
+    if (!q || !k_new || !v_new || !seq_lens || !out)
+        return fail(FTD_ERR_INVALID_ARG, "q, k_new, v_new, seq_lens and out must be non-NULL");
+    if (!k_cache) k_cache = ctx->k_cache;
+    if (!v_cache) v_cache = ctx->v_cache;
+    const bool i8 = ctx->cfg.cache_dtype == FTD_I8;
+    if (i8 && !scales) scales = ctx->scales;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || (i8 && !aligned16(scales)) || !aligned16(out))
+        return fail(FTD_ERR_INVALID_ARG, "caches, scales and out must be 16-byte aligned");
+    const int qeb = elem_bytes(ctx->cfg.qkv_dtype);
+    const uintptr_t qmask = static_cast<uintptr_t>(qeb - 1);
+    if ((reinterpret_cast<uintptr_t>(q) & qmask) || (reinterpret_cast<uintptr_t>(k_new) & qmask) ||
+        (reinterpret_cast<uintptr_t>(v_new) & qmask) || (reinterpret_cast<uintptr_t>(bias) & qmask) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return fail(FTD_ERR_INVALID_ARG, "q, k_new, v_new, bias, seq_lens must be naturally aligned");
+
+    const ftd_config& c = ctx->cfg;
+    ftd::DecodeParams p{};
+    p.q = q;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.bias = bias;
+    p.k_cache = static_cast<unsigned char*>(k_cache);
+    p.v_cache = static_cast<unsigned char*>(v_cache);
+    const size_t plane = static_cast<size_t>(c.max_batch) * c.n_kv_heads * c.max_len;
+    p.k_scales = i8 ? scales : nullptr;
+    p.v_scales = i8 ? scales + plane : nullptr;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.ws = ctx->ws;
+    p.counters = ctx->counters;
+    p.err = ctx->err;
+    p.B = c.max_batch;
+    p.Hq = c.n_q_heads;
+    p.Hkv = c.n_kv_heads;
+    p.Lmax = c.max_len;
+    p.group = c.n_q_heads / c.n_kv_heads;
+    p.nhb = ctx->nhb;
+    p.qkv_dtype = static_cast<int>(c.qkv_dtype);
+    p.qscale = ctx->qscale;
+
+    void* args[] = {&p};
+    cudaError_t e = cudaLaunchKernel(ctx->ki.fn, dim3(ctx->grid), dim3(ftd::kThreads), args,
+                                     static_cast<size_t>(ctx->ki.smem), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
+    g_launches.fetch_add(1);
+    ctx->last_stream = stream;
+    return FTD_OK;
+}
+
+ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                          const void* qkv_bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
+                          float* scales, float* out, void* stream) {
+    g_last_error.clear();
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha: ctx is NULL");
+    return launch_decode(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out,
+                         static_cast<cudaStream_t>(stream));
+}
+
+ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                               const void* qkv_bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
+                               float* scales, float* out, void* stream) {
+    g_last_error.clear();
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_host: ctx is NULL");
+    if (!q || !k_new || !v_new || !seq_lens || !out)
+        return fail(FTD_ERR_INVALID_ARG, "q, k_new, v_new, seq_lens and out must be non-NULL");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t B = ctx->cfg.max_batch;
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(ctx->st_q, q, ctx->q_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(ctx->st_k, k_new, ctx->kv_new_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(ctx->st_v, v_new, ctx->kv_new_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(ctx->st_lens, seq_lens, B * sizeof(int32_t), cudaMemcpyHostToDevice, s)) !=
+            cudaSuccess)
+        return cuda_fail(e, "host-to-device copy of the step inputs");
+    if (qkv_bias) {
+        e = cudaMemcpyAsync(ctx->st_bias, qkv_bias, ctx->bias_bytes, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of the bias");
+    }
+    ftd_status st = launch_decode(ctx, ctx->st_q, ctx->st_k, ctx->st_v, qkv_bias ? ctx->st_bias : nullptr,
+                                  k_cache, v_cache, ctx->st_lens, scales, ctx->st_out, s);
+    if (st != FTD_OK) return st;
+    e = cudaMemcpyAsync(out, ctx->st_out, ctx->out_bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of the output");
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return FTD_OK;
+}
+
+ftd_status ftd_get_error(ftd_ctx* ctx) {
+    g_last_error.clear();
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_get_error: ctx is NULL");
+    cudaError_t e = cudaStreamSynchronize(ctx->last_stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    uint32_t h = 0;
+    e = cudaMemcpy(&h, ctx->err, sizeof h, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (!h) return FTD_OK;
+    e = cudaMemset(ctx->err, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    if (h & ftd::kErrTimeout) {
+        // an abandoned launch may have left segment counters part-way; restart them
+        e = cudaMemset(ctx->counters, 0, ctx->n_counters * sizeof(uint32_t));
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the split-K counters");
+        return fail(FTD_ERR_DEVICE_TIMEOUT, "a decode kernel gave up waiting for a copy");
+    }
+    return fail(FTD_ERR_SEQ_OVERFLOW, "some seq_lens[b] >= max_len; those slots were skipped");
+}
+
+void ftd_destroy(ftd_ctx* ctx) {
+    if (!ctx) return;
+    cudaDeviceSynchronize();
+    cudaFree(ctx->pool);
+    delete ctx;
+}
+
+}  // extern "C"

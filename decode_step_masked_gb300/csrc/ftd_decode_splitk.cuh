@@ -1,0 +1,642 @@
+// ftd_decode_splitk.cuh -- one decode step of masked multi-head attention as a
+// single persistent kernel on CUDA cores (sm_103a).
+//
+// What one launch computes (see include/ftd.h for the full contract):
+//   fused QKV bias add, append of the new K/V row at position L_b, scores of
+//   the current token against positions 0..L_b, a numerically stable softmax
+//   and the weighted sum of V -- the decode path of the FasterTransformer
+//   masked multi-head attention kernel ("FasterTransformer source reading",
+//   lmnt.cn, section 4.1; lpnh.cn section 2.1: q.K, softmax and x V fused so
+//   no score tensor reaches HBM).
+//
+// Work decomposition (split-K over the cache length):
+//   A "segment" is one (slot b, kv head, block of G query heads).  Segment
+//   (b, .) owns ceil((L_b + 1) / T) tiles of T cache rows.  All tiles of all
+//   segments form one global index space, ordered slot-major.  Every warp of
+//   the grid is an independent worker that takes an equal contiguous range of
+//   that space (static, balanced to one tile), so ragged batches cannot leave
+//   SMs idle.  A worker streams its tiles through a private ring of shared
+//   memory stages filled by the bulk-copy engine (cp.async.bulk, one copy per
+//   K tile and per V tile, completing on an mbarrier), keeps the running max,
+//   sum and output of an online softmax in registers ("10 tricks",
+//   pptc.cn, section 2.2), and at the end of each piece of a segment either
+//   writes the final output (the piece is the whole segment) or a partial
+//   (max, sum, o) to the workspace, in slot (segment index + worker index),
+//   which is unique because both indices only grow along the tile space.
+//   Each piece adds its tile count to the segment's counter; the piece that
+//   completes the count merges the partials by log-sum-exp and resets the
+//   counter, so the whole step is one launch with no inter-block waiting.
+//
+// Lane layout inside a warp: half-warp hr = lane / 16 takes the even or odd
+// rows of a tile, lane c = lane % 16 owns head dimensions [c*EPL, (c+1)*EPL).
+// q.k partial sums are reduced across the 16 lanes with a reduce-scatter
+// (log2(16) shuffle rounds that halve the live values each round).
+#pragma once
+
+#include <cmath>
+#include <type_traits>
+
+#include "ftd_common.cuh"
+
+namespace ftd {
+
+template <typename CT>
+struct CacheTraits;
+template <>
+struct CacheTraits<float> { static constexpr int EB = 4; static constexpr bool I8 = false; };
+template <>
+struct CacheTraits<__half> { static constexpr int EB = 2; static constexpr bool I8 = false; };
+template <>
+struct CacheTraits<__nv_bfloat16> { static constexpr int EB = 2; static constexpr bool I8 = false; };
+template <>
+struct CacheTraits<int8_t> { static constexpr int EB = 1; static constexpr bool I8 = true; };
+
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+constexpr int cmax(int a, int b) { return a > b ? a : b; }
+constexpr int round_up(int a, int b) { return (a + b - 1) / b * b; }
+
+template <typename CT, int D, int G>
+struct Tiling {
+    static constexpr int EB = CacheTraits<CT>::EB;
+    static constexpr bool I8 = CacheTraits<CT>::I8;
+    static constexpr int ROW = D * EB;                         // bytes per cache row
+    static constexpr int T = cmax(8, cmin(32, 4096 / ROW));    // rows per tile (4 KB K tiles)
+    static constexpr int R = T / 2;                            // rows per half-warp
+    static constexpr int EPL = D / 16;                         // elements per lane
+    static constexpr int TILE = T * ROW;
+    static constexpr int SCL = I8 ? T * 4 : 0;                 // per-row scales of one tile
+    static constexpr int STAGE = 2 * TILE + 2 * SCL;
+    static constexpr int SPW = cmax(2, cmin(4, 26624 / STAGE));  // ring stages per warp
+    static constexpr int RB = cmax(1, cmin(R, 16 / G));        // rows per reduce-scatter batch
+    static constexpr int SCRATCH = 2 * G * T * 4;              // scores + probabilities
+    static constexpr int WARP_BYTES = round_up(SPW * STAGE + SCRATCH + SPW * 8, 128);
+    static constexpr int PREFIX_BYTES = round_up((2 * kMaxBatch + 1) * 4, 128);
+    static constexpr int SMEM = PREFIX_BYTES + kWarps * WARP_BYTES;
+    static constexpr int OOFF = round_up(2 * G, 4);            // o offset in a partial slot
+    static constexpr int SLOT = OOFF + G * D;                  // floats per partial slot
+    static_assert(D % 16 == 0 && (EPL == 4 || EPL == 8), "head_dim 64 or 128");
+    static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(G * RB <= 16 && R % RB == 0, "reduce-scatter batch");
+};
+
+// ------------------------------------------------ shared-memory row access
+template <typename CT, int N>
+__device__ __forceinline__ void ld_cvt(const unsigned char* p, float (&f)[N]) {
+    if constexpr (std::is_same_v<CT, __nv_bfloat16>) {
+        // bfloat16 -> binary32 is exact: the pattern becomes the upper half
+        uint32_t w[N / 2];
+        if constexpr (N == 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(p);
+            w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            w[0] = u.x; w[1] = u.y;
+        }
+#pragma unroll
+        for (int k = 0; k < N / 2; ++k) {
+            f[2 * k] = __uint_as_float(w[k] << 16);
+            f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    } else if constexpr (std::is_same_v<CT, __half>) {
+        uint32_t w[N / 2];
+        if constexpr (N == 8) {
+            const uint4 u = *reinterpret_cast<const uint4*>(p);
+            w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+        } else {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            w[0] = u.x; w[1] = u.y;
+        }
+#pragma unroll
+        for (int k = 0; k < N / 2; ++k) {
+            __half2 h2;
+            memcpy(&h2, &w[k], 4);
+            const float2 ff = __half22float2(h2);
+            f[2 * k] = ff.x;
+            f[2 * k + 1] = ff.y;
+        }
+    } else if constexpr (std::is_same_v<CT, float>) {
+#pragma unroll
+        for (int k = 0; k < N / 4; ++k) {
+            const float4 u = reinterpret_cast<const float4*>(p)[k];
+            f[4 * k] = u.x; f[4 * k + 1] = u.y; f[4 * k + 2] = u.z; f[4 * k + 3] = u.w;
+        }
+    } else {  // int8 codes
+        uint32_t w[N / 4];
+        if constexpr (N == 8) {
+            const uint2 u = *reinterpret_cast<const uint2*>(p);
+            w[0] = u.x; w[1] = u.y;
+        } else {
+            w[0] = *reinterpret_cast<const uint32_t*>(p);
+        }
+#pragma unroll
+        for (int k = 0; k < N; ++k)
+            f[k] = static_cast<float>(static_cast<int8_t>((w[k / 4] >> (8 * (k % 4))) & 0xffu));
+    }
+}
+
+// Round N binary32 values to the cache type (nearest even) and store them.
+template <typename CT, int N>
+__device__ __forceinline__ void cvt_st(unsigned char* p, const float (&x)[N]) {
+    if constexpr (std::is_same_v<CT, float>) {
+#pragma unroll
+        for (int k = 0; k < N / 4; ++k)
+            reinterpret_cast<float4*>(p)[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+    } else {
+        uint32_t w[N / 2];
+#pragma unroll
+        for (int k = 0; k < N / 2; ++k) {
+            uint16_t lo, hi;
+            if constexpr (std::is_same_v<CT, __half>) {
+                lo = __half_as_ushort(__float2half_rn(x[2 * k]));
+                hi = __half_as_ushort(__float2half_rn(x[2 * k + 1]));
+            } else {
+                lo = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * k]));
+                hi = __bfloat16_as_ushort(__float2bfloat16_rn(x[2 * k + 1]));
+            }
+            w[k] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+        }
+        if constexpr (N == 8) *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+        else *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
+    }
+}
+
+// ------------------------------------------------------- reduce-scatter
+// Sum N values over the 16 lanes of a half-warp.  Each halving round sends
+// half of the live values to the partner lane and keeps the other half, so
+// after log2(N) rounds every lane holds one fully reduced value, whose index
+// is returned in idx; remaining rounds are plain butterflies.
+template <int N, int MASK>
+struct ReduceScatter {
+    static __device__ __forceinline__ void run(float* v, int c, int& idx) {
+        if constexpr (MASK == 0) {
+            return;
+        } else if constexpr (N > 1) {
+            const bool up = (c & MASK) != 0;
+#pragma unroll
+            for (int k = 0; k < N / 2; ++k) {
+                const float send = up ? v[k] : v[k + N / 2];
+                const float keep = up ? v[k + N / 2] : v[k];
+                v[k] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
+            }
+            if (up) idx += N / 2;
+            ReduceScatter<N / 2, MASK / 2>::run(v, c, idx);
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
+            ReduceScatter<1, MASK / 2>::run(v, c, idx);
+        }
+    }
+};
+
+// ---------------------------------------------------------- tile cursor
+struct Cursor {
+    int b, seg, tile, nt;
+};
+
+__device__ __forceinline__ Cursor locate(int t, const int* P, int B, int segs) {
+    int lo = 0, hi = B - 1;  // largest b with P[b] <= t; then P[b] <= t < P[b + 1]
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    Cursor cu;
+    cu.b = lo;
+    cu.nt = (P[lo + 1] - P[lo]) / segs;
+    const int rem = t - P[lo];
+    cu.seg = rem / cu.nt;
+    cu.tile = rem - cu.seg * cu.nt;
+    return cu;
+}
+
+__device__ __forceinline__ void advance(Cursor& cu, const int* P, int segs) {
+    if (++cu.tile < cu.nt) return;
+    cu.tile = 0;
+    if (++cu.seg < segs) return;
+    cu.seg = 0;
+    do {
+        ++cu.b;
+    } while (P[cu.b + 1] == P[cu.b]);
+    cu.nt = (P[cu.b + 1] - P[cu.b]) / segs;
+}
+
+// Worker (global warp index) whose range holds tile t, for ranges
+// [floor(w*U/W), floor((w+1)*U/W)).
+__device__ __forceinline__ int worker_of(long long t, long long U, long long W) {
+    return static_cast<int>(((t + 1) * W - 1) / U);
+}
+
+// ================================================================ kernel
+template <typename CT, int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const DecodeParams p) {
+    using TL = Tiling<CT, D, G>;
+    constexpr int T = TL::T, R = TL::R, EPL = TL::EPL, ROW = TL::ROW, SPW = TL::SPW, RB = TL::RB;
+    constexpr int TILE = TL::TILE, SCL = TL::SCL, STAGE = TL::STAGE, EB = TL::EB;
+    constexpr bool I8 = TL::I8;
+    constexpr unsigned FULL = 0xffffffffu;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    int* P = reinterpret_cast<int*>(smem);  // [B + 1] tile prefix over slots
+    int* Ls = P + (kMaxBatch + 1);          // [B] cached length, -1 when the slot has no work
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hr = lane >> 4, c = lane & 15;
+    unsigned char* wbase = smem + TL::PREFIX_BYTES + warp * TL::WARP_BYTES;
+    float* sc = reinterpret_cast<float*>(wbase + SPW * STAGE);  // [G][T] scores
+    float* pb = sc + G * T;                                     // [G][T] weights
+    uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + SPW * STAGE + TL::SCRATCH);
+    const int segs = p.Hkv * p.nhb;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int s = 0; s < SPW; ++s) mbar_init(smem_addr(&bars[s]), 1);
+    }
+    // Tiles per slot and their prefix; overflowing slots raise the sticky flag.
+    if (warp == 0) {
+        int carry = 0;
+        bool ovf = false;
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
+            const bool valid = L >= 0 && L < p.Lmax;
+            ovf |= (b < p.B) && (L >= p.Lmax);
+            int v = valid ? ((L + T) / T) * segs : 0;  // ceil((L + 1) / T) tiles per segment
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const int y = __shfl_up_sync(FULL, v, m);
+                if (lane >= m) v += y;
+            }
+            if (b < p.B) {
+                P[b + 1] = carry + v;
+                Ls[b] = valid ? L : -1;
+            }
+            carry += __shfl_sync(FULL, v, 31);
+        }
+        if (lane == 0) P[0] = 0;
+        if (__any_sync(FULL, ovf) && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
+    }
+    fence_mbar_init();
+    __syncthreads();
+
+    // Slots without work (inactive or overflowing) get a zero output.
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        if (P[b + 1] == P[b]) {
+            float4* o4 = reinterpret_cast<float4*>(p.out + static_cast<size_t>(b) * p.Hq * D);
+            for (int i = threadIdx.x; i < p.Hq * D / 4; i += kThreads) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+
+    const long long U = P[p.B];
+    const long long W = static_cast<long long>(gridDim.x) * kWarps;
+    const int wid = blockIdx.x * kWarps + warp;
+    const int t_begin = static_cast<int>(wid * U / W);
+    const int n_my = static_cast<int>((wid + 1) * U / W) - t_begin;
+    if (n_my <= 0) return;
+
+    // ---- bulk copies of one tile (lane 0 only) ----
+    auto issue = [&](int s, const Cursor& cu) {
+        const int L = Ls[cu.b];
+        const int t0 = cu.tile * T;
+        const int n_total = min(T, L + 1 - t0);
+        const int n_cache = (cu.tile == cu.nt - 1) ? n_total - 1 : n_total;
+        const int kvh = cu.seg / p.nhb;
+        const size_t rowbase = (static_cast<size_t>(cu.b) * p.Hkv + kvh) * p.Lmax + t0;
+        const uint32_t kb = static_cast<uint32_t>(n_cache) * ROW;
+        const uint32_t sb = I8 ? static_cast<uint32_t>((n_cache * 4 + 15) & ~15) : 0u;
+        unsigned char* st = wbase + s * STAGE;
+        const uint32_t bar = smem_addr(&bars[s]);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(bar, 2 * kb + 2 * sb);
+        if (kb) {
+            bulk_g2s(smem_addr(st), p.k_cache + rowbase * ROW, kb, bar);
+            bulk_g2s(smem_addr(st + TILE), p.v_cache + rowbase * ROW, kb, bar);
+        }
+        if constexpr (I8) {
+            if (sb) {
+                bulk_g2s(smem_addr(st + 2 * TILE), p.k_scales + rowbase, sb, bar);
+                bulk_g2s(smem_addr(st + 2 * TILE + SCL), p.v_scales + rowbase, sb, bar);
+            }
+        }
+    };
+
+    Cursor ci = locate(t_begin, P, p.B, segs);
+    Cursor cc = ci;
+    const int npre = min(SPW, n_my);
+    for (int k = 0; k < npre; ++k) {
+        if (lane == 0) issue(k, ci);
+        if (k + 1 < n_my) advance(ci, P, segs);
+    }
+
+    float qr[G][EPL], o[G][EPL], m[G], l[G];
+    auto begin_segment = [&](const Cursor& cu) {
+        const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            const int h = kvh * p.group + hb * G + j;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const int d = c * EPL + e;
+                float x = ld_qkv(p.q, p.qkv_dtype, (static_cast<size_t>(cu.b) * p.Hq + h) * D + d);
+                if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + d);
+                qr[j][e] = x * p.qscale;
+                o[j][e] = 0.f;
+            }
+            m[j] = -INFINITY;
+            l[j] = 0.f;
+        }
+    };
+    begin_segment(cc);
+    int piece_first = cc.tile;
+
+    int k = 0;
+    for (; k < n_my; ++k) {
+        const int s = k % SPW;
+        unsigned char* st = wbase + s * STAGE;
+        if (!mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((k / SPW) & 1), p.err)) break;
+
+        const int L = Ls[cc.b];
+        const int t0 = cc.tile * T;
+        const int n_total = min(T, L + 1 - t0);
+        const bool last_tile = cc.tile == cc.nt - 1;
+        const int kvh = cc.seg / p.nhb, hb = cc.seg % p.nhb;
+        const size_t rowbase = (static_cast<size_t>(cc.b) * p.Hkv + kvh) * p.Lmax + t0;
+
+        // ---- append: the new token is the last visible row of the last tile ----
+        if (last_tile) {
+            const int nr = n_total - 1;  // its row inside the tile (position L)
+            const bool isv = hr != 0;   // half-warp 0 writes K, half-warp 1 writes V
+            const void* src = isv ? p.v_new : p.k_new;
+            const size_t si = (static_cast<size_t>(cc.b) * p.Hkv + kvh) * D + c * EPL;
+            const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + c * EPL;
+            float x[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                x[e] = ld_qkv(src, p.qkv_dtype, si + e);
+                if (p.bias) x[e] += ld_qkv(p.bias, p.qkv_dtype, bi + e);  // one binary32 add
+            }
+            unsigned char* srow = st + (isv ? TILE : 0) + nr * ROW + c * EPL * EB;
+            unsigned char* grow = (isv ? p.v_cache : p.k_cache) + (rowbase + nr) * ROW + c * EPL * EB;
+            if constexpr (I8) {
+                float amax = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+                for (int mm = 8; mm >= 1; mm >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, mm));
+                const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 127.f);
+                uint32_t w[EPL / 4];
+#pragma unroll
+                for (int k4 = 0; k4 < EPL / 4; ++k4) w[k4] = 0u;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    int code = 0;
+                    if (amax != 0.f) code = max(-127, min(127, __float2int_rn(__fdiv_rn(x[e], qs))));
+                    w[e / 4] |= (static_cast<uint32_t>(code) & 0xffu) << (8 * (e % 4));
+                }
+                if constexpr (EPL == 8) {
+                    *reinterpret_cast<uint2*>(srow) = make_uint2(w[0], w[1]);
+                    if (hb == 0) *reinterpret_cast<uint2*>(grow) = make_uint2(w[0], w[1]);
+                } else {
+                    *reinterpret_cast<uint32_t*>(srow) = w[0];
+                    if (hb == 0) *reinterpret_cast<uint32_t*>(grow) = w[0];
+                }
+                if (c == 0) {
+                    reinterpret_cast<float*>(st + 2 * TILE + (isv ? SCL : 0))[nr] = qs;
+                    if (hb == 0) (isv ? p.v_scales : p.k_scales)[rowbase + nr] = qs;
+                }
+            } else {
+                cvt_st<CT, EPL>(srow, x);
+                if (hb == 0) cvt_st<CT, EPL>(grow, x);
+            }
+            __syncwarp();
+        }
+
+        // ---- scores: q . k for every row, reduced across the 16 lanes ----
+        const unsigned char* Kt = st;
+        const unsigned char* Vt = st + TILE;
+#pragma unroll
+        for (int ib = 0; ib < R / RB; ++ib) {
+            float part[G * RB];
+#pragma unroll
+            for (int i = 0; i < RB; ++i) {
+                const int row = 2 * (ib * RB + i) + hr;
+                float kf[EPL];
+                ld_cvt<CT, EPL>(Kt + row * ROW + c * EPL * EB, kf);
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) a = fmaf(qr[j][e], kf[e], a);
+                    part[j * RB + i] = a;
+                }
+            }
+            int idx = 0;
+            ReduceScatter<G * RB, 8>::run(part, c, idx);
+            const int j = idx / RB, i = idx % RB;
+            sc[j * T + 2 * (ib * RB + i) + hr] = part[0];
+        }
+        __syncwarp();
+
+        // ---- online softmax over the tile (log2 domain) ----
+        float alpha[G];
+        const int r = lane % T;
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            float sv = -INFINITY;
+            if (r < n_total) {
+                sv = sc[j * T + r];
+                if constexpr (I8) sv *= reinterpret_cast<const float*>(st + 2 * TILE)[r];
+            }
+            float tmax = sv;
+#pragma unroll
+            for (int mm = T / 2; mm >= 1; mm >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, mm));
+            const float mnew = fmaxf(m[j], tmax);
+            alpha[j] = exp2f(m[j] - mnew);
+            const float pv = exp2f(sv - mnew);
+            float tsum = pv;
+#pragma unroll
+            for (int mm = T / 2; mm >= 1; mm >>= 1) tsum += __shfl_xor_sync(FULL, tsum, mm);
+            l[j] = l[j] * alpha[j] + tsum;
+            m[j] = mnew;
+            if (lane < T) {
+                float wgt = pv;
+                if constexpr (I8) wgt = r < n_total ? pv * reinterpret_cast<const float*>(st + 2 * TILE + SCL)[r] : 0.f;
+                pb[j * T + r] = wgt;
+            }
+        }
+        __syncwarp();
+
+        // ---- o = alpha * o + sum_rows p * v ----
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[j][e] *= alpha[j];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int row = 2 * i + hr;
+            if (row < n_total) {
+                float vf[EPL];
+                ld_cvt<CT, EPL>(Vt + row * ROW + c * EPL * EB, vf);
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const float pj = pb[j * T + row];
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pj, vf[e], o[j][e]);
+                }
+            }
+        }
+        __syncwarp();
+
+        // ---- refill this stage with the tile SPW ahead ----
+        if (k + SPW < n_my) {
+            if (lane == 0) issue(s, ci);
+            if (k + SPW + 1 < n_my) advance(ci, P, segs);
+        }
+
+        // ---- end of a piece: final output, or partial + merge by the last arrival ----
+        if (last_tile || k == n_my - 1) {
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[j][e] += __shfl_xor_sync(FULL, o[j][e], 16);
+            const int segg = cc.b * segs + cc.seg;
+            if (piece_first == 0 && last_tile) {
+                if (hr == 0) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const int h = kvh * p.group + hb * G + j;
+                        const float inv = 1.f / l[j];
+                        float* dst = p.out + (static_cast<size_t>(cc.b) * p.Hq + h) * D + c * EPL;
+#pragma unroll
+                        for (int e4 = 0; e4 < EPL / 4; ++e4)
+                            reinterpret_cast<float4*>(dst)[e4] =
+                                make_float4(o[j][4 * e4] * inv, o[j][4 * e4 + 1] * inv, o[j][4 * e4 + 2] * inv,
+                                            o[j][4 * e4 + 3] * inv);
+                    }
+                }
+            } else {
+                float* slot = p.ws + static_cast<size_t>(segg + wid) * TL::SLOT;
+                if (lane == 0) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        slot[j] = m[j];
+                        slot[G + j] = l[j];
+                    }
+                }
+                if (hr == 0) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        float* dst = slot + TL::OOFF + j * D + c * EPL;
+#pragma unroll
+                        for (int e4 = 0; e4 < EPL / 4; ++e4)
+                            reinterpret_cast<float4*>(dst)[e4] =
+                                make_float4(o[j][4 * e4], o[j][4 * e4 + 1], o[j][4 * e4 + 2], o[j][4 * e4 + 3]);
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                // The counter accumulates tiles, not pieces: when U < W some
+                // workers own no tile, so the number of pieces is not wf..wl.
+                const uint32_t piece_tiles = static_cast<uint32_t>(cc.tile - piece_first + 1);
+                uint32_t prev = 0;
+                if (lane == 0) prev = atomicAdd(&p.counters[segg], piece_tiles);
+                prev = __shfl_sync(FULL, prev, 0);
+                if (prev + piece_tiles == static_cast<uint32_t>(cc.nt)) {
+                    // last piece of this segment: log-sum-exp merge of all partials
+                    __threadfence();
+                    const long long S0 = P[cc.b] + static_cast<long long>(cc.seg) * cc.nt;
+                    const int wf = worker_of(S0, U, W);
+                    const int wl = worker_of(S0 + cc.nt - 1, U, W);
+                    auto has_piece = [&](int w) { return (w * U) / W < ((w + 1) * U) / W; };
+                    constexpr int DL = D / 32;
+#pragma unroll 1
+                    for (int j = 0; j < G; ++j) {
+                        float mx = -INFINITY;
+                        for (int w = wf + lane; w <= wl; w += 32)
+                            if (has_piece(w)) mx = fmaxf(mx, __ldcg(p.ws + static_cast<size_t>(segg + w) * TL::SLOT + j));
+                        mx = warp_max(mx);
+                        float lsum = 0.f, acc[DL];
+#pragma unroll
+                        for (int e = 0; e < DL; ++e) acc[e] = 0.f;
+                        for (int w = wf; w <= wl; ++w) {
+                            if (!has_piece(w)) continue;
+                            const float* sl = p.ws + static_cast<size_t>(segg + w) * TL::SLOT;
+                            const float f = exp2f(__ldcg(sl + j) - mx);
+                            lsum += f * __ldcg(sl + G + j);
+                            const float* ov = sl + TL::OOFF + j * D + lane * DL;
+                            if constexpr (DL == 4) {
+                                const float4 u = __ldcg(reinterpret_cast<const float4*>(ov));
+                                acc[0] += f * u.x; acc[1] += f * u.y; acc[2] += f * u.z; acc[3] += f * u.w;
+                            } else {
+                                const float2 u = __ldcg(reinterpret_cast<const float2*>(ov));
+                                acc[0] += f * u.x; acc[1] += f * u.y;
+                            }
+                        }
+                        const int h = kvh * p.group + hb * G + j;
+                        float* dst = p.out + (static_cast<size_t>(cc.b) * p.Hq + h) * D + lane * DL;
+                        const float inv = 1.f / lsum;
+#pragma unroll
+                        for (int e = 0; e < DL; ++e) dst[e] = acc[e] * inv;
+                    }
+                    if (lane == 0) p.counters[segg] = 0u;
+                }
+            }
+            if (k + 1 < n_my) {
+                advance(cc, P, segs);
+                begin_segment(cc);
+                piece_first = cc.tile;
+            }
+        } else {
+            advance(cc, P, segs);
+        }
+    }
+
+    if (k < n_my) {
+        // A copy did not arrive in time: the error bit is set.  Wait (bounded)
+        // for the copies this warp still has in flight before leaving, so no
+        // transfer lands in shared memory after the block has exited.
+        const int last_issued = min(n_my, k + SPW) - 1;
+        for (int kk = k; kk <= last_issued; ++kk)
+            mbar_wait_bounded(smem_addr(&bars[kk % SPW]), static_cast<uint32_t>((kk / SPW) & 1), p.err);
+    }
+}
+
+// ---------------------------------------------------------- host selection
+struct KernelInfo {
+    const void* fn;
+    int smem;
+    int T;
+    int slot_floats;
+    int G;
+};
+
+template <typename CT, int D, int G>
+KernelInfo kernel_info() {
+    using TL = Tiling<CT, D, G>;
+    return KernelInfo{reinterpret_cast<const void*>(&decode_splitk_kernel<CT, D, G>), TL::SMEM, TL::T, TL::SLOT, G};
+}
+
+template <typename CT>
+KernelInfo select_kernel(int D, int G) {
+    if (D == 64) {
+        switch (G) {
+            case 1: return kernel_info<CT, 64, 1>();
+            case 2: return kernel_info<CT, 64, 2>();
+            case 4: return kernel_info<CT, 64, 4>();
+            case 8: return kernel_info<CT, 64, 8>();
+        }
+    } else if (D == 128) {
+        switch (G) {
+            case 1: return kernel_info<CT, 128, 1>();
+            case 2: return kernel_info<CT, 128, 2>();
+            case 4: return kernel_info<CT, 128, 4>();
+            case 8: return kernel_info<CT, 128, 8>();
+        }
+    }
+    return KernelInfo{nullptr, 0, 0, 0, 0};
+}
+
+KernelInfo select_f32(int D, int G);
+KernelInfo select_f16(int D, int G);
+KernelInfo select_bf16(int D, int G);
+KernelInfo select_i8(int D, int G);
+
+}  // namespace ftd

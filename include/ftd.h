@@ -1,0 +1,168 @@
+/*
+ * ftd.h -- C ABI of the GB300 masked multi-head attention decode step.
+ *
+ * One call performs one decode step of masked multi-head attention for every
+ * slot of a continuous batch, entirely in hand-written sm_103a kernels:
+ *
+ *   1. fused QKV bias add           q' = q + b_q, k' = k_new + b_k, v' = v_new + b_v
+ *                                   (FasterTransformer practice notes, lpnh.cn,
+ *                                   section 2.1: the projection output is split
+ *                                   into Q/K/V and the bias is added in the fused
+ *                                   attention kernel, with no extra HBM round trip)
+ *   2. KV-cache append              K[b, h, L_b, :] = round(k'), V likewise
+ *                                   (lpnh.cn section 2.2: a pre-allocated cache the
+ *                                   new K/V is appended to at every token;
+ *                                   "FasterTransformer source analysis",
+ *                                   framerc.cn, section 3.2: one buffer sized for
+ *                                   the preset maximum length, shared by offset)
+ *   3. scores over the whole cache  s_t = scale * q' . K[t],  t = 0 .. L_b
+ *   4. masked, stable softmax       p = softmax(s) over t <= L_b (the current
+ *                                   position; nothing after it is visible)
+ *   5. weighted sum                 o = sum_t p_t V[t]
+ *   6. split-K merge                partial (max, sum, o) of several thread
+ *                                   blocks combined by log-sum-exp ("10 tricks
+ *                                   for Transformer throughput", pptc.cn,
+ *                                   section 2.2: online softmax statistics, no
+ *                                   N x N matrix in memory)
+ *
+ * with ragged per-slot lengths (intelliparadigm.com section 3.2, continuous
+ * batching), grouped / multi-query heads (pptc.cn section 3.4: query head h
+ * reads kv head h / (Hq / Hkv)) and an INT8 cache with an fp32 scale per
+ * (slot, kv head, position) (pptc.cn section 3.1).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - B = max_batch, Hq = n_q_heads, Hkv = n_kv_heads, D = head_dim,
+ *    Lmax = max_len.  L_b = seq_lens[b] is the number of tokens already in
+ *    the cache for slot b; the new token is written at position L_b and
+ *    attends to positions 0 .. L_b inclusive.
+ *  - Layouts are dense and row-major:
+ *        q      [B][Hq][D]        qkv dtype
+ *        k_new  [B][Hkv][D]       qkv dtype      v_new likewise
+ *        bias   [(Hq + 2*Hkv)*D]  qkv dtype, the q part, then k, then v
+ *        cache  [B][Hkv][Lmax][D] cache dtype    (k_cache, v_cache)
+ *        scales [2][B][Hkv][Lmax] fp32, plane 0 for K and plane 1 for V
+ *                                 (INT8 caches only)
+ *        out    [B][Hq][D]        fp32
+ *  - Slots with seq_lens[b] < 0 are inactive: their cache is untouched and
+ *    their output is zero.  seq_lens[b] >= Lmax is an overflow: the slot is
+ *    skipped the same way and a sticky device error is raised, which
+ *    ftd_get_error() reports as FTD_ERR_SEQ_OVERFLOW.  Nothing traps.
+ *  - Device pointers must be 16-byte aligned.  All device work goes to the
+ *    caller's stream (a cudaStream_t passed as void*; NULL = legacy default
+ *    stream) and is asynchronous; the decode entry points never allocate.
+ *  - The caller advances seq_lens after a step; the library never writes it.
+ *  - Errors found on the host return synchronously and leave the device
+ *    untouched.  ftd_last_error() describes the most recent one.
+ */
+#ifndef FTD_H
+#define FTD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FTD_OK = 0,
+    FTD_ERR_INVALID_ARG = 1,     /* null pointer, bad size, misaligned pointer */
+    FTD_ERR_UNSUPPORTED = 2,     /* dtype / head_dim combination not built */
+    FTD_ERR_OOM = 3,             /* ftd_init could not allocate its pool */
+    FTD_ERR_CUDA = 4,            /* a CUDA runtime call failed */
+    FTD_ERR_SEQ_OVERFLOW = 5,    /* some seq_lens[b] >= max_len in a past call */
+    FTD_ERR_DEVICE_TIMEOUT = 6   /* a kernel gave up waiting for a copy (bounded wait) */
+} ftd_status;
+
+typedef enum { FTD_F32 = 0, FTD_F16 = 1, FTD_BF16 = 2, FTD_I8 = 3 } ftd_dtype;
+
+typedef struct {
+    int max_batch;       /* B, 1 .. 1024 */
+    int n_q_heads;       /* Hq, a multiple of n_kv_heads */
+    int n_kv_heads;      /* Hkv >= 1 (Hkv == Hq: MHA, Hkv == 1: MQA) */
+    int head_dim;        /* D: 64 or 128 */
+    int max_len;         /* Lmax: a multiple of 16 */
+    ftd_dtype qkv_dtype;   /* q, k_new, v_new, bias: F32, F16 or BF16 */
+    ftd_dtype cache_dtype; /* F32, F16, BF16 or I8 */
+    float softmax_scale;   /* 0 selects 1/sqrt(head_dim) */
+} ftd_config;
+
+typedef struct ftd_ctx ftd_ctx;
+
+/*
+ * ftd_init -- validate cfg and pre-allocate the cache pool.
+ * One cudaMalloc on the current device holds the K and V caches (zeroed),
+ * the INT8 scale planes, the split-K workspace, the sticky error word and the
+ * staging buffers of ftd_decode_mha_host.  Zeroing runs on `stream`.
+ * The pool is the pre-allocated buffer of framerc.cn section 3.2 (allocated
+ * once for max_batch x max_len, requests share it by offset, no resize).
+ * On success *out owns the pool until ftd_destroy.  Returns INVALID_ARG,
+ * UNSUPPORTED, OOM or CUDA on failure, with *out set to NULL.
+ */
+ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out);
+
+/*
+ * ftd_cache_ptrs -- device addresses of the context's own pool.
+ * Any output pointer may be NULL.  *scales is NULL unless the cache is INT8.
+ * The caller may fill the cache (prefill) through these pointers.
+ */
+ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** scales);
+
+/*
+ * ftd_decode_mha -- one decode step for all max_batch slots (device buffers).
+ *   q, k_new, v_new : device, caller-owned, qkv dtype, layouts above.
+ *   qkv_bias        : device or NULL (no bias).
+ *   k_cache, v_cache: device caches with the layout above, read and appended
+ *                     to in place; NULL selects the context's own pool.
+ *   seq_lens        : device int32 [B]; read only.
+ *   scales          : device fp32 [2][B][Hkv][Lmax] for INT8 caches (NULL
+ *                     selects the pool's planes); ignored otherwise.
+ *   out             : device fp32 [B][Hq][D]; every element is written.
+ *   stream          : cudaStream_t as void*.
+ * Launches one kernel; no host synchronisation and no allocation.  Two calls
+ * on the same context must not overlap in time (they share the workspace):
+ * issue them on one stream, or order their streams with events.
+ */
+ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                          const void* qkv_bias, void* k_cache, void* v_cache,
+                          const int32_t* seq_lens, float* scales, float* out, void* stream);
+
+/*
+ * ftd_decode_mha_host -- the same step for callers whose per-step inputs live
+ * in host memory.  q, k_new, v_new, qkv_bias (nullable), seq_lens and out are
+ * HOST pointers (pinned memory makes the copies asynchronous and faster); the
+ * caches stay on the device as in ftd_decode_mha (NULL = the pool).  The
+ * inputs are copied into the pool's staging buffers on `stream`, the kernel
+ * runs, out is copied back, and the call synchronises `stream` before it
+ * returns, so out is valid on return.
+ */
+ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                               const void* qkv_bias, void* k_cache, void* v_cache,
+                               const int32_t* seq_lens, float* scales, float* out, void* stream);
+
+/*
+ * ftd_get_error -- synchronise the stream of the context's last call, then
+ * read and clear the sticky device error word.  Returns FTD_OK,
+ * FTD_ERR_SEQ_OVERFLOW, FTD_ERR_DEVICE_TIMEOUT or FTD_ERR_CUDA.
+ */
+ftd_status ftd_get_error(ftd_ctx* ctx);
+
+/* ftd_destroy -- free the pool (synchronises the device first).  NULL is a no-op. */
+void ftd_destroy(ftd_ctx* ctx);
+
+/* ftd_status_str -- static name of a status code. */
+const char* ftd_status_str(ftd_status s);
+
+/* ftd_last_error -- text of the most recent host-side error in this thread ("" if none). */
+const char* ftd_last_error(void);
+
+/* ftd_kernel_launches -- number of kernels this library has launched in this
+ * process (every decode call adds one; host-side failures add none). */
+uint64_t ftd_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FTD_H */

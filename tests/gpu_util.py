@@ -1,0 +1,105 @@
+"""Helpers for the GPU parity tests: move seeded inputs to the device, run one
+step through the C ABI, compare with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+import decode_step_masked_gb300 as ftd
+from synthetic import gen_cache_slot, gen_scales_slot
+
+# Parity bars: fp32/fp16/bf16 caches with fp32 accumulation, and INT8 caches
+# against the oracle run on the dequantised values.
+TOL_MAXABS = 2e-3
+TOL_RELL2 = 1e-3
+TOL_MAXABS_I8 = 1e-2
+
+
+def dev(a):
+    import torch
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    return torch.from_numpy(a).cuda()
+
+
+def host(t, like):
+    a = t.cpu().numpy()
+    return a.view(like.dtype) if a.dtype != like.dtype else a
+
+
+def run_step(w, inp, step=None, softmax_scale=0.0, use_bias=True):
+    """One decode step on the GPU with caller-owned device buffers."""
+    import torch
+    own = step is None
+    if own:
+        step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, softmax_scale)
+    q, kn, vn = dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"])
+    bias = dev(inp["bias"]) if (use_bias and inp.get("bias") is not None) else None
+    kc, vc, sl = dev(inp["k_cache"]), dev(inp["v_cache"]), dev(inp["seq_lens"])
+    sc = dev(inp["scales"]) if inp.get("scales") is not None else None
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
+    step(q, kn, vn, sl, out, bias=bias, k_cache=kc, v_cache=vc, scales=sc)
+    torch.cuda.synchronize()
+    status = step.get_error()
+    res = dict(out=out.cpu().numpy().astype(np.float64), k_cache=host(kc, inp["k_cache"]),
+               v_cache=host(vc, inp["v_cache"]), scales=None if sc is None else sc.cpu().numpy(),
+               status=status)
+    if own:
+        step.close()
+    return res
+
+
+def assert_close(got, ref, i8=False, what=""):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    if i8:
+        assert err <= TOL_MAXABS_I8, f"{what}: max-abs {err:.3e} > {TOL_MAXABS_I8}"
+        return err, None
+    nref = float(np.linalg.norm(ref))
+    rel = float(np.linalg.norm(got - ref) / nref) if nref > 0 else float(np.linalg.norm(got))
+    assert err <= TOL_MAXABS, f"{what}: max-abs {err:.3e} > {TOL_MAXABS}"
+    assert rel <= TOL_RELL2, f"{what}: rel-L2 {rel:.3e} > {TOL_RELL2}"
+    return err, rel
+
+
+def assert_same_bytes(a, b, what):
+    a = np.ascontiguousarray(a)
+    b = np.ascontiguousarray(b)
+    assert a.shape == b.shape and a.dtype.itemsize == b.dtype.itemsize, what
+    diff = np.nonzero(a.reshape(-1).view(np.uint8) != b.reshape(-1).view(np.uint8))[0]
+    if diff.size:
+        first = np.unravel_index(diff[0] // a.dtype.itemsize, a.shape)
+        raise AssertionError(f"{what}: {diff.size} bytes differ, first at element {tuple(int(i) for i in first)}")
+
+
+class _CudaArray:
+    """Wraps a raw device address so torch can view it (CUDA array interface)."""
+
+    def __init__(self, ptr, shape, typestr):
+        self.__cuda_array_interface__ = {"shape": tuple(int(x) for x in shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+def device_view(ptr, shape, np_dtype):
+    """torch tensor aliasing library-owned device memory at ``ptr``."""
+    import torch
+    return torch.as_tensor(_CudaArray(ptr, shape, np.dtype(np_dtype).str), device="cuda")
+
+
+def fill_device_cache(w, seed, lens, which, fill_beyond="nan"):
+    """Device cache [B,Hkv,Lmax,D] filled slot by slot from the seeded generator."""
+    import torch
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.int16, "i8": torch.int8}[w.cache_dtype]
+    t = torch.empty((w.B, w.Hkv, w.Lmax, w.D), dtype=dt, device="cuda")
+    for b in range(w.B):
+        t[b].copy_(dev(gen_cache_slot(w, seed, which, b, int(lens[b]), fill_beyond)))
+    return t
+
+
+def fill_device_scales(w, seed, lens, fill_beyond="nan"):
+    import torch
+    t = torch.empty((2, w.B, w.Hkv, w.Lmax), dtype=torch.float32, device="cuda")
+    for b in range(w.B):
+        t[0, b].copy_(dev(gen_scales_slot(w, seed, "k", b, int(lens[b]), fill_beyond)))
+        t[1, b].copy_(dev(gen_scales_slot(w, seed, "v", b, int(lens[b]), fill_beyond)))
+    return t

@@ -1,0 +1,94 @@
+"""The C ABI on the host: the library loads, exports what include/ftd.h declares,
+and rejects bad arguments synchronously without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import decode_step_masked_gb300 as ftd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ftd.build_library()
+    return ftd.load_library()
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "ftd.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ftd_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9, names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ftd.h but not exported"
+    assert set(names) == set(ftd.EXPORTS)
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "FTD_OK"), (1, "FTD_ERR_INVALID_ARG"), (2, "FTD_ERR_UNSUPPORTED"),
+                       (3, "FTD_ERR_OOM"), (4, "FTD_ERR_CUDA"), (5, "FTD_ERR_SEQ_OVERFLOW"),
+                       (6, "FTD_ERR_DEVICE_TIMEOUT")]:
+        assert ftd.ftd_status_str(code) == name
+    assert ftd.ftd_status_str(99) == "FTD_ERR_UNKNOWN"
+
+
+def cfg(**kw):
+    base = dict(max_batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, max_len=256,
+                qkv_dtype=ftd.FTD_BF16, cache_dtype=ftd.FTD_BF16, softmax_scale=0.0)
+    base.update(kw)
+    return ftd.FtdConfig(*[base[f] for f, _ in ftd.FtdConfig._fields_])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(max_batch=0), ftd.FTD_ERR_INVALID_ARG),
+    (dict(max_batch=1025), ftd.FTD_ERR_INVALID_ARG),
+    (dict(n_kv_heads=0), ftd.FTD_ERR_INVALID_ARG),
+    (dict(n_q_heads=6, n_kv_heads=4), ftd.FTD_ERR_INVALID_ARG),
+    (dict(n_q_heads=2, n_kv_heads=4), ftd.FTD_ERR_INVALID_ARG),
+    (dict(max_len=0), ftd.FTD_ERR_INVALID_ARG),
+    (dict(max_len=100), ftd.FTD_ERR_INVALID_ARG),
+    (dict(head_dim=0), ftd.FTD_ERR_INVALID_ARG),
+    (dict(head_dim=96), ftd.FTD_ERR_UNSUPPORTED),
+    (dict(qkv_dtype=ftd.FTD_I8), ftd.FTD_ERR_UNSUPPORTED),
+    (dict(cache_dtype=7), ftd.FTD_ERR_UNSUPPORTED),
+    (dict(softmax_scale=-1.0), ftd.FTD_ERR_INVALID_ARG),
+    (dict(softmax_scale=float("nan")), ftd.FTD_ERR_INVALID_ARG),
+    (dict(softmax_scale=float("inf")), ftd.FTD_ERR_INVALID_ARG),
+])
+def test_init_rejects_bad_config(lib, kw, status):
+    st, ctx = ftd.ftd_init(cfg(**kw))
+    assert st == status, (ftd.ftd_status_str(st), ftd.ftd_last_error())
+    assert ctx is None
+    assert ftd.ftd_last_error() != ""
+
+
+def test_null_arguments(lib):
+    assert lib.ftd_init(None, None, None) == ftd.FTD_ERR_INVALID_ARG
+    out = ctypes.c_void_p(1234)
+    assert lib.ftd_init(None, None, ctypes.byref(out)) == ftd.FTD_ERR_INVALID_ARG
+    assert out.value is None, "ftd_init must clear *out on failure"
+    assert ftd.ftd_decode_mha(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
+    assert ftd.ftd_decode_mha_host(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
+    assert ftd.ftd_get_error(0) == ftd.FTD_ERR_INVALID_ARG
+    assert ftd.ftd_cache_ptrs(0)[0] == ftd.FTD_ERR_INVALID_ARG
+    ftd.ftd_destroy(0)  # no-op
+
+
+def test_no_launches_from_host_failures(lib):
+    n = ftd.ftd_kernel_launches()
+    ftd.ftd_init(cfg(max_batch=0))
+    ftd.ftd_decode_mha(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0)
+    assert ftd.ftd_kernel_launches() == n
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(FileNotFoundError, match="no fallback"):
+        ftd.load_library(str(tmp_path / "libftd.so"))

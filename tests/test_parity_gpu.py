@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA decode step against the float64 oracle on the same seeded inputs.
+
+Append is compared bit for bit (caches and INT8 scales); attention outputs
+within max-abs 2e-3 and relative L2 1e-3 (fp32/fp16/bf16 caches) or max-abs
+1e-2 (INT8 cache, oracle on the dequantised values).
+"""
+import numpy as np
+import pytest
+
+import decode_step_masked_gb300 as ftd
+import oracle
+from synthetic import WORKLOADS, Workload, gen_all, gen_qkv, gen_seq_lens
+from tests.gpu_util import (assert_close, assert_same_bytes, dev, device_view, fill_device_cache,
+                            fill_device_scales, run_step)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    ftd.build_library()
+    ftd.load_library()
+
+
+def small(cache, qkv, B, Hq, Hkv, D, Lmax, lens, bias=0.1, seed=11):
+    w = Workload("case", B=B, Hq=Hq, Hkv=Hkv, D=D, Lmax=Lmax, qkv_dtype=qkv, cache_dtype=cache,
+                 bias_std=bias, seed=seed)
+    return w, gen_all(w, seed=seed, seq_lens=np.array(lens, np.int32), fill_beyond="nan")
+
+
+def check_step(w, inp, softmax_scale=0.0, use_bias=True, what=""):
+    o = oracle.load()
+    ref_inp = dict(inp)
+    if not use_bias:
+        ref_inp["bias"] = None
+    ref = o.decode_step(w, ref_inp, softmax_scale=softmax_scale)
+    got = run_step(w, inp, softmax_scale=softmax_scale, use_bias=use_bias)
+    assert_same_bytes(got["k_cache"], ref["k_cache"], f"{what} K cache after append")
+    assert_same_bytes(got["v_cache"], ref["v_cache"], f"{what} V cache after append")
+    if w.cache_dtype == "i8":
+        assert_same_bytes(got["scales"], ref["scales"], f"{what} INT8 scales after append")
+    assert_close(got["out"], ref["out"], i8=w.cache_dtype == "i8", what=what)
+    want = ftd.FTD_ERR_SEQ_OVERFLOW if ref["overflow"] else ftd.FTD_OK
+    assert got["status"] == want, (ftd.ftd_status_str(got["status"]), what)
+    return got, ref
+
+
+def test_tiny_workload():
+    w = WORKLOADS["tiny"]
+    check_step(w, gen_all(w), what="tiny")
+
+
+LENS = [0, 1, 15, 16, 17, 100, 255, 300]  # ctx 1, tile edges, ragged tails
+
+
+@pytest.mark.parametrize("cache", ["f32", "f16", "bf16", "i8"])
+@pytest.mark.parametrize("qkv", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_dtype_grid(cache, qkv, D):
+    w, inp = small(cache, qkv, B=len(LENS), Hq=4, Hkv=4, D=D, Lmax=304, lens=LENS)
+    check_step(w, inp, what=f"{cache}/{qkv}/D{D}")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (16, 2), (32, 1), (24, 8), (12, 2)])
+@pytest.mark.parametrize("cache", ["bf16", "f16", "i8"])
+def test_gqa_mqa(Hq, Hkv, cache):
+    qkv = "f16" if cache == "i8" else cache
+    w, inp = small(cache, qkv, B=3, Hq=Hq, Hkv=Hkv, D=128, Lmax=512, lens=[511, 37, 200])
+    check_step(w, inp, what=f"gqa {Hq}/{Hkv} {cache}")
+
+
+def test_inactive_and_overflow_slots():
+    w, inp = small("bf16", "bf16", B=6, Hq=4, Hkv=2, D=128, Lmax=128, lens=[-1, 127, 128, 5, 1000, -7])
+    got, ref = check_step(w, inp, what="inactive/overflow")
+    assert not got["out"][[0, 2, 4, 5]].any(), "inactive and overflowing slots must be zero"
+    assert got["status"] == ftd.FTD_ERR_SEQ_OVERFLOW
+
+
+def test_error_is_sticky_then_cleared():
+    import torch
+    w, inp = small("bf16", "bf16", B=2, Hq=2, Hkv=2, D=64, Lmax=32, lens=[32, 3])
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    run_step(w, inp, step=step)  # reads and clears the overflow
+    assert step.get_error() == ftd.FTD_OK
+    inp2 = dict(inp, seq_lens=np.array([3, 4], np.int32))
+    assert run_step(w, inp2, step=step)["status"] == ftd.FTD_OK
+    step.close()
+    torch.cuda.synchronize()
+
+
+def test_all_inactive():
+    w, inp = small("f16", "f16", B=4, Hq=4, Hkv=4, D=128, Lmax=64, lens=[-1, -1, -1, -1])
+    got, _ = check_step(w, inp, what="all inactive")
+    assert not got["out"].any()
+
+
+def test_no_bias_and_custom_scale():
+    w, inp = small("bf16", "f32", B=3, Hq=8, Hkv=2, D=128, Lmax=256, lens=[200, 9, 255])
+    check_step(w, inp, use_bias=False, what="no bias")
+    check_step(w, inp, softmax_scale=0.37, what="scale 0.37")
+
+
+def test_one_long_sequence_split_across_many_workers():
+    # one segment spread over hundreds of warps: exercises the log-sum-exp merge
+    w, inp = small("bf16", "bf16", B=1, Hq=1, Hkv=1, D=128, Lmax=16384, lens=[16000], bias=None)
+    check_step(w, inp, what="one long sequence")
+
+
+def test_many_short_segments_per_worker():
+    rng = np.random.default_rng(5)
+    lens = rng.integers(0, 40, 64)
+    w, inp = small("f16", "f16", B=64, Hq=32, Hkv=32, D=128, Lmax=48, lens=lens)
+    check_step(w, inp, what="many short segments")
+
+
+def test_large_scores_stay_finite():
+    w, inp = small("f32", "f32", B=2, Hq=4, Hkv=4, D=64, Lmax=512, lens=[400, 77], bias=None)
+    inp = dict(inp, q=(inp["q"] * np.float32(40.0)).astype(np.float32))
+    check_step(w, inp, what="large scores")
+
+
+def test_consecutive_steps_continue_the_sequence():
+    """Two decode steps in a row on one context: the second sees the first's append."""
+    import torch
+    w, inp = small("bf16", "bf16", B=4, Hq=8, Hkv=4, D=128, Lmax=256, lens=[10, 100, 250, 0])
+    o = oracle.load()
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    q, kn, vn, bias = dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"]), dev(inp["bias"])
+    kc, vc = dev(inp["k_cache"]), dev(inp["v_cache"])
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    ref_inp = dict(inp)
+    lens = inp["seq_lens"].copy()
+    for it in range(3):
+        step(q, kn, vn, dev(lens), out, bias=bias, k_cache=kc, v_cache=vc)
+        ref = o.decode_step(w, dict(ref_inp, seq_lens=lens))
+        torch.cuda.synchronize()
+        assert_close(out.cpu().numpy().astype(np.float64), ref["out"], what=f"step {it}")
+        assert_same_bytes(kc.cpu().numpy().view(np.uint16), ref["k_cache"], f"K after step {it}")
+        ref_inp = dict(ref_inp, k_cache=ref["k_cache"], v_cache=ref["v_cache"])
+        lens = lens + 1
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+
+
+def test_pool_pointers_and_host_entry_point():
+    """NULL caches select the context's own pool; the host-buffer entry point gives the same result."""
+    import torch
+    w, inp = small("i8", "f16", B=3, Hq=4, Hkv=2, D=128, Lmax=96, lens=[95, 20, 63])
+    ref = oracle.load().decode_step(w, inp)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    kp, vp, sp = step.cache_ptrs()
+    assert kp and vp and sp
+    kview = device_view(kp, inp["k_cache"].shape, np.int8)
+    vview = device_view(vp, inp["v_cache"].shape, np.int8)
+    sview = device_view(sp, inp["scales"].shape, np.float32)
+    kview.copy_(dev(inp["k_cache"]))
+    vview.copy_(dev(inp["v_cache"]))
+    sview.copy_(dev(inp["scales"]))
+    torch.cuda.synchronize()
+    host = {k: np.ascontiguousarray(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens")}
+    out = np.zeros((w.B, w.Hq, w.D), np.float32)
+    s = torch.cuda.current_stream().cuda_stream
+    st = ftd.ftd_decode_mha_host(step.ctx, host["q"].ctypes.data, host["k_new"].ctypes.data,
+                                 host["v_new"].ctypes.data, host["bias"].ctypes.data, 0, 0,
+                                 host["seq_lens"].ctypes.data, 0, out.ctypes.data, s)
+    ftd.check(st)
+    assert_close(out.astype(np.float64), ref["out"], i8=True, what="host entry point / pool")
+    assert_same_bytes(kview.cpu().numpy(), ref["k_cache"], "pool K after append")
+    assert_same_bytes(sview.cpu().numpy(), ref["scales"], "pool scales after append")
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+
+
+# ------------------------------------------------------------- full size
+SAMPLED = {"7b": [(0, 0), (3, 17), (7, 31)], "13b": [(0, 5), (11, 39), (31, 0), (17, 22)],
+           "70b": [(0, 0), (5, 37), (15, 63)], "int8": [(0, 1), (33, 30), (63, 31)]}
+
+
+@pytest.mark.parametrize("name", ["7b", "13b", "70b", "int8"])
+def test_full_size_workload_sampled(name):
+    """Full-size workloads in the launch configuration the bench times; the oracle checks
+    sampled (slot, head) outputs one slot at a time, and every appended row bit for bit."""
+    import torch
+    w = WORKLOADS[name]
+    lens = gen_seq_lens(w)
+    q, kn, vn, bias = gen_qkv(w)
+    kc = fill_device_cache(w, w.seed, lens, "k")
+    vc = fill_device_cache(w, w.seed, lens, "v")
+    sc = fill_device_scales(w, w.seed, lens) if w.cache_dtype == "i8" else None
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device="cuda")
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    step(dev(q), dev(kn), dev(vn), dev(lens), out, bias=None if bias is None else dev(bias),
+         k_cache=kc, v_cache=vc, scales=sc)
+    torch.cuda.synchronize()
+    assert step.get_error() == ftd.FTD_OK
+    got = out.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    o = oracle.load()
+    idx = torch.arange(w.B, device="cuda")
+    pos = torch.from_numpy(lens.astype(np.int64)).cuda()
+    k_rows = kc[idx, :, pos, :].cpu().numpy()      # [B, Hkv, D]
+    v_rows = vc[idx, :, pos, :].cpu().numpy()
+    slots = sorted({b for b, _ in SAMPLED[name]})
+    w1 = w.with_(B=1)
+    for b in slots:
+        from synthetic import gen_cache_slot, gen_scales_slot
+        sub = dict(q=q[b:b + 1], k_new=kn[b:b + 1], v_new=vn[b:b + 1], bias=bias,
+                   k_cache=gen_cache_slot(w, w.seed, "k", b, lens[b])[None],
+                   v_cache=gen_cache_slot(w, w.seed, "v", b, lens[b])[None],
+                   seq_lens=lens[b:b + 1], scales=None)
+        if w.cache_dtype == "i8":
+            sub["scales"] = np.stack([gen_scales_slot(w, w.seed, "k", b, lens[b])[None],
+                                      gen_scales_slot(w, w.seed, "v", b, lens[b])[None]])
+        ref = o.decode_step(w1, sub, nthreads=8)
+        L = int(lens[b])
+        assert_same_bytes(k_rows[b], ref["k_cache"][0, :, L, :].view(k_rows.dtype), f"{name} K row slot {b}")
+        assert_same_bytes(v_rows[b], ref["v_cache"][0, :, L, :].view(v_rows.dtype), f"{name} V row slot {b}")
+        heads = [h for bb, h in SAMPLED[name] if bb == b]
+        assert_close(got[b, heads], ref["out"][0, heads], i8=w.cache_dtype == "i8", what=f"{name} slot {b}")
+    step.close()
