@@ -1,0 +1,520 @@
+"""Benchmark of the decode step: KV-read GB/s (fraction of HBM peak) and µs per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 7b|13b|70b|int8|tiny]
+    python bench.py --impl reference ...   # the float64 CPU oracle as the reference arm
+
+One step is one ``ftd_decode_mha`` call: bias add, KV append, scores, softmax,
+P.V and the split-K merge for every slot of the batch.  Inputs are synthetic
+(seeded, the workload shapes of the decode step's pages) and resident in HBM
+before timing starts.  Consecutive steps rotate between cache pools whose
+combined size is several times the 129 MB L2, so each step streams its KV
+cache from HBM.  Rank 0 prints one JSON line.
+
+With ``--gpus N`` under torchrun every rank runs an independent replica (its
+own batch; the decode step needs no collective), ``value`` is the aggregate of
+all ranks over the slowest rank's time and ``scaling`` is "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synthetic import WORKLOADS, gen_seq_lens  # noqa: E402
+
+METRIC = "decode-attention KV-read GB/s (frac of 8 TB/s HBM); µs per decode step"
+EB = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
+                  "decode_step_masked_gb300/csrc/ftd_decode_splitk.cuh")
+
+
+# ---------------------------------------------------------------- workload
+def step_bytes(w, lens) -> dict:
+    """Algorithmic bytes of one step: each cached K/V row once per kv head."""
+    lens = np.asarray(lens, np.int64)
+    act = (lens >= 0) & (lens < w.Lmax)
+    ctx = int((lens[act] + 1).sum())
+    nact = int(act.sum())
+    eb = EB[w.cache_dtype]
+    qeb = EB[w.qkv_dtype]
+    kv_read = 2 * w.Hkv * w.D * eb * int(lens[act].sum())
+    kv_write = 2 * w.Hkv * w.D * eb * nact
+    scale_rw = 8 * w.Hkv * ctx if w.cache_dtype == "i8" else 0
+    small = (w.B * w.Hq * w.D + 2 * w.B * w.Hkv * w.D) * qeb + 4 * w.B + 4 * w.B * w.Hq * w.D
+    return dict(kv=kv_read + kv_write + scale_rw, total=kv_read + kv_write + scale_rw + small, ctx=ctx)
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured")
+    return dict(hbm_gbs=FALLBACK_HBM_GBS, source="fallback")
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- device
+def make_pools(w, npools, seed, device):
+    """Seeded synthetic caches drawn on the device (same distributions as the parity inputs)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    pools = []
+    shape = (w.B, w.Hkv, w.Lmax, w.D)
+    for _ in range(npools):
+        if w.cache_dtype == "i8":
+            lo, hi = w.scale_range
+            sc = torch.rand((2, w.B, w.Hkv, w.Lmax), device=device, generator=g) * (hi - lo) + lo
+            kc = torch.clamp(torch.round(torch.randn(shape, device=device, generator=g) / sc[0, ..., None]),
+                             -128, 127).to(torch.int8)
+            vc = torch.clamp(torch.round(torch.randn(shape, device=device, generator=g) / sc[1, ..., None]),
+                             -128, 127).to(torch.int8)
+        else:
+            dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.cache_dtype]
+            kc = torch.randn(shape, device=device, generator=g).to(dt)
+            vc = torch.randn(shape, device=device, generator=g).to(dt)
+            sc = None
+        pools.append((kc, vc, sc))
+    return pools
+
+
+def make_step_inputs(w, lens, seed, device):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed + 1000)
+    dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.qkv_dtype]
+    q = torch.randn((w.B, w.Hq, w.D), device=device, generator=g).to(dt)
+    kn = torch.randn((w.B, w.Hkv, w.D), device=device, generator=g).to(dt)
+    vn = torch.randn((w.B, w.Hkv, w.D), device=device, generator=g).to(dt)
+    bias = None
+    if w.bias_std is not None:
+        bias = (torch.randn(((w.Hq + 2 * w.Hkv) * w.D,), device=device, generator=g) * w.bias_std).to(dt)
+    sl = torch.from_numpy(np.asarray(lens, np.int32)).to(device)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=device)
+    return dict(q=q, k_new=kn, v_new=vn, bias=bias, seq_lens=sl, out=out)
+
+
+def n_pools_for(w, kv_bytes):
+    # enough pools that a pool is re-read only after > 2x L2 (129 MB) of other traffic
+    if kv_bytes < 1e6:
+        return 1
+    return int(max(2, min(4, np.ceil(300e6 / kv_bytes) + 1)))
+
+
+def run_timed(step, w, pools, inp, steps, warmup, stream, chunk=100):
+    """W untimed steps, then exactly K steps timed with CUDA events on the launching stream.
+
+    The K steps are replayed from CUDA graphs of ``chunk`` captured steps (plus
+    one graph for the remainder), the pattern the pages recommend for the
+    fixed-shape decode loop, so host launch latency does not starve the GPU.
+    """
+    import torch
+    import decode_step_masked_gb300 as ftd
+    n = len(pools)
+
+    def one(i):
+        kc, vc, sc = pools[i % n]
+        ftd.check(ftd.ftd_decode_mha(step.ctx, inp["q"].data_ptr(), inp["k_new"].data_ptr(),
+                                     inp["v_new"].data_ptr(), 0 if inp["bias"] is None else inp["bias"].data_ptr(),
+                                     kc.data_ptr(), vc.data_ptr(), inp["seq_lens"].data_ptr(),
+                                     0 if sc is None else sc.data_ptr(), inp["out"].data_ptr(), stream.cuda_stream))
+
+    def capture(nsteps):
+        g = torch.cuda.CUDAGraph()
+        before = ftd.ftd_kernel_launches()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(nsteps):
+                one(i)
+        return g, ftd.ftd_kernel_launches() - before
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            one(i)
+    torch.cuda.synchronize()
+    chunk = max(1, min(chunk, steps))
+    g_full, launches_full = capture(chunk)
+    rem = steps % chunk
+    g_rem, launches_rem = capture(rem) if rem else (None, 0)
+    nrep = steps // chunk
+    g_full.replay()  # graph upload, untimed
+    if g_rem is not None:
+        g_rem.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nrep + 1)]
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for r in range(nrep):
+            g_full.replay()
+            evs[r + 1].record(stream)
+        end = torch.cuda.Event(enable_timing=True)
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    per = np.array([evs[r].elapsed_time(evs[r + 1]) for r in range(nrep)]) * 1e3 / chunk  # µs per step
+    total_ms = evs[0].elapsed_time(end)
+    ftd.check(step.get_error())
+    launches = launches_full * nrep + launches_rem
+    return dict(total_ms=total_ms, per_us=per, launches=launches, wall=(t_wall0, t_wall1))
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, window):
+        if not self.proc or not self.file:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0, note="nvidia-smi unavailable")
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+                except ValueError:
+                    continue
+        os.unlink(self.file.name)
+        inside = [r for r in rows if window[0] <= r[0] <= window[1]]
+        src = "timed region"
+        if len(inside) < 3:
+            inside = [r for r in rows if r[0] <= window[1]]
+            src = "warm-up and timed region (timed region shorter than the sampling interval)"
+        if not inside:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0, note="no samples")
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4) if r[3][i + 1].lower().startswith("active")})
+        return dict(sm_mhz=float(np.median([r[1] for r in inside])), sm_max_mhz=max(r[2] for r in inside),
+                    reasons=reasons, samples=len(inside), window=src)
+
+
+def gpu_id_for(local_rank: int) -> str:
+    import torch
+    props = torch.cuda.get_device_properties(local_rank)
+    bus = getattr(props, "pci_bus_id", None)
+    dom = getattr(props, "pci_domain_id", None)
+    dev = getattr(props, "pci_device_id", None)
+    if bus is not None and dom is not None and dev is not None:
+        return f"{dom:08X}:{bus:02X}:{dev:02X}.0"
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_timing(w, seconds: float, nthreads: int, seed: int = 0):
+    """Time the float64 oracle on bounded samples of the workload: whole slots, in turn."""
+    import oracle
+    from synthetic import gen_cache_slot, gen_qkv, gen_scales_slot
+    o = oracle.load()
+    lens = gen_seq_lens(w, seed or None)
+    q, kn, vn, bias = gen_qkv(w, seed or None)
+    w1 = w.with_(B=1)
+    done_bytes, elapsed, slots = 0, 0.0, 0
+    b = 0
+    while elapsed < seconds or slots == 0:
+        L = int(lens[b])
+        sub = dict(q=q[b:b + 1], k_new=kn[b:b + 1], v_new=vn[b:b + 1], bias=bias,
+                   k_cache=gen_cache_slot(w, seed or None, "k", b, L, "zero")[None],
+                   v_cache=gen_cache_slot(w, seed or None, "v", b, L, "zero")[None],
+                   seq_lens=lens[b:b + 1], scales=None)
+        if w.cache_dtype == "i8":
+            sub["scales"] = np.stack([gen_scales_slot(w, seed or None, "k", b, L, "zero")[None],
+                                      gen_scales_slot(w, seed or None, "v", b, L, "zero")[None]])
+        t0 = time.perf_counter()
+        o.decode_step(w1, sub, nthreads=nthreads)
+        elapsed += time.perf_counter() - t0
+        done_bytes += step_bytes(w1, lens[b:b + 1])["kv"]
+        slots += 1
+        b = (b + 1) % w.B
+    return dict(gbs=done_bytes / elapsed / 1e9, slots=slots, seconds=elapsed, bytes=done_bytes)
+
+
+def oracle_one_head_seconds(w, nthreads=1) -> float:
+    import oracle
+    from synthetic import gen_all
+    lens = gen_seq_lens(w)
+    L = int(np.max(lens))
+    ws = w.with_(B=1, Hq=1, Hkv=1, Lmax=max(16, (L + 16) // 16 * 16), bias_std=None)
+    inp = gen_all(ws, seq_lens=np.array([L], np.int32), fill_beyond="zero")
+    t0 = time.perf_counter()
+    oracle.load().decode_step(ws, inp, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+# ---------------------------------------------------------------- multi-rank
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_over_ranks(local_ms: float, local_units: float, world: int, device=None):
+    """Max of the per-rank timed-region length and the sum of the units processed."""
+    if world == 1:
+        return local_ms, local_units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([local_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([local_units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------- arms
+def reference_arm(args):
+    """The float64 CPU oracle, timed on the host cores on bounded samples of the same workload."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = WORKLOADS[args.config]
+    lens = gen_seq_lens(w)
+    per_step = step_bytes(w, lens)
+    nthreads = os.cpu_count() or 1
+    t_head = max(oracle_one_head_seconds(w, nthreads=1), 1e-4)
+    budget = 90.0 / max(1, args.steps + args.warmup)  # the whole run ends within a few minutes
+    heads = int(max(1, min(w.B * w.Hq, budget / t_head)))
+    import oracle
+    from synthetic import gen_all
+    L = int(np.max(lens))
+    ws = w.with_(B=1, Hq=heads, Hkv=heads, Lmax=max(16, (L + 16) // 16 * 16), bias_std=None)
+    inp = gen_all(ws, seq_lens=np.array([L], np.int32), fill_beyond="zero")
+    o = oracle.load()
+    for _ in range(args.warmup):
+        o.decode_step(ws, inp, nthreads=1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.decode_step(ws, inp, nthreads=1)
+    dt = time.perf_counter() - t0
+    sample_bytes = step_bytes(ws, [L])["kv"]
+    gbs = sample_bytes * args.steps / dt / 1e9
+    line = dict(metric=METRIC, value=gbs, unit="GB/s", n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
+                ms_per_step=dt / args.steps * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic", impl="reference",
+                config=dict(workload=w.description, name=w.name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D,
+                            Lmax=w.Lmax, cache_dtype=w.cache_dtype),
+                cpu_baseline=dict(value=gbs, unit="GB/s", cores=1, kind="oracle",
+                                  sample=f"{heads} head(s) x context {L + 1} per step (float64 C oracle, one "
+                                         f"thread); full step would be {per_step['kv'] / 1e6:.1f} MB"),
+                e2e=dict(value=gbs, unit="GB/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line), flush=True)
+
+
+def measure_config(name, steps, warmup, seed, device, stream):
+    import decode_step_masked_gb300 as ftd
+    w = WORKLOADS[name]
+    lens = gen_seq_lens(w)
+    by = step_bytes(w, lens)
+    pools = make_pools(w, n_pools_for(w, by["kv"]), seed, device)
+    inp = make_step_inputs(w, lens, seed, device)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    r = run_timed(step, w, pools, inp, steps, warmup, stream)
+    step.close()
+    us = r["total_ms"] * 1e3 / steps
+    return w, lens, by, pools, inp, r, us
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--config", default="7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ftd", choices=["ftd", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip per-config, e2e and CPU-baseline legs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import decode_step_masked_gb300 as ftd
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    ftd.build_library()
+    ftd.load_library()
+    stream = torch.cuda.Stream(device=device)
+    peaks = load_peaks()
+
+    # ---- headline: the named workload, K timed steps ----
+    sampler = ClockSampler(gpu_id_for(local))
+    with sampler:
+        if world > 1:
+            torch.distributed.barrier()
+        w, lens, by, pools, inp, r, us = measure_config(args.config, args.steps, args.warmup, 1234 + rank,
+                                                        device, stream)
+        if world > 1:
+            torch.distributed.barrier()
+    clocks = sampler.summary(r["wall"])
+    max_ms, units = reduce_over_ranks(r["total_ms"], float(by["kv"]) * args.steps, world, device)
+    value = units / (max_ms * 1e-3) / 1e9
+    per = r["per_us"]
+    kern_us = r["total_ms"] * 1e3 / args.steps
+    achieved = by["total"] / (kern_us * 1e-6) / 1e9
+    traffic = load_traffic(w.name)
+    line = dict(
+        metric=METRIC, value=value, unit="GB/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+        ms_per_step=max_ms / args.steps, us_per_step=max_ms / args.steps * 1e3,
+        us_per_step_median=float(np.median(per)), us_per_step_p99=float(np.percentile(per, 99)),
+        frac_of_hbm_peak=value / world / peaks["hbm_gbs"], higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype="f32", data="synthetic",
+        config=dict(workload=w.description, name=w.name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, D=w.D, Lmax=w.Lmax,
+                    cache_dtype=w.cache_dtype, qkv_dtype=w.qkv_dtype, context_tokens=by["ctx"],
+                    kv_bytes_per_step=by["kv"], l2="caches rotated over %d pools of %.0f MB each (> L2 129 MB)"
+                    % (len(pools), by["kv"] / 1e6), parallelism=f"replicas x{world}"),
+        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                      frac=achieved / peaks["hbm_gbs"], traffic=traffic,
+                      peak_source=f"{peaks['source']} (STREAM-style copy)", kernel="decode_splitk_kernel",
+                      bytes_per_launch=by["total"], launch_us=kern_us),
+        gpu_launches=int(r["launches"]), clocks=clocks)
+    del pools
+
+    if rank == 0 and not args.no_extras:
+        # ---- end to end through the host-buffer entry point ----
+        line["e2e"] = e2e_leg(w, lens, by, device, stream, min(args.steps, 2000))
+        # ---- every large workload of the suite, same protocol ----
+        per_cfg = {}
+        for name in ("7b", "13b", "70b", "int8", "tiny"):
+            if name == w.name:
+                per_cfg[name] = dict(us=line["us_per_step"], gbs=value / world, frac=value / world / peaks["hbm_gbs"])
+                continue
+            w2, _, by2, pools2, _, r2, us2 = measure_config(name, 1000, 50, 99, device, stream)
+            per_cfg[name] = dict(us=us2, us_median=float(np.median(r2["per_us"])), gbs=by2["kv"] / us2 / 1e3,
+                                 frac=by2["kv"] / us2 / 1e3 / peaks["hbm_gbs"], kv_mb=by2["kv"] / 1e6)
+            del pools2
+            torch.cuda.empty_cache()
+        line["per_config"] = per_cfg
+        # ---- the float64 oracle on the host cores ----
+        cores = os.cpu_count() or 1
+        cb = oracle_timing(w, 10.0, cores)
+        line["cpu_baseline"] = dict(value=cb["gbs"], unit="GB/s", cores=cores, kind="oracle",
+                                    sample=f"{cb['slots']} whole slot(s) of the {w.name} workload "
+                                           f"({cb['bytes'] / 1e6:.0f} MB of KV) in {cb['seconds']:.1f} s, "
+                                           f"OpenMP over (slot, head)")
+    elif rank == 0:
+        line["e2e"] = None
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def e2e_leg(w, lens, by, device, stream, steps):
+    """Same metric through ftd_decode_mha_host: pinned host inputs in, fp32 output back, every step."""
+    import torch
+    import decode_step_masked_gb300 as ftd
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    kp, vp, sp = step.cache_ptrs()
+    src = make_pools(w, 1, 7, device)[0]
+    for ptr, t in ((kp, src[0]), (vp, src[1])):
+        _copy_into(ptr, t)
+    if src[2] is not None:
+        _copy_into(sp, src[2])
+    del src
+    torch.cuda.synchronize()
+    inp = make_step_inputs(w, lens, 7, device)
+    host = {k: (v.cpu().pin_memory() if v is not None else None) for k, v in inp.items() if k != "out"}
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32).pin_memory()
+    args = [host["q"].data_ptr(), host["k_new"].data_ptr(), host["v_new"].data_ptr(),
+            0 if host["bias"] is None else host["bias"].data_ptr(), 0, 0, host["seq_lens"].data_ptr(), 0,
+            out.data_ptr(), stream.cuda_stream]
+    for _ in range(20):
+        ftd.check(ftd.ftd_decode_mha_host(step.ctx, *args))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        ftd.check(ftd.ftd_decode_mha_host(step.ctx, *args))
+    dt = time.perf_counter() - t0
+    ftd.check(step.get_error())
+    step.close()
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    return dict(value=by["kv"] * steps / dt / 1e9, unit="GB/s", us_per_step=dt / steps * 1e6,
+                h2d_bytes_per_step=int(h2d), d2h_bytes_per_step=int(out.numel() * 4), steps=steps,
+                api="ftd_decode_mha_host (pinned host buffers, stream synchronised every step)")
+
+
+def _copy_into(ptr, t):
+    """Copy a device tensor into library-owned device memory at ``ptr``."""
+    import torch
+
+    class _CAI:
+        __cuda_array_interface__ = {"shape": (t.numel() * t.element_size(),), "typestr": "|u1",
+                                    "data": (int(ptr), False), "version": 3, "strides": None}
+
+    dst = torch.as_tensor(_CAI(), device=t.device)
+    dst.copy_(t.contiguous().view(-1).view(torch.uint8))
+
+
+if __name__ == "__main__":
+    main()
