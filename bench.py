@@ -277,15 +277,19 @@ def oracle_timing(w, seconds: float, nthreads: int, seed: int = 0):
     w1 = w.with_(B=1)
     done_bytes, elapsed, slots = 0, 0.0, 0
     b = 0
+    cache = {}
     while elapsed < seconds or slots == 0:
         L = int(lens[b])
-        sub = dict(q=q[b:b + 1], k_new=kn[b:b + 1], v_new=vn[b:b + 1], bias=bias,
-                   k_cache=gen_cache_slot(w, seed or None, "k", b, L, "zero")[None],
-                   v_cache=gen_cache_slot(w, seed or None, "v", b, L, "zero")[None],
-                   seq_lens=lens[b:b + 1], scales=None)
-        if w.cache_dtype == "i8":
-            sub["scales"] = np.stack([gen_scales_slot(w, seed or None, "k", b, L, "zero")[None],
-                                      gen_scales_slot(w, seed or None, "v", b, L, "zero")[None]])
+        if b not in cache:  # input generation is not timed; each slot is drawn once
+            sub = dict(q=q[b:b + 1], k_new=kn[b:b + 1], v_new=vn[b:b + 1], bias=bias,
+                       k_cache=gen_cache_slot(w, seed or None, "k", b, L, "zero")[None],
+                       v_cache=gen_cache_slot(w, seed or None, "v", b, L, "zero")[None],
+                       seq_lens=lens[b:b + 1], scales=None)
+            if w.cache_dtype == "i8":
+                sub["scales"] = np.stack([gen_scales_slot(w, seed or None, "k", b, L, "zero")[None],
+                                          gen_scales_slot(w, seed or None, "v", b, L, "zero")[None]])
+            cache[b] = sub
+        sub = cache[b]
         t0 = time.perf_counter()
         o.decode_step(w1, sub, nthreads=nthreads)
         elapsed += time.perf_counter() - t0
@@ -389,7 +393,11 @@ def main():
     ap.add_argument("--config", default="7b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ftd", choices=["ftd", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip per-config, e2e and CPU-baseline legs")
+    ap.add_argument("--ncu-launches", type=int, default=0,
+                    help="profiling mode: launch N untimed steps of --config on one cache pool, print nothing")
     args = ap.parse_args()
+    if args.ncu_launches:
+        return profile_launches(args.config, args.ncu_launches)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
@@ -469,6 +477,25 @@ def main():
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def profile_launches(name, n):
+    """N plain launches of one workload on one cache pool (for ncu captures of a single launch)."""
+    import torch
+    import decode_step_masked_gb300 as ftd
+    w = WORKLOADS[name]
+    lens = gen_seq_lens(w)
+    device = torch.device("cuda", 0)
+    ftd.build_library()
+    kc, vc, sc = make_pools(w, 1, 5, device)[0]
+    inp = make_step_inputs(w, lens, 5, device)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    for _ in range(n):
+        step(inp["q"], inp["k_new"], inp["v_new"], inp["seq_lens"], inp["out"], bias=inp["bias"], k_cache=kc,
+             v_cache=vc, scales=sc)
+    torch.cuda.synchronize()
+    ftd.check(step.get_error())
+    step.close()
 
 
 def e2e_leg(w, lens, by, device, stream, steps):
