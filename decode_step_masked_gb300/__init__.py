@@ -30,7 +30,7 @@ DTYPES = {"f32": FTD_F32, "f16": FTD_F16, "bf16": FTD_BF16, "i8": FTD_I8}
 
 # Symbols include/ftd.h declares; the loader checks each one is exported.
 EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_host", "ftd_get_error",
-           "ftd_destroy", "ftd_status_str", "ftd_last_error", "ftd_kernel_launches")
+           "ftd_destroy", "ftd_status_str", "ftd_last_error", "ftd_kernel_launches", "ftd_decode_mha_noalloc")
 
 
 class FtdConfig(ctypes.Structure):
@@ -79,6 +79,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ftd_last_error.restype = ctypes.c_char_p
     lib.ftd_kernel_launches.argtypes = []
     lib.ftd_kernel_launches.restype = ctypes.c_uint64
+    lib.ftd_decode_mha_noalloc.argtypes = [ctypes.POINTER(FtdConfig)] + [P] * 11
+    lib.ftd_decode_mha_noalloc.restype = I
     if path == LIB:
         _lib = lib
     return lib
@@ -123,6 +125,14 @@ def ftd_decode_mha_host(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_le
                         stream) -> int:
     return load_library().ftd_decode_mha_host(*_ptrs(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache,
                                                      seq_lens, scales, out, stream))
+
+
+def ftd_decode_mha_noalloc(cfg: FtdConfig, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out,
+                           device_err, stream) -> int:
+    """The decode step without a context: scratch lives in the library's static device array."""
+    return load_library().ftd_decode_mha_noalloc(ctypes.byref(cfg), *_ptrs(q, k_new, v_new, qkv_bias, k_cache,
+                                                                           v_cache, seq_lens, scales, out,
+                                                                           device_err, stream))
 
 
 def ftd_get_error(ctx) -> int:

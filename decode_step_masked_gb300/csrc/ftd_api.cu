@@ -54,6 +54,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+namespace ftd {
+// Internal to the library (hidden): used by the no-allocation entry point so its
+// failures show in ftd_last_error() and its launches in ftd_kernel_launches().
+__attribute__((visibility("hidden"))) void set_last_error(const char* msg) { g_last_error = msg; }
+__attribute__((visibility("hidden"))) void note_launch() { g_launches.fetch_add(1); }
+}  // namespace ftd
+
 struct ftd_ctx {
     ftd_config cfg;
     int device = 0;

@@ -634,6 +634,9 @@ KernelInfo select_kernel(int D, int G) {
     return KernelInfo{nullptr, 0, 0, 0, 0};
 }
 
+void set_last_error(const char* msg);
+void note_launch();
+
 KernelInfo select_f32(int D, int G);
 KernelInfo select_f16(int D, int G);
 KernelInfo select_bf16(int D, int G);

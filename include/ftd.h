@@ -161,6 +161,48 @@ const char* ftd_last_error(void);
  * process (every decode call adds one; host-side failures add none). */
 uint64_t ftd_kernel_launches(void);
 
+/* Size of the fixed device array that ftd_decode_mha_noalloc uses as scratch. */
+#define FTD_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * ftd_decode_mha_noalloc -- the decode step of ftd_decode_mha for callers that
+ * must not allocate device memory.  The pages describe nothing like it: it
+ * exists for callers that cannot call cudaMalloc at all -- a plugin inside a
+ * host runtime whose own allocator owns all device memory, or a serving loop
+ * that forbids allocation (which can synchronise the device or fail) after
+ * start-up -- and so cannot create a context with ftd_init.
+ *
+ *   cfg              : shape and dtypes, same rules as ftd_init.
+ *   q ... out        : as in ftd_decode_mha, all caller-owned device memory;
+ *                      k_cache and v_cache are required (there is no pool), and
+ *                      so are scales for an INT8 cache.
+ *   device_err       : device uint32, or NULL.  When given, the kernel ORs its
+ *                      error bits into it (1 = some seq_lens[b] >= max_len,
+ *                      2 = a bounded wait gave up); the caller reads and clears
+ *                      it.  When NULL those bits are dropped (overflowing slots
+ *                      still get a zero output).
+ *   stream           : cudaStream_t as void*.
+ *
+ * It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Its split-K partials, counters and error word live in one static device
+ * array of FTD_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the
+ * library holds until the process exits.  A configuration that needs more
+ * (max_batch * n_kv_heads * heads-per-kv-block slots plus 8 per SM, each of
+ * about head_dim * 4 bytes per query head of a block) is rejected with
+ * FTD_ERR_INVALID_ARG and a message in ftd_last_error().
+ * The first call on each device does a one-time set-up with that device
+ * current (it looks up the array's device address and raises the kernel's
+ * shared-memory limit); make that first call before any stream capture.
+ * Every call clears the counters and error word it uses at the start, on
+ * `stream`.  All calls share the one array: calls whose kernels overlap in
+ * time on the same GPU race and give wrong results, so issue them on one
+ * stream or order them with events.
+ */
+ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* q, const void* k_new,
+                                  const void* v_new, const void* qkv_bias, void* k_cache,
+                                  void* v_cache, const int32_t* seq_lens, float* scales, float* out,
+                                  uint32_t* device_err, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

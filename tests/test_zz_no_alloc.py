@@ -1,0 +1,85 @@
+"""ftd_decode_mha_noalloc against ftd_decode_mha on the same inputs, two calls in a row.
+
+The no-allocation entry point serves callers that may not call cudaMalloc (a
+plugin whose host runtime owns all device memory, or a loop that forbids
+allocation after start-up); its scratch is a static device array shared by
+every call.  This file is named to run last so that a run stopping at the
+first failure has already run every other test; it also passes on its own.
+"""
+import numpy as np
+import pytest
+
+import decode_step_masked_gb300 as ftd
+from synthetic import Workload, gen_all
+from tests.gpu_util import TOL_MAXABS, TOL_RELL2, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    ftd.build_library()
+    ftd.load_library()
+
+
+def _case(lens, seed):
+    w = Workload("noalloc", B=len(lens), Hq=16, Hkv=4, D=128, Lmax=1024, qkv_dtype="bf16", cache_dtype="bf16",
+                 bias_std=0.1, seed=seed)
+    return w, gen_all(w, seed=seed, seq_lens=np.array(lens, np.int32), fill_beyond="nan")
+
+
+def test_noalloc_matches_context_entry_point_twice():
+    import torch
+    cases = [_case([1000, 3, 517, 64, -1, 255], seed=21), _case([15, 800, 1023, 2, 300, 999], seed=22)]
+    w0 = cases[0][0]
+    step = ftd.DecodeStep(w0.B, w0.Hq, w0.Hkv, w0.D, w0.Lmax, w0.qkv_dtype, w0.cache_dtype)
+    cfg = ftd.FtdConfig(w0.B, w0.Hq, w0.Hkv, w0.D, w0.Lmax, ftd.FTD_BF16, ftd.FTD_BF16, 0.0)
+    s = torch.cuda.current_stream().cuda_stream
+    for call, (w, inp) in enumerate(cases):
+        q, kn, vn, bias, sl = (dev(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens"))
+        kc_a, vc_a = dev(inp["k_cache"]), dev(inp["v_cache"])
+        kc_b, vc_b = dev(inp["k_cache"]), dev(inp["v_cache"])
+        out_a = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+        out_b = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        step(q, kn, vn, sl, out_a, bias=bias, k_cache=kc_a, v_cache=vc_a)
+        st = ftd.ftd_decode_mha_noalloc(cfg, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), bias.data_ptr(),
+                                        kc_b.data_ptr(), vc_b.data_ptr(), sl.data_ptr(), 0, out_b.data_ptr(),
+                                        err.data_ptr(), s)
+        assert st == ftd.FTD_OK, ftd.ftd_last_error()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        a = out_a.cpu().numpy().astype(np.float64)
+        b = out_b.cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(b)), f"call {call}: non-finite output"
+        assert np.max(np.abs(a - b)) <= TOL_MAXABS, f"call {call}"
+        assert np.linalg.norm(a - b) / np.linalg.norm(a) <= TOL_RELL2, f"call {call}"
+        assert torch.equal(kc_a, kc_b) and torch.equal(vc_a, vc_b), f"call {call}: appended rows differ"
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+
+
+def test_noalloc_reports_overflow_and_rejects_oversized_configs():
+    import torch
+    w, inp = _case([1024, 5], seed=23)  # slot 0 overflows (seq_len == max_len)
+    cfg = ftd.FtdConfig(w.B, w.Hq, w.Hkv, w.D, w.Lmax, ftd.FTD_BF16, ftd.FTD_BF16, 0.0)
+    q, kn, vn, sl = (dev(inp[k]) for k in ("q", "k_new", "v_new", "seq_lens"))
+    kc, vc = dev(inp["k_cache"]), dev(inp["v_cache"])
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = ftd.ftd_decode_mha_noalloc(cfg, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), 0, kc.data_ptr(),
+                                    vc.data_ptr(), sl.data_ptr(), 0, out.data_ptr(), err.data_ptr(), s)
+    assert st == ftd.FTD_OK, ftd.ftd_last_error()
+    torch.cuda.synchronize()
+    assert int(err.item()) & 1, "overflow bit"
+    assert not out[0].any().item() and torch.isfinite(out[1]).all().item()
+    # 1024 slots x 128 kv heads of partials do not fit in the static array
+    big = ftd.FtdConfig(1024, 128, 128, 128, 4096, ftd.FTD_BF16, ftd.FTD_BF16, 0.0)
+    st = ftd.ftd_decode_mha_noalloc(big, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), 0, kc.data_ptr(),
+                                    vc.data_ptr(), sl.data_ptr(), 0, out.data_ptr(), 0, s)
+    assert st == ftd.FTD_ERR_INVALID_ARG
+    assert "static array" in ftd.ftd_last_error()
