@@ -4,9 +4,11 @@
 // (the pre-allocated KV-cache buffer of "FasterTransformer source analysis",
 // framerc.cn, section 3.2), kernel selection and launch.  Every step of the
 // decode path itself runs in the kernels of ftd_decode_splitk.cuh.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <cstdarg>
 #include <cmath>
 #include <cstdio>
@@ -16,6 +18,7 @@
 
 #include "../../include/ftd.h"
 #include "ftd_decode_splitk.cuh"
+#include "ftd_decode_gqa_tc.cuh"
 
 namespace {
 
@@ -52,6 +55,39 @@ int elem_bytes(ftd_dtype d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// cuTensorMapEncodeTiled, fetched once through the runtime (no link against libcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// 2-D view of a [B][Hkv][Lmax][128] fp16/bf16 cache as rows of 128 elements,
+// read in boxes of 64 columns x 128 rows with the 128-byte swizzle the
+// tensor-core operands expect.
+bool encode_cache_map(CUtensorMap* map, void* base, bool bf16, size_t rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {128 * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 namespace ftd {
@@ -67,6 +103,13 @@ struct ftd_ctx {
     int grid = 0;
     int G = 1, nhb = 1;
     ftd::KernelInfo ki{};
+    bool use_tc = false;       // grouped-query fp16/bf16 caches run on the tensor cores
+    ftd::TcKernelInfo tki{};
+    int tc_nhb = 1;
+    alignas(64) CUtensorMap tmk;
+    alignas(64) CUtensorMap tmv;
+    const void* tm_k_base = nullptr;
+    const void* tm_v_base = nullptr;
     float qscale = 0.f;
     void* pool = nullptr;
     size_t pool_bytes = 0;
@@ -156,13 +199,30 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     e = cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
 
-    const int grid = sms;  // one persistent CTA of 8 worker warps per SM
+    const int grid = sms;  // one persistent CTA per SM
     const size_t B = c.max_batch, Hq = c.n_q_heads, Hkv = c.n_kv_heads, D = c.head_dim, L = c.max_len;
     const size_t cache_bytes = B * Hkv * L * D * elem_bytes(c.cache_dtype);
     const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * B * Hkv * L * sizeof(float) : 0;
-    const size_t n_seg = B * Hkv * nhb;
-    const size_t n_slots = n_seg + static_cast<size_t>(grid) * ftd::kWarps;
-    const size_t ws_bytes = n_slots * ki.slot_floats * sizeof(float);
+
+    // Grouped-query fp16/bf16 caches with head_dim 128 and groups of 8 or 16
+    // query heads use the tensor-core kernel; FTD_FORCE_CUDA_CORE=1 in the
+    // environment at ftd_init selects the CUDA-core kernel instead.
+    const char* force = getenv("FTD_FORCE_CUDA_CORE");
+    const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
+                         g % 8 == 0 && B * Hkv * L < (static_cast<size_t>(1) << 31) && !(force && force[0] == '1');
+    ftd::TcKernelInfo tki{};
+    int tc_nhb = 1;
+    if (want_tc && encode_tiled()) {
+        const int Gt = g % 16 == 0 ? 16 : 8;
+        tki = ftd::select_tc(c.cache_dtype == FTD_BF16, Gt);
+        tc_nhb = g / Gt;
+        e = cudaFuncSetAttribute(tki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tki.smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (tensor-core kernel)");
+    }
+    const bool use_tc = tki.fn != nullptr;
+    const size_t n_seg = use_tc ? B * Hkv * tc_nhb : B * Hkv * nhb;
+    const size_t n_slots = n_seg + static_cast<size_t>(grid) * (use_tc ? 1 : ftd::kWarps);
+    const size_t ws_bytes = n_slots * (use_tc ? tki.slot_floats : ki.slot_floats) * sizeof(float);
     const int qeb = elem_bytes(c.qkv_dtype);
 
     ftd_ctx* ctx = new (std::nothrow) ftd_ctx();
@@ -173,6 +233,9 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     ctx->G = G;
     ctx->nhb = nhb;
     ctx->ki = ki;
+    ctx->use_tc = use_tc;
+    ctx->tki = tki;
+    ctx->tc_nhb = tc_nhb;
     const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf(static_cast<float>(D));
     ctx->qscale = scale * 1.4426950408889634f;
     ctx->q_bytes = B * Hq * D * qeb;
@@ -277,9 +340,29 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     p.qkv_dtype = static_cast<int>(c.qkv_dtype);
     p.qscale = ctx->qscale;
 
-    void* args[] = {&p};
-    cudaError_t e = cudaLaunchKernel(ctx->ki.fn, dim3(ctx->grid), dim3(ftd::kThreads), args,
-                                     static_cast<size_t>(ctx->ki.smem), stream);
+    cudaError_t e;
+    if (ctx->use_tc) {
+        const size_t rows = static_cast<size_t>(c.max_batch) * c.n_kv_heads * c.max_len;
+        const bool bf16 = c.cache_dtype == FTD_BF16;
+        if (ctx->tm_k_base != k_cache) {
+            if (!encode_cache_map(&ctx->tmk, k_cache, bf16, rows))
+                return fail(FTD_ERR_CUDA, "cuTensorMapEncodeTiled failed for k_cache");
+            ctx->tm_k_base = k_cache;
+        }
+        if (ctx->tm_v_base != v_cache) {
+            if (!encode_cache_map(&ctx->tmv, v_cache, bf16, rows))
+                return fail(FTD_ERR_CUDA, "cuTensorMapEncodeTiled failed for v_cache");
+            ctx->tm_v_base = v_cache;
+        }
+        p.nhb = ctx->tc_nhb;
+        void* args[] = {&ctx->tmk, &ctx->tmv, &p};
+        e = cudaLaunchKernel(ctx->tki.fn, dim3(ctx->grid), dim3(256), args, static_cast<size_t>(ctx->tki.smem),
+                             stream);
+    } else {
+        void* args[] = {&p};
+        e = cudaLaunchKernel(ctx->ki.fn, dim3(ctx->grid), dim3(ftd::kThreads), args,
+                             static_cast<size_t>(ctx->ki.smem), stream);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     g_launches.fetch_add(1);
     ctx->last_stream = stream;

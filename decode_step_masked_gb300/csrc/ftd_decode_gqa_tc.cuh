@@ -1,0 +1,605 @@
+// ftd_decode_gqa_tc.cuh -- decode step for grouped-query caches on the
+// 5th-generation tensor cores (tcgen05 + TMEM, sm_103a).
+//
+// With g = Hq / Hkv query heads sharing a kv head, every cached K/V element
+// feeds g multiply-adds for the scores and g for P.V.  At g = 8 that is
+// 8 flop per byte of bf16 cache, more than the CUDA cores can issue at HBM
+// speed, so here the two contractions of a 128-row tile run on the tensor
+// cores as real dense products ("10 tricks", pptc.cn, section 3.4: the query
+// heads of one group share K and V):
+//
+//   S^T [128 rows x 2G] = K_tile [128 x D]   . Qs^T [D x 2G]     (A, B K-major)
+//   O^T [D x 2G]        = V_tile^T [D x 128] . Ps^T [128 x 2G]   (A MN-major)
+//
+// Qs holds the G query heads twice: a bf16 (or fp16) high part and the
+// rounding remainder as a low part, and Ps likewise for the softmax weights,
+// so each product keeps about 16 mantissa bits of the fp32 operand; the
+// accumulators are fp32 in TMEM and hi + lo are summed when read back.
+//
+// Roles (256 threads, one CTA per SM, persistent):
+//   warp 0  bulk tensor copies (TMA, 128B swizzle) of K and V tiles into a
+//           3-stage ring;
+//   warp 1  TMEM allocation, the append and the tcgen05.mma issue: its lanes
+//           wait for every staged tile in order; in the last tile of a segment
+//           they write k' = k_new + b_k (and v') rounded to the cache type into
+//           the cache and into the staged tile and zero the staged V rows past
+//           the sequence end (so 0 * garbage never reaches the product), then
+//           lane 0 issues the MMAs;
+//   warps 4-7 (128 threads) the online softmax: thread i owns row i of S and
+//           dimension i of O; they build Qs, read S from TMEM, keep the
+//           running max / sum per head, write Ps, rescale-and-add O, and at
+//           the end of a piece write the output or a split-K partial, merged
+//           by the last piece exactly as in the CUDA-core kernel.
+// Work split: the same balanced contiguous ranges of a global tile space as
+// ftd_decode_splitk.cuh, with 128-row tiles and one CTA per worker.
+#pragma once
+
+#include <cuda.h>
+
+#include "ftd_decode_splitk.cuh"
+
+namespace ftd {
+namespace tc {
+
+constexpr int TM = 128;   // rows per tile (the MMA M of the score product)
+constexpr int D = 128;    // head dimension (the MMA M of the P.V product)
+constexpr int NS = 3;     // K/V stages
+constexpr int KB = 16384; // one 64-column box of 128 rows (bytes)
+constexpr int STAGE = 4 * KB;  // K (2 boxes) + V (2 boxes)
+
+template <int G>
+struct Layout {
+    static constexpr int N = 2 * G;                // hi and lo parts
+    static constexpr int QS = 2 * N * 128;         // Qs / Ps: 2 k-blocks of N rows x 128 B
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_QS = NS * STAGE;
+    static constexpr int OFF_P = OFF_QS + round_up(QS, 1024);
+    static constexpr int OFF_RED = OFF_P + 2 * round_up(QS, 1024);
+    static constexpr int RED_BYTES = 4 * G * 4 * 2;  // per warp, per head: max and sum
+    static constexpr int OFF_MISC = OFF_RED + round_up(RED_BYTES, 128);
+    static constexpr int MISC_BYTES = 256;           // barriers, TMEM base, flags
+    static constexpr int OFF_PREFIX = OFF_MISC + MISC_BYTES;
+    static constexpr int PREFIX_BYTES = (2 * kMaxBatch + 1) * 4;
+    static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;  // + alignment slack
+    static constexpr int TMEM_COLS = (4 * N <= 32) ? 32 : (4 * N <= 64 ? 64 : 128);
+    static constexpr int OOFF = round_up(2 * G, 4);
+    static constexpr int SLOT = OOFF + G * D;
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+// ------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;  // descriptor version of tcgen05
+    d |= static_cast<uint64_t>(2) << 61;  // 128-byte swizzle
+    return d;
+}
+
+// kind::f16 instruction descriptor: fp32 accumulate, A/B bf16 (or fp16), M x N.
+__device__ __forceinline__ uint32_t instr_desc(bool bf16, int M, int N, bool a_mn_major) {
+    uint32_t d = 0;
+    d |= 1u << 4;                                  // D: f32
+    d |= (bf16 ? 1u : 0u) << 7;                    // A type
+    d |= (bf16 ? 1u : 0u) << 10;                   // B type
+    d |= (a_mn_major ? 1u : 0u) << 15;             // A major-ness
+    d |= static_cast<uint32_t>(N >> 3) << 17;
+    d |= static_cast<uint32_t>(M >> 4) << 24;
+    return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1 : 0));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+template <int NC>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[NC]);
+
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
+    float a[16], b[16];
+    tmem_ld<16>(taddr, a);
+    tmem_ld<16>(taddr + 16, b);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[i] = a[i];
+        v[16 + i] = b[i];
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Byte offset of element (row r, column k) in a K-major operand with 128-byte
+// swizzle made of 64-column blocks of `rows` rows: 16-byte chunk c of row r
+// sits at chunk c ^ (r % 8) of that row.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int k, int rows) {
+    const int blk = k >> 6, c = (k & 63) >> 3, e = k & 7;
+    return static_cast<uint32_t>(blk * rows * 128 + r * 128 + ((c ^ (r & 7)) << 4) + e * 2);
+}
+
+// Operand layout of the MN-major V tile (A of the P.V product): two 64-column
+// boxes of 128 rows; the stride between boxes (16 KB) and between 8-row groups
+// (1 KB) go into the descriptor's leading / stride byte offsets.
+constexpr uint32_t kVLbo = KB;
+constexpr uint32_t kVSbo = 1024;
+
+// Barrier-wide OR of a predicate over `n` threads (named barrier `id`).
+__device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// Bounded wait that also gives up as soon as another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t* err, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            atomicOr(err, kErrTimeout);
+            *abort_flag = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+template <typename CT>
+__device__ __forceinline__ CT to_ct(float x);
+template <>
+__device__ __forceinline__ __nv_bfloat16 to_ct<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+template <>
+__device__ __forceinline__ __half to_ct<__half>(float x) { return __float2half_rn(x); }
+template <typename CT>
+__device__ __forceinline__ float from_ct(CT x);
+template <>
+__device__ __forceinline__ float from_ct<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <>
+__device__ __forceinline__ float from_ct<__half>(__half x) { return __half2float(x); }
+
+}  // namespace tc
+
+// Barrier slots in the misc area.
+enum : int { kBarFull = 0, kBarEmpty = 3, kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarQReady = 12,
+             kNumBars = 13 };
+
+template <typename CT, int G>
+__global__ void __launch_bounds__(256, 1)
+    decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                         const DecodeParams p) {
+    using LY = tc::Layout<G>;
+    constexpr int N = LY::N, TM = tc::TM, D = tc::D, NS = tc::NS, KB = tc::KB;
+    constexpr int PSZ = round_up(LY::QS, 1024);
+    constexpr bool BF = std::is_same_v<CT, __nv_bfloat16>;
+    constexpr unsigned FULL = 0xffffffffu;
+
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~static_cast<uintptr_t>(1023));
+    unsigned char* stages = smem + LY::OFF_STAGE;
+    unsigned char* Qs = smem + LY::OFF_QS;
+    unsigned char* Ps = smem + LY::OFF_P;
+    float* red_max = reinterpret_cast<float*>(smem + LY::OFF_RED);
+    float* red_sum = red_max + 4 * G;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + LY::OFF_MISC);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::OFF_MISC + kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_MISC + kNumBars * 8 + 4);
+    int* bcast = reinterpret_cast<int*>(smem + LY::OFF_MISC + kNumBars * 8 + 8);
+    int* P = reinterpret_cast<int*>(smem + LY::OFF_PREFIX);
+    int* Ls = P + (kMaxBatch + 1);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int segs = p.Hkv * p.nhb;
+    auto bar = [&](int i) { return smem_addr(&bars[i]); };
+
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
+        *abort_flag = 0;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(LY::TMEM_COLS));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (warp == 0) {
+        int carry = 0;
+        bool ovf = false;
+        for (int base = 0; base < p.B; base += 32) {
+            const int b = base + lane;
+            const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
+            const bool valid = L >= 0 && L < p.Lmax;
+            ovf |= (b < p.B) && (L >= p.Lmax);
+            int v = valid ? ((L + TM) / TM) * segs : 0;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const int y = __shfl_up_sync(FULL, v, m);
+                if (lane >= m) v += y;
+            }
+            if (b < p.B) {
+                P[b + 1] = carry + v;
+                Ls[b] = valid ? L : -1;
+            }
+            carry += __shfl_sync(FULL, v, 31);
+        }
+        if (lane == 0) P[0] = 0;
+        if (__any_sync(FULL, ovf) && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
+    }
+    fence_mbar_init();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        if (P[b + 1] == P[b]) {
+            float4* o4 = reinterpret_cast<float4*>(p.out + static_cast<size_t>(b) * p.Hq * D);
+            for (int i = tid; i < p.Hq * D / 4; i += blockDim.x) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+
+    const long long U = P[p.B];
+    const long long W = gridDim.x;
+    const int wid = blockIdx.x;
+    const int t_begin = static_cast<int>(wid * U / W);
+    const int n_my = static_cast<int>((wid + 1) * U / W) - t_begin;
+
+    if (n_my > 0) {
+        if (warp == 0) {
+            // ------------------------------------------------ TMA producer
+            if (lane == 0) {
+                Cursor cu = locate(t_begin, P, p.B, segs);
+                int k = 0;
+                for (; k < n_my; ++k) {
+                    const int s = k % NS;
+                    if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag)) break;
+                    const int kvh = cu.seg / p.nhb;
+                    const int row0 = (cu.b * p.Hkv + kvh) * p.Lmax + cu.tile * TM;
+                    const uint32_t st = smem_addr(stages + s * tc::STAGE);
+                    mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
+                    tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s));
+                    tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s));
+                    tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s));
+                    tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s));
+                    if (k + 1 < n_my) advance(cu, P, segs);
+                }
+                if (k < n_my) {
+                    // aborted: let the copies already issued land before the block exits
+                    for (int kk = max(0, k - NS); kk < k; ++kk)
+                        mbar_wait_bounded(bar(kBarFull + kk % NS), (kk / NS) & 1, p.err);
+                }
+            }
+        } else if (warp == 1) {
+            // ------------------------------------------- append + MMA issue
+            // All 32 lanes walk every stage phase in order (a waiter that skipped
+            // phases could be fooled by the parity of an older one); the lanes
+            // patch the last tile of a segment together, lane 0 issues the MMAs.
+            Cursor cu = locate(t_begin, P, p.B, segs);
+            const uint32_t id_s = tc::instr_desc(BF, TM, N, false);
+            const uint32_t id_o = tc::instr_desc(BF, D, N, true);
+            int qcount = 0;
+            bool ok = true;
+            auto issue_pv = [&](int kk) -> bool {
+                const bool w = tc::wait_or_abort(bar(kBarPFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
+                if (__any_sync(FULL, !w)) return false;
+                if (lane == 0) {
+                    tc::tc_fence_after();
+                    const uint32_t vbase = smem_addr(stages + (kk % NS) * tc::STAGE + 2 * KB);
+                    const uint32_t pbase = smem_addr(Ps + (kk & 1) * PSZ);
+#pragma unroll
+                    for (int ks = 0; ks < TM / 16; ++ks) {
+                        const uint64_t a = tc::smem_desc_sw128(vbase + ks * 2048, tc::kVLbo, tc::kVSbo);
+                        const uint64_t bd = tc::smem_desc_sw128(pbase + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+                        tc::mma_f16(tmem + 2 * N + (kk & 1) * N, a, bd, id_o, ks > 0);
+                    }
+                    tc::mma_commit(bar(kBarOFull + (kk & 1)));
+                    tc::mma_commit(bar(kBarEmpty + kk % NS));
+                }
+                __syncwarp();
+                return true;
+            };
+            for (int k = 0; k < n_my; ++k) {
+                const int s = k % NS;
+                const bool new_piece = (k == 0) || (cu.tile == 0);
+                const bool last = cu.tile == cu.nt - 1;
+                if (k > 0 && new_piece && !issue_pv(k - 1)) { ok = false; break; }
+                const bool wf = tc::wait_or_abort(bar(kBarFull + s), (k / NS) & 1, p.err, abort_flag);
+                if (__any_sync(FULL, !wf)) { ok = false; break; }
+                if (last) {
+                    // ---- append the new token and zero staged V rows past the end ----
+                    const int L = Ls[cu.b];
+                    const int t0 = cu.tile * TM;
+                    const int n_total = L + 1 - t0;  // 1 .. TM
+                    const int nr = n_total - 1;      // row of the new token
+                    const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
+                    unsigned char* st = stages + s * tc::STAGE;
+                    const int nz = (TM - n_total) * 8;
+                    for (int c = lane; c < 2 * nz; c += 32) {
+                        const int box = c / nz, rem = c - box * nz;
+                        const int r = n_total + (rem >> 3);
+                        *reinterpret_cast<uint4*>(st + 2 * KB + box * KB + r * 128 + (rem & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    const bool isv = lane >= 16;  // lanes 0-15: K row, 16-31: V row, 8 elements each
+                    const int d0 = (lane & 15) * 8;
+                    const void* src = isv ? p.v_new : p.k_new;
+                    const size_t si = (static_cast<size_t>(cu.b) * p.Hkv + kvh) * D + d0;
+                    const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + d0;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float x0 = ld_qkv(src, p.qkv_dtype, si + 2 * e);
+                        float x1 = ld_qkv(src, p.qkv_dtype, si + 2 * e + 1);
+                        if (p.bias) {
+                            x0 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e);
+                            x1 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e + 1);
+                        }
+                        const CT y0 = tc::to_ct<CT>(x0), y1 = tc::to_ct<CT>(x1);
+                        uint16_t u0, u1;
+                        memcpy(&u0, &y0, 2);
+                        memcpy(&u1, &y1, 2);
+                        w[e] = static_cast<uint32_t>(u0) | (static_cast<uint32_t>(u1) << 16);
+                    }
+                    const uint4 wv = make_uint4(w[0], w[1], w[2], w[3]);
+                    unsigned char* srow = st + (isv ? 2 * KB : 0) + (d0 >> 6) * KB + nr * 128 +
+                                          ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
+                    *reinterpret_cast<uint4*>(srow) = wv;
+                    if (hb == 0) {
+                        const size_t rowg = (static_cast<size_t>(cu.b) * p.Hkv + kvh) * p.Lmax + L;
+                        *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + (rowg * D + d0) * 2) = wv;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (new_piece) {
+                    const bool wq = tc::wait_or_abort(bar(kBarQReady), qcount & 1, p.err, abort_flag);
+                    if (__any_sync(FULL, !wq)) { ok = false; break; }
+                    ++qcount;
+                }
+                if (lane == 0) {
+                    tc::tc_fence_after();
+                    const uint32_t kbase = smem_addr(stages + s * tc::STAGE);
+                    const uint32_t qbase = smem_addr(Qs);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t a = tc::smem_desc_sw128(kbase + (ks >> 2) * KB + (ks & 3) * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(qbase + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+                        tc::mma_f16(tmem + (k & 1) * N, a, bd, id_s, ks > 0);
+                    }
+                    tc::mma_commit(bar(kBarSFull + (k & 1)));
+                }
+                __syncwarp();
+                if (k > 0 && !new_piece && !issue_pv(k - 1)) { ok = false; break; }
+                if (k + 1 < n_my) advance(cu, P, segs);
+            }
+            if (ok) issue_pv(n_my - 1);
+        } else if (warp >= 4) {
+            // ------------------------------------------------ softmax and output
+            const int r = tid - 128;  // TMEM lane = row of S = dimension of O
+            const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
+            const int q4 = warp - 4;
+            Cursor cu = locate(t_begin, P, p.B, segs);
+            float m[G], l[G], o[G], al[G];
+            bool pending = false;
+            int piece_first = cu.tile;
+            auto acc_o = [&](int kk) -> bool {
+                const bool okw = tc::wait_or_abort(bar(kBarOFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
+                if (tc::bar_any(2, 128, !okw)) return false;
+                tc::tc_fence_after();
+                __syncwarp();
+                float ov[N];
+                tc::tmem_ld<N>(tmem + lane_base + 2 * N + (kk & 1) * N, ov);
+#pragma unroll
+                for (int j = 0; j < G; ++j) o[j] = al[j] * o[j] + (ov[j] + ov[G + j]);
+                return true;
+            };
+            for (int k = 0; k < n_my; ++k) {
+                const bool new_piece = (k == 0) || (cu.tile == 0);
+                const bool last = cu.tile == cu.nt - 1;
+                const int L = Ls[cu.b];
+                const int t0 = cu.tile * TM;
+                const int n_total = min(TM, L + 1 - t0);
+                const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
+                if (new_piece) {
+                    piece_first = cu.tile;
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const int h = kvh * p.group + hb * G + j;
+                        float x = ld_qkv(p.q, p.qkv_dtype, (static_cast<size_t>(cu.b) * p.Hq + h) * D + r);
+                        if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + r);
+                        x *= p.qscale;
+                        const CT hi = tc::to_ct<CT>(x);
+                        const CT lo = tc::to_ct<CT>(x - tc::from_ct<CT>(hi));
+                        *reinterpret_cast<CT*>(Qs + tc::sw128_offset(j, r, N)) = hi;
+                        *reinterpret_cast<CT*>(Qs + tc::sw128_offset(G + j, r, N)) = lo;
+                        m[j] = -INFINITY;
+                        l[j] = 0.f;
+                        o[j] = 0.f;
+                    }
+                    fence_proxy_async_smem();
+                    tc::named_bar_sync(1, 128);
+                    if (r == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarQReady)) : "memory");
+                }
+                // ---- scores of this tile ----
+                const bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag);
+                if (tc::bar_any(2, 128, !oks)) break;
+                tc::tc_fence_after();
+                __syncwarp();
+                float sv[N];
+                tc::tmem_ld<N>(tmem + lane_base + (k & 1) * N, sv);
+                const bool valid = r < n_total;
+                float sc[G];
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    sc[j] = valid ? sv[j] + sv[G + j] : -INFINITY;
+                    float v = sc[j];
+#pragma unroll
+                    for (int mm = 16; mm >= 1; mm >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, mm));
+                    if (lane == 0) red_max[q4 * G + j] = v;
+                }
+                tc::named_bar_sync(1, 128);
+                float alpha[G];
+                unsigned char* pb = Ps + (k & 1) * PSZ;
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const float tmax = fmaxf(fmaxf(red_max[j], red_max[G + j]), fmaxf(red_max[2 * G + j], red_max[3 * G + j]));
+                    const float mnew = fmaxf(m[j], tmax);
+                    alpha[j] = exp2f(m[j] - mnew);
+                    const float pj = valid ? exp2f(sc[j] - mnew) : 0.f;
+                    l[j] = l[j] * alpha[j] + pj;
+                    m[j] = mnew;
+                    const CT hi = tc::to_ct<CT>(pj);
+                    const CT lo = tc::to_ct<CT>(pj - tc::from_ct<CT>(hi));
+                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(j, r, N)) = hi;
+                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(G + j, r, N)) = lo;
+                }
+                fence_proxy_async_smem();
+                tc::tc_fence_before();
+                tc::named_bar_sync(1, 128);
+                if (r == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + (k & 1))) : "memory");
+                if (pending && !acc_o(k - 1)) break;
+#pragma unroll
+                for (int j = 0; j < G; ++j) al[j] = alpha[j];
+                pending = true;
+
+                if (last || k == n_my - 1) {
+                    if (!acc_o(k)) break;
+                    pending = false;
+                    // ---- end of a piece ----
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        float v = l[j];
+#pragma unroll
+                        for (int mm = 16; mm >= 1; mm >>= 1) v += __shfl_xor_sync(FULL, v, mm);
+                        if (lane == 0) red_sum[q4 * G + j] = v;
+                    }
+                    tc::named_bar_sync(1, 128);
+                    float lt[G];
+#pragma unroll
+                    for (int j = 0; j < G; ++j) lt[j] = red_sum[j] + red_sum[G + j] + red_sum[2 * G + j] + red_sum[3 * G + j];
+                    const int segg = cu.b * segs + cu.seg;
+                    if (piece_first == 0 && last) {
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            const int h = kvh * p.group + hb * G + j;
+                            p.out[(static_cast<size_t>(cu.b) * p.Hq + h) * D + r] = o[j] / lt[j];
+                        }
+                    } else {
+                        float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
+                        if (r == 0) {
+#pragma unroll
+                            for (int j = 0; j < G; ++j) {
+                                slot[j] = m[j];
+                                slot[G + j] = lt[j];
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < G; ++j) slot[LY::OOFF + j * D + r] = o[j];
+                        __threadfence();
+                        tc::named_bar_sync(1, 128);
+                        const uint32_t piece_tiles = static_cast<uint32_t>(cu.tile - piece_first + 1);
+                        if (r == 0) {
+                            const uint32_t prev = atomicAdd(&p.counters[segg], piece_tiles);
+                            bcast[0] = (prev + piece_tiles == static_cast<uint32_t>(cu.nt)) ? 1 : 0;
+                        }
+                        tc::named_bar_sync(1, 128);
+                        if (bcast[0]) {
+                            __threadfence();
+                            const long long S0 = P[cu.b] + static_cast<long long>(cu.seg) * cu.nt;
+                            const int wf = worker_of(S0, U, W);
+                            const int wl = worker_of(S0 + cu.nt - 1, U, W);
+#pragma unroll 1
+                            for (int j = 0; j < G; ++j) {
+                                float mx = -INFINITY;
+                                for (int w = wf; w <= wl; ++w)
+                                    if ((w * U) / W < ((w + 1) * U) / W)
+                                        mx = fmaxf(mx, __ldcg(p.ws + static_cast<size_t>(segg + w) * LY::SLOT + j));
+                                float lsum = 0.f, acc = 0.f;
+                                for (int w = wf; w <= wl; ++w) {
+                                    if (!((w * U) / W < ((w + 1) * U) / W)) continue;
+                                    const float* sl = p.ws + static_cast<size_t>(segg + w) * LY::SLOT;
+                                    const float f = exp2f(__ldcg(sl + j) - mx);
+                                    lsum += f * __ldcg(sl + G + j);
+                                    acc += f * __ldcg(sl + LY::OOFF + j * D + r);
+                                }
+                                const int h = kvh * p.group + hb * G + j;
+                                p.out[(static_cast<size_t>(cu.b) * p.Hq + h) * D + r] = acc / lsum;
+                            }
+                            if (r == 0) p.counters[segg] = 0u;
+                        }
+                        tc::named_bar_sync(1, 128);
+                    }
+                }
+                if (k + 1 < n_my) advance(cu, P, segs);
+            }
+        }
+    }
+
+    __syncwarp();
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LY::TMEM_COLS));
+    }
+}
+
+// ---------------------------------------------------------- host selection
+struct TcKernelInfo {
+    const void* fn;
+    int smem;
+    int slot_floats;
+    int G;
+};
+
+template <typename CT, int G>
+TcKernelInfo tc_kernel_info() {
+    using LY = tc::Layout<G>;
+    return TcKernelInfo{reinterpret_cast<const void*>(&decode_gqa_tc_kernel<CT, G>), LY::SMEM, LY::SLOT, G};
+}
+
+TcKernelInfo select_tc(bool bf16, int G);
+
+}  // namespace ftd

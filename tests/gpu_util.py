@@ -27,12 +27,26 @@ def host(t, like):
     return a.view(like.dtype) if a.dtype != like.dtype else a
 
 
-def run_step(w, inp, step=None, softmax_scale=0.0, use_bias=True):
+def make_step(w, softmax_scale=0.0, force_cuda_core=False):
+    """A library context; force_cuda_core selects the CUDA-core kernel for grouped caches."""
+    import os
+    old = os.environ.get("FTD_FORCE_CUDA_CORE")
+    os.environ["FTD_FORCE_CUDA_CORE"] = "1" if force_cuda_core else "0"
+    try:
+        return ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, softmax_scale)
+    finally:
+        if old is None:
+            del os.environ["FTD_FORCE_CUDA_CORE"]
+        else:
+            os.environ["FTD_FORCE_CUDA_CORE"] = old
+
+
+def run_step(w, inp, step=None, softmax_scale=0.0, use_bias=True, force_cuda_core=False):
     """One decode step on the GPU with caller-owned device buffers."""
     import torch
     own = step is None
     if own:
-        step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, softmax_scale)
+        step = make_step(w, softmax_scale, force_cuda_core)
     q, kn, vn = dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"])
     bias = dev(inp["bias"]) if (use_bias and inp.get("bias") is not None) else None
     kc, vc, sl = dev(inp["k_cache"]), dev(inp["v_cache"]), dev(inp["seq_lens"])

@@ -31,13 +31,13 @@ def small(cache, qkv, B, Hq, Hkv, D, Lmax, lens, bias=0.1, seed=11):
     return w, gen_all(w, seed=seed, seq_lens=np.array(lens, np.int32), fill_beyond="nan")
 
 
-def check_step(w, inp, softmax_scale=0.0, use_bias=True, what=""):
+def check_step(w, inp, softmax_scale=0.0, use_bias=True, what="", force_cuda_core=False):
     o = oracle.load()
     ref_inp = dict(inp)
     if not use_bias:
         ref_inp["bias"] = None
-    ref = o.decode_step(w, ref_inp, softmax_scale=softmax_scale)
-    got = run_step(w, inp, softmax_scale=softmax_scale, use_bias=use_bias)
+    ref = o.decode_step(w, ref_inp, softmax_scale=softmax_scale, nthreads=8)
+    got = run_step(w, inp, softmax_scale=softmax_scale, use_bias=use_bias, force_cuda_core=force_cuda_core)
     assert_same_bytes(got["k_cache"], ref["k_cache"], f"{what} K cache after append")
     assert_same_bytes(got["v_cache"], ref["v_cache"], f"{what} V cache after append")
     if w.cache_dtype == "i8":
@@ -64,12 +64,36 @@ def test_dtype_grid(cache, qkv, D):
     check_step(w, inp, what=f"{cache}/{qkv}/D{D}")
 
 
-@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (16, 2), (32, 1), (24, 8), (12, 2)])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 8), (8, 4), (8, 2), (8, 1), (16, 2), (16, 1), (32, 1), (64, 8), (24, 8),
+                                     (12, 2)])
 @pytest.mark.parametrize("cache", ["bf16", "f16", "i8"])
-def test_gqa_mqa(Hq, Hkv, cache):
+@pytest.mark.parametrize("path", ["auto", "cuda_core"])
+def test_gqa_mqa(Hq, Hkv, cache, path):
+    """Groups of 8 or 16 query heads on fp16/bf16 caches take the tensor-core kernel under "auto"."""
     qkv = "f16" if cache == "i8" else cache
     w, inp = small(cache, qkv, B=3, Hq=Hq, Hkv=Hkv, D=128, Lmax=512, lens=[511, 37, 200])
-    check_step(w, inp, what=f"gqa {Hq}/{Hkv} {cache}")
+    check_step(w, inp, what=f"gqa {Hq}/{Hkv} {cache} {path}", force_cuda_core=path == "cuda_core")
+
+
+@pytest.mark.parametrize("lens", [[16000], [127], [128], [0], [129, 255, 256, 383, 1000, 3]])
+@pytest.mark.parametrize("cache", ["bf16", "f16"])
+def test_tensor_core_gqa_tile_edges(lens, cache):
+    """Tensor-core path: 128-row tile edges, one token, and a long sequence merged across many CTAs."""
+    Lmax = 16384 if max(lens) >= 4096 else 1024
+    w, inp = small(cache, cache, B=len(lens), Hq=16, Hkv=2, D=128, Lmax=Lmax, lens=lens)
+    check_step(w, inp, what=f"tc edges {lens} {cache}")
+
+
+@pytest.mark.parametrize("cache", ["bf16", "f16"])
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
+    (16, 8, 1, 8192, [8191] * 16),                                    # ~6.7 tiles per CTA, G = 8
+    (8, 32, 2, 8192, [8191, 4000, 7000, 129, 8000, 6143, 5000, 7777]),  # G = 16, ragged
+])
+def test_tensor_core_many_tiles_per_cta(cache, B, Hq, Hkv, Lmax, lens):
+    """Each CTA streams several 128-row tiles through its stage ring and starts new
+    segments mid-range: the case that exposed a waiter skipping barrier phases."""
+    w, inp = small(cache, cache, B=B, Hq=Hq, Hkv=Hkv, D=128, Lmax=Lmax, lens=lens, bias=0.1)
+    check_step(w, inp, what=f"tc many tiles {B}x{Hq}/{Hkv} {cache}")
 
 
 def test_inactive_and_overflow_slots():
