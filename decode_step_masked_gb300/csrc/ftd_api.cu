@@ -106,8 +106,8 @@ struct ftd_ctx {
     bool use_tc = false;       // grouped-query fp16/bf16 caches run on the tensor cores
     ftd::TcKernelInfo tki{};
     int tc_nhb = 1;
-    alignas(64) CUtensorMap tmk;
-    alignas(64) CUtensorMap tmv;
+    CUtensorMap tmk;  // the type carries its own alignment
+    CUtensorMap tmv;
     const void* tm_k_base = nullptr;
     const void* tm_v_base = nullptr;
     float qscale = 0.f;

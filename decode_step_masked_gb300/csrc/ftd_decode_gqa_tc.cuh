@@ -549,22 +549,38 @@ __global__ void __launch_bounds__(256, 1)
                             const long long S0 = P[cu.b] + static_cast<long long>(cu.seg) * cu.nt;
                             const int wf = worker_of(S0, U, W);
                             const int wl = worker_of(S0 + cu.nt - 1, U, W);
-#pragma unroll 1
+                            // one pass over the pieces with a running log-sum-exp; all loads
+                            // of a piece are independent, so each piece costs one L2 round trip
+                            float Mx[G], Ls_[G], Ac[G];
+#pragma unroll
                             for (int j = 0; j < G; ++j) {
-                                float mx = -INFINITY;
-                                for (int w = wf; w <= wl; ++w)
-                                    if ((w * U) / W < ((w + 1) * U) / W)
-                                        mx = fmaxf(mx, __ldcg(p.ws + static_cast<size_t>(segg + w) * LY::SLOT + j));
-                                float lsum = 0.f, acc = 0.f;
-                                for (int w = wf; w <= wl; ++w) {
-                                    if (!((w * U) / W < ((w + 1) * U) / W)) continue;
-                                    const float* sl = p.ws + static_cast<size_t>(segg + w) * LY::SLOT;
-                                    const float f = exp2f(__ldcg(sl + j) - mx);
-                                    lsum += f * __ldcg(sl + G + j);
-                                    acc += f * __ldcg(sl + LY::OOFF + j * D + r);
+                                Mx[j] = -INFINITY;
+                                Ls_[j] = 0.f;
+                                Ac[j] = 0.f;
+                            }
+                            for (int w = wf; w <= wl; ++w) {
+                                if (!((w * U) / W < ((w + 1) * U) / W)) continue;
+                                const float* sl = p.ws + static_cast<size_t>(segg + w) * LY::SLOT;
+                                float mw[G], lw[G], ow[G];
+#pragma unroll
+                                for (int j = 0; j < G; ++j) {
+                                    mw[j] = __ldcg(sl + j);
+                                    lw[j] = __ldcg(sl + G + j);
+                                    ow[j] = __ldcg(sl + LY::OOFF + j * D + r);
                                 }
+#pragma unroll
+                                for (int j = 0; j < G; ++j) {
+                                    const float mn = fmaxf(Mx[j], mw[j]);
+                                    const float a = exp2f(Mx[j] - mn), bb = exp2f(mw[j] - mn);
+                                    Ls_[j] = Ls_[j] * a + lw[j] * bb;
+                                    Ac[j] = Ac[j] * a + ow[j] * bb;
+                                    Mx[j] = mn;
+                                }
+                            }
+#pragma unroll
+                            for (int j = 0; j < G; ++j) {
                                 const int h = kvh * p.group + hb * G + j;
-                                p.out[(static_cast<size_t>(cu.b) * p.Hq + h) * D + r] = acc / lsum;
+                                p.out[(static_cast<size_t>(cu.b) * p.Hq + h) * D + r] = Ac[j] / Ls_[j];
                             }
                             if (r == 0) p.counters[segg] = 0u;
                         }

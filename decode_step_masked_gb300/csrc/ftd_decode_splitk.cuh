@@ -121,16 +121,21 @@ __device__ __forceinline__ void ld_cvt(const unsigned char* p, float (&f)[N]) {
             f[4 * k] = u.x; f[4 * k + 1] = u.y; f[4 * k + 2] = u.z; f[4 * k + 3] = u.w;
         }
     } else {  // int8 codes
+        // Integer to float without the int-to-float unit: flipping the sign bit
+        // turns code c into the unsigned byte c + 128; placed as the low
+        // mantissa byte under the exponent of 2^23 (0x4B000000) it forms the
+        // binary32 value 2^23 + c + 128 exactly, and subtracting 2^23 + 128
+        // (also exact) leaves c.  One byte permute and one add per element.
         uint32_t w[N / 4];
         if constexpr (N == 8) {
             const uint2 u = *reinterpret_cast<const uint2*>(p);
-            w[0] = u.x; w[1] = u.y;
+            w[0] = u.x ^ 0x80808080u; w[1] = u.y ^ 0x80808080u;
         } else {
-            w[0] = *reinterpret_cast<const uint32_t*>(p);
+            w[0] = *reinterpret_cast<const uint32_t*>(p) ^ 0x80808080u;
         }
 #pragma unroll
         for (int k = 0; k < N; ++k)
-            f[k] = static_cast<float>(static_cast<int8_t>((w[k / 4] >> (8 * (k % 4))) & 0xffu));
+            f[k] = __uint_as_float(__byte_perm(w[k / 4], 0x4B000000u, 0x7540u + (k % 4))) - 8388736.0f;
     }
 }
 
@@ -546,35 +551,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                     const int wf = worker_of(S0, U, W);
                     const int wl = worker_of(S0 + cc.nt - 1, U, W);
                     auto has_piece = [&](int w) { return (w * U) / W < ((w + 1) * U) / W; };
+                    // one pass over the pieces with a running log-sum-exp per head;
+                    // the loads of a piece are independent (one L2 round trip each)
                     constexpr int DL = D / 32;
-#pragma unroll 1
-                    for (int j = 0; j < G; ++j) {
-                        float mx = -INFINITY;
-                        for (int w = wf + lane; w <= wl; w += 32)
-                            if (has_piece(w)) mx = fmaxf(mx, __ldcg(p.ws + static_cast<size_t>(segg + w) * TL::SLOT + j));
-                        mx = warp_max(mx);
-                        float lsum = 0.f, acc[DL];
+                    float Mx[G], Ls_[G], Ac[G][DL];
 #pragma unroll
-                        for (int e = 0; e < DL; ++e) acc[e] = 0.f;
-                        for (int w = wf; w <= wl; ++w) {
-                            if (!has_piece(w)) continue;
-                            const float* sl = p.ws + static_cast<size_t>(segg + w) * TL::SLOT;
-                            const float f = exp2f(__ldcg(sl + j) - mx);
-                            lsum += f * __ldcg(sl + G + j);
+                    for (int j = 0; j < G; ++j) {
+                        Mx[j] = -INFINITY;
+                        Ls_[j] = 0.f;
+#pragma unroll
+                        for (int e = 0; e < DL; ++e) Ac[j][e] = 0.f;
+                    }
+                    for (int w = wf; w <= wl; ++w) {
+                        if (!has_piece(w)) continue;
+                        const float* sl = p.ws + static_cast<size_t>(segg + w) * TL::SLOT;
+                        float mw[G], lw[G], ow[G][DL];
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            mw[j] = __ldcg(sl + j);
+                            lw[j] = __ldcg(sl + G + j);
                             const float* ov = sl + TL::OOFF + j * D + lane * DL;
                             if constexpr (DL == 4) {
                                 const float4 u = __ldcg(reinterpret_cast<const float4*>(ov));
-                                acc[0] += f * u.x; acc[1] += f * u.y; acc[2] += f * u.z; acc[3] += f * u.w;
+                                ow[j][0] = u.x; ow[j][1] = u.y; ow[j][2] = u.z; ow[j][3] = u.w;
                             } else {
                                 const float2 u = __ldcg(reinterpret_cast<const float2*>(ov));
-                                acc[0] += f * u.x; acc[1] += f * u.y;
+                                ow[j][0] = u.x; ow[j][1] = u.y;
                             }
                         }
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            const float mn = fmaxf(Mx[j], mw[j]);
+                            const float a = exp2f(Mx[j] - mn), bb = exp2f(mw[j] - mn);
+                            Ls_[j] = Ls_[j] * a + lw[j] * bb;
+#pragma unroll
+                            for (int e = 0; e < DL; ++e) Ac[j][e] = Ac[j][e] * a + ow[j][e] * bb;
+                            Mx[j] = mn;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
                         const int h = kvh * p.group + hb * G + j;
                         float* dst = p.out + (static_cast<size_t>(cc.b) * p.Hq + h) * D + lane * DL;
-                        const float inv = 1.f / lsum;
+                        const float inv = 1.f / Ls_[j];
 #pragma unroll
-                        for (int e = 0; e < DL; ++e) dst[e] = acc[e] * inv;
+                        for (int e = 0; e < DL; ++e) dst[e] = Ac[j][e] * inv;
                     }
                     if (lane == 0) p.counters[segg] = 0u;
                 }
