@@ -38,7 +38,15 @@ METRIC = "decode-attention KV-read GB/s (frac of 8 TB/s HBM); µs per decode ste
 EB = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
-                  "decode_step_masked_gb300/csrc/ftd_decode_splitk.cuh")
+                  "decode_step_masked_gb300/csrc/ftd_decode_splitk.cuh",
+                  "decode_step_masked_gb300/csrc/ftd_decode_gqa_tc.cuh")
+
+
+def kernel_name(w) -> str:
+    """The kernel one step of workload ``w`` runs (the library's own selection rule)."""
+    tc = (w.cache_dtype in ("f16", "bf16") and w.D == 128 and (w.Hq // w.Hkv) % 8 == 0
+          and os.environ.get("FTD_FORCE_CUDA_CORE", "0") != "1")
+    return "decode_gqa_tc_kernel" if tc else "decode_splitk_kernel"
 
 
 # ---------------------------------------------------------------- workload
@@ -444,7 +452,7 @@ def main():
                     % (len(pools), by["kv"] / 1e6), parallelism=f"replicas x{world}"),
         roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
                       frac=achieved / peaks["hbm_gbs"], traffic=traffic,
-                      peak_source=f"{peaks['source']} (STREAM-style copy)", kernel="decode_splitk_kernel",
+                      peak_source=f"{peaks['source']} (STREAM-style copy)", kernel=kernel_name(w),
                       bytes_per_launch=by["total"], launch_us=kern_us),
         gpu_launches=int(r["launches"]), clocks=clocks)
     del pools
