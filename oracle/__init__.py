@@ -31,7 +31,7 @@ CODES = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3}
 class _Cfg(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
                 ("D", ctypes.c_int), ("Lmax", ctypes.c_int), ("qkv_dtype", ctypes.c_int),
-                ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_double)]
+                ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_double), ("window", ctypes.c_int)]
 
 
 def build(src: str = _SRC, out_dir: Optional[str] = None, defines=()) -> str:
@@ -109,18 +109,19 @@ class Oracle:
                                o.ctypes.data, p.ctypes.data)
         return o, p
 
-    def decode_step(self, w, inputs: dict, nthreads: int = 1, softmax_scale: float = 0.0):
+    def decode_step(self, w, inputs: dict, nthreads: int = 1, softmax_scale: float = 0.0, window: int = 0):
         """Run one decode step on copies of the caches.
 
         ``w`` needs attributes B, Hq, Hkv, D, Lmax, qkv_dtype, cache_dtype
-        (a ``synthetic.Workload``).  Returns a dict with ``out`` (float64
+        (a ``synthetic.Workload``).  ``window`` > 0 attends only the last
+        ``window`` positions.  Returns a dict with ``out`` (float64
         [B,Hq,D]), the updated ``k_cache`` / ``v_cache`` / ``scales`` and the
         ``overflow`` flag.
         """
         if w.D > 1024:
             raise ValueError("oracle supports head_dim <= 1024")
         cfg = _Cfg(w.B, w.Hq, w.Hkv, w.D, w.Lmax, CODES[w.qkv_dtype], CODES[w.cache_dtype],
-                   float(softmax_scale))
+                   float(softmax_scale), int(window))
         q = np.ascontiguousarray(inputs["q"])
         kn = np.ascontiguousarray(inputs["k_new"])
         vn = np.ascontiguousarray(inputs["v_new"])

@@ -63,7 +63,7 @@ def _quant(row):
     return codes, s
 
 
-def decode_step(w, inp, softmax_scale: float = 0.0):
+def decode_step(w, inp, softmax_scale: float = 0.0, window: int = 0):
     """Same contract as ``Oracle.decode_step`` (returns out, caches, scales, overflow)."""
     B, Hq, Hkv, D, Lmax = w.B, w.Hq, w.Hkv, w.D, w.Lmax
     g = Hq // Hkv
@@ -115,8 +115,9 @@ def decode_step(w, inp, softmax_scale: float = 0.0):
         for h in range(Hq):
             kvh = h // g
             qv = [float(np.float32(q[b, h, d] + bq[h, d])) for d in range(D)]
+            lo = max(0, L + 1 - window) if window > 0 else 0
             scores = []
-            for t in range(L + 1):
+            for t in range(lo, L + 1):
                 acc = 0.0
                 for d in range(D):
                     acc += qv[d] * float(K[b, kvh, t, d])
@@ -125,5 +126,5 @@ def decode_step(w, inp, softmax_scale: float = 0.0):
             ws = [math.exp(s - m) for s in scores]
             tot = sum(ws)
             for d in range(D):
-                out[b, h, d] = sum(ws[t] * float(V[b, kvh, t, d]) for t in range(L + 1)) / tot
+                out[b, h, d] = sum(ws[i] * float(V[b, kvh, lo + i, d]) for i in range(L + 1 - lo)) / tot
     return dict(out=out, k_cache=kc, v_cache=vc, scales=sc, overflow=overflow)

@@ -32,6 +32,9 @@
  *         s_t = scale * sum_d q'_d * K[t][d],   scale = 1/sqrt(D) by default,
  *         p_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u),
  *         o_d = sum_t p_t * V[t][d],
+ *      With a sliding window of W > 0 positions ("10 tricks", pptc.cn,
+ *      section 3.1: keep only the most recent history) the sums run over
+ *      t = max(0, L + 1 - W) .. L instead.
  *      with q head h reading kv head h / (Hq / Hkv) (contiguous groups,
  *      pptc.cn section 3.4 on MQA/GQA).  int8 rows are dequantised as
  *      scale[t] * code before use.  Everything after the binary32 bias add is
@@ -55,6 +58,7 @@ typedef struct {
     int qkv_dtype;    /* q, k_new, v_new, bias: OR_F32 / OR_F16 / OR_BF16 */
     int cache_dtype;  /* OR_F32 / OR_F16 / OR_BF16 / OR_I8 */
     double softmax_scale; /* <= 0 selects 1/sqrt(D) */
+    int window;           /* > 0: attend only the last `window` positions (sliding window) */
 } oracle_cfg;
 
 /* ---- storage formats (IEEE-754 definitions) ---------------------------- */
@@ -234,21 +238,22 @@ int oracle_decode_step(const oracle_cfg* c, const void* q, const void* k_new, co
         for (int d = 0; d < D; ++d) o[d] = 0.0;
         if (L < 0 || L >= Lmax) continue;
         int n = L + 1;
+        int t_lo = (c->window > 0 && n > c->window) ? n - c->window : 0;
         double qd[1024];
         for (int d = 0; d < D; ++d) {
             float qb = bias ? load_elem(bias, c->qkv_dtype, (size_t)h * D + d) : 0.0f;
             qd[d] = (double)(load_elem(q, c->qkv_dtype, (size_t)bh * D + d) + qb);
         }
-        /* plain two-pass softmax over the n visible positions */
+        /* plain two-pass softmax over the visible positions t_lo .. L */
         double m = -INFINITY;
-        for (int t = 0; t < n; ++t) {
+        for (int t = t_lo; t < n; ++t) {
             double s = 0.0;
             for (int d = 0; d < D; ++d) s += qd[d] * dequant(c, k_cache, ks, b, kvh, t, d);
             s *= scale;
             if (s > m) m = s;
         }
         double denom = 0.0;
-        for (int t = 0; t < n; ++t) {
+        for (int t = t_lo; t < n; ++t) {
             double s = 0.0;
             for (int d = 0; d < D; ++d) s += qd[d] * dequant(c, k_cache, ks, b, kvh, t, d);
             s *= scale;

@@ -238,6 +238,23 @@ def pin_workload_tiny(o):
     assert np.array_equal(a["k_cache"], b["k_cache"]) and np.array_equal(a["v_cache"], b["v_cache"])
 
 
+def pin_sliding_window(o):
+    """A window covering the context changes nothing; a window of 1 returns the new V; brute force."""
+    w, inp = _small(cache="bf16", qkv="bf16", B=3, Hq=4, Hkv=2, D=8, Lmax=32, lens=(20, 3, 31))
+    full = o.decode_step(w, inp)
+    assert np.array_equal(o.decode_step(w, inp, window=32)["out"], full["out"]), "window >= context"
+    assert not np.array_equal(o.decode_step(w, inp, window=4)["out"], full["out"]), "window must matter"
+    one = o.decode_step(w, inp, window=1)
+    kvh = np.arange(w.Hq) // w.group
+    for b, L in enumerate(inp["seq_lens"]):
+        v_new = _bf(one["v_cache"][b, :, L, :]).astype(np.float64)
+        assert np.array_equal(one["out"][b], v_new[kvh]), "window 1 -> the new token's V"
+    for win in (2, 5, 17):
+        a = o.decode_step(w, inp, window=win)
+        bb = brute.decode_step(w, inp, window=win)
+        assert np.max(np.abs(a["out"] - bb["out"])) <= 1e-12, f"window {win} vs brute force"
+
+
 ALL_PINS = [pin_bf16_rounding, pin_f16_rounding, pin_quant_i8, pin_attend_closed_forms,
             pin_attend_invariants, pin_brute_force, pin_append_semantics, pin_gqa_mapping,
-            pin_golden, pin_workload_tiny]
+            pin_golden, pin_workload_tiny, pin_sliding_window]

@@ -17,6 +17,8 @@ MUTANTS = {
     "kv_head_modulo": [("kvh = h / g;", "kvh = h % Hkv;")],
     "mask_excludes_new_token": [("int n = L + 1;", "int n = L;")],
     "mask_one_past": [("int n = L + 1;", "int n = L + 2;")],
+    "window_off_by_one": [("n - c->window : 0;", "n - c->window + 1 : 0;")],
+    "window_ignored": [("int t_lo = (c->window > 0 && n > c->window) ? n - c->window : 0;", "int t_lo = 0;")],
     "no_k_bias": [("kf[d] = load_elem(k_new, c->qkv_dtype, i) + kb;",
                    "kf[d] = load_elem(k_new, c->qkv_dtype, i);")],
     "no_q_bias": [("qd[d] = (double)(load_elem(q, c->qkv_dtype, (size_t)bh * D + d) + qb);",
