@@ -24,19 +24,23 @@ FTD_ERR_OOM = 3
 FTD_ERR_CUDA = 4
 FTD_ERR_SEQ_OVERFLOW = 5
 FTD_ERR_DEVICE_TIMEOUT = 6
+FTD_ERR_BAD_PAGE = 7
 
 FTD_F32, FTD_F16, FTD_BF16, FTD_I8 = 0, 1, 2, 3
 DTYPES = {"f32": FTD_F32, "f16": FTD_F16, "bf16": FTD_BF16, "i8": FTD_I8}
 
 # Symbols include/ftd.h declares; the loader checks each one is exported.
-EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_host", "ftd_get_error",
-           "ftd_destroy", "ftd_status_str", "ftd_last_error", "ftd_kernel_launches", "ftd_decode_mha_noalloc")
+EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_paged", "ftd_decode_mha_host",
+           "ftd_get_error", "ftd_destroy", "ftd_status_str", "ftd_last_error", "ftd_kernel_launches",
+           "ftd_decode_mha_noalloc")
 
 
 class FtdConfig(ctypes.Structure):
     _fields_ = [("max_batch", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("max_len", ctypes.c_int), ("qkv_dtype", ctypes.c_int),
-                ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float)]
+                ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float),
+                ("out_dtype", ctypes.c_int), ("window", ctypes.c_int), ("page_size", ctypes.c_int),
+                ("num_pages", ctypes.c_int)]
 
 
 class FtdError(RuntimeError):
@@ -69,6 +73,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     for fn in (lib.ftd_decode_mha, lib.ftd_decode_mha_host):
         fn.argtypes = [P] * 11
         fn.restype = I
+    lib.ftd_decode_mha_paged.argtypes = [P] * 12
+    lib.ftd_decode_mha_paged.restype = I
     lib.ftd_get_error.argtypes = [P]
     lib.ftd_get_error.restype = I
     lib.ftd_destroy.argtypes = [P]
@@ -121,6 +127,12 @@ def ftd_decode_mha(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, s
                                                 scales, out, stream))
 
 
+def ftd_decode_mha_paged(ctx, q, k_new, v_new, qkv_bias, k_pages, v_pages, block_table, seq_lens, scales, out,
+                         stream) -> int:
+    return load_library().ftd_decode_mha_paged(*_ptrs(ctx, q, k_new, v_new, qkv_bias, k_pages, v_pages,
+                                                      block_table, seq_lens, scales, out, stream))
+
+
 def ftd_decode_mha_host(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out,
                         stream) -> int:
     return load_library().ftd_decode_mha_host(*_ptrs(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache,
@@ -157,10 +169,12 @@ class DecodeStep:
     """Owns one library context; calls take torch CUDA tensors (marshalling only)."""
 
     def __init__(self, max_batch, n_q_heads, n_kv_heads, head_dim, max_len, qkv_dtype="bf16",
-                 cache_dtype="bf16", softmax_scale=0.0, stream: Optional[int] = None):
+                 cache_dtype="bf16", softmax_scale=0.0, stream: Optional[int] = None, out_dtype="f32",
+                 window=0, page_size=0, num_pages=0):
         import torch
         self.cfg = FtdConfig(max_batch, n_q_heads, n_kv_heads, head_dim, max_len, DTYPES[qkv_dtype],
-                             DTYPES[cache_dtype], float(softmax_scale))
+                             DTYPES[cache_dtype], float(softmax_scale), DTYPES[out_dtype], int(window),
+                             int(page_size), int(num_pages))
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         st, ctx = ftd_init(self.cfg, s)
         check(st)
@@ -175,8 +189,18 @@ class DecodeStep:
                  stream: Optional[int] = None):
         import torch
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        if self.cfg.page_size:
+            raise ValueError("a paged context takes paged(..., block_table, ...)")
         check(ftd_decode_mha(self.ctx, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(bias), _ptr(k_cache),
                              _ptr(v_cache), _ptr(seq_lens), _ptr(scales), _ptr(out), s))
+
+    def paged(self, q, k_new, v_new, block_table, seq_lens, out, bias=None, k_pages=None, v_pages=None,
+              scales=None, stream: Optional[int] = None):
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        check(ftd_decode_mha_paged(self.ctx, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(bias), _ptr(k_pages),
+                                   _ptr(v_pages), _ptr(block_table), _ptr(seq_lens), _ptr(scales), _ptr(out),
+                                   s))
 
     def get_error(self) -> int:
         return ftd_get_error(self.ctx)

@@ -125,8 +125,11 @@ struct ftd_ctx {
     void* st_v = nullptr;
     void* st_bias = nullptr;
     int32_t* st_lens = nullptr;
-    float* st_out = nullptr;
+    void* st_out = nullptr;
     size_t q_bytes = 0, kv_new_bytes = 0, bias_bytes = 0, out_bytes = 0;
+    size_t rows = 0;         // cache rows (of head_dim elements) in the pool
+    bool paged = false;
+    int pages_per_seq = 0;
     cudaStream_t last_stream = nullptr;
 };
 
@@ -141,6 +144,7 @@ const char* ftd_status_str(ftd_status s) {
         case FTD_ERR_CUDA: return "FTD_ERR_CUDA";
         case FTD_ERR_SEQ_OVERFLOW: return "FTD_ERR_SEQ_OVERFLOW";
         case FTD_ERR_DEVICE_TIMEOUT: return "FTD_ERR_DEVICE_TIMEOUT";
+        case FTD_ERR_BAD_PAGE: return "FTD_ERR_BAD_PAGE";
     }
     return "FTD_ERR_UNKNOWN";
 }
@@ -172,6 +176,13 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
         return fail(FTD_ERR_UNSUPPORTED, "cache_dtype %d", static_cast<int>(c.cache_dtype));
     if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale))
         return fail(FTD_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    if (c.out_dtype != FTD_F32 && c.out_dtype != FTD_F16 && c.out_dtype != FTD_BF16)
+        return fail(FTD_ERR_UNSUPPORTED, "out_dtype %d (F32, F16 or BF16)", static_cast<int>(c.out_dtype));
+    if (c.window < 0) return fail(FTD_ERR_INVALID_ARG, "window %d must be >= 0", c.window);
+    const bool paged = c.page_size != 0;
+    if (paged && (c.page_size < 0 || c.page_size % 128 != 0 || c.num_pages < 1))
+        return fail(FTD_ERR_INVALID_ARG, "page_size %d must be a positive multiple of 128 with num_pages %d >= 1",
+                    c.page_size, c.num_pages);
 
     const int g = c.n_q_heads / c.n_kv_heads;
     int G = 8;
@@ -201,15 +212,19 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
 
     const int grid = sms;  // one persistent CTA per SM
     const size_t B = c.max_batch, Hq = c.n_q_heads, Hkv = c.n_kv_heads, D = c.head_dim, L = c.max_len;
-    const size_t cache_bytes = B * Hkv * L * D * elem_bytes(c.cache_dtype);
-    const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * B * Hkv * L * sizeof(float) : 0;
+    // cache rows of D elements: [B][Hkv][Lmax] contiguous, or [num_pages][Hkv][page_size] paged
+    const size_t rows = paged ? static_cast<size_t>(c.num_pages) * Hkv * c.page_size : B * Hkv * L;
+    if (rows >= (static_cast<size_t>(1) << 31))
+        return fail(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit row indices");
+    const size_t cache_bytes = rows * D * elem_bytes(c.cache_dtype);
+    const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * rows * sizeof(float) : 0;
 
     // Grouped-query fp16/bf16 caches with head_dim 128 and groups of 8 or 16
     // query heads use the tensor-core kernel; FTD_FORCE_CUDA_CORE=1 in the
     // environment at ftd_init selects the CUDA-core kernel instead.
     const char* force = getenv("FTD_FORCE_CUDA_CORE");
     const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
-                         g % 8 == 0 && B * Hkv * L < (static_cast<size_t>(1) << 31) && !(force && force[0] == '1');
+                         g % 8 == 0 && !(force && force[0] == '1');
     ftd::TcKernelInfo tki{};
     int tc_nhb = 1;
     if (want_tc && encode_tiled()) {
@@ -241,7 +256,10 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     ctx->q_bytes = B * Hq * D * qeb;
     ctx->kv_new_bytes = B * Hkv * D * qeb;
     ctx->bias_bytes = (Hq + 2 * Hkv) * D * qeb;
-    ctx->out_bytes = B * Hq * D * sizeof(float);
+    ctx->out_bytes = B * Hq * D * static_cast<size_t>(elem_bytes(c.out_dtype));
+    ctx->rows = rows;
+    ctx->paged = paged;
+    ctx->pages_per_seq = paged ? (c.max_len + c.page_size - 1) / c.page_size : 0;
     ctx->n_counters = n_seg;
 
     size_t off = 0;
@@ -276,7 +294,7 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     ctx->st_v = base + o_vn;
     ctx->st_bias = base + o_b;
     ctx->st_lens = reinterpret_cast<int32_t*>(base + o_l);
-    ctx->st_out = reinterpret_cast<float*>(base + o_o);
+    ctx->st_out = base + o_o;
     ctx->last_stream = static_cast<cudaStream_t>(stream);
 
     e = cudaMemsetAsync(ctx->pool, 0, zero_end, static_cast<cudaStream_t>(stream));
@@ -298,8 +316,8 @@ ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** 
 }
 
 static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
-                                const void* bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
-                                float* scales, float* out, cudaStream_t stream) {
+                                const void* bias, void* k_cache, void* v_cache, const int32_t* block_table,
+                                const int32_t* seq_lens, float* scales, void* out, cudaStream_t stream) {
     if (!q || !k_new || !v_new || !seq_lens || !out)
         return fail(FTD_ERR_INVALID_ARG, "q, k_new, v_new, seq_lens and out must be non-NULL");
     if (!k_cache) k_cache = ctx->k_cache;
@@ -323,7 +341,9 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     p.bias = bias;
     p.k_cache = static_cast<unsigned char*>(k_cache);
     p.v_cache = static_cast<unsigned char*>(v_cache);
-    const size_t plane = static_cast<size_t>(c.max_batch) * c.n_kv_heads * c.max_len;
+    if (ctx->paged && (!block_table || (reinterpret_cast<uintptr_t>(block_table) & 3u)))
+        return fail(FTD_ERR_INVALID_ARG, "a paged context needs a 4-byte aligned block table");
+    const size_t plane = ctx->rows;
     p.k_scales = i8 ? scales : nullptr;
     p.v_scales = i8 ? scales + plane : nullptr;
     p.seq_lens = seq_lens;
@@ -339,10 +359,16 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     p.nhb = ctx->nhb;
     p.qkv_dtype = static_cast<int>(c.qkv_dtype);
     p.qscale = ctx->qscale;
+    p.out_dtype = static_cast<int>(c.out_dtype);
+    p.window = c.window;
+    p.block_table = ctx->paged ? block_table : nullptr;
+    p.pages_per_seq = ctx->pages_per_seq;
+    p.page_size = c.page_size;
+    p.num_pages = c.num_pages;
 
     cudaError_t e;
     if (ctx->use_tc) {
-        const size_t rows = static_cast<size_t>(c.max_batch) * c.n_kv_heads * c.max_len;
+        const size_t rows = ctx->rows;
         const bool bf16 = c.cache_dtype == FTD_BF16;
         if (ctx->tm_k_base != k_cache) {
             if (!encode_cache_map(&ctx->tmk, k_cache, bf16, rows))
@@ -371,18 +397,30 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
 
 ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                           const void* qkv_bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
-                          float* scales, float* out, void* stream) {
+                          float* scales, void* out, void* stream) {
     g_last_error.clear();
     if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha: ctx is NULL");
-    return launch_decode(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out,
+    if (ctx->paged) return fail(FTD_ERR_INVALID_ARG, "the context is paged: use ftd_decode_mha_paged");
+    return launch_decode(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, nullptr, seq_lens, scales, out,
+                         static_cast<cudaStream_t>(stream));
+}
+
+ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                                const void* qkv_bias, void* k_pages, void* v_pages, const int32_t* block_table,
+                                const int32_t* seq_lens, float* scales, void* out, void* stream) {
+    g_last_error.clear();
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_paged: ctx is NULL");
+    if (!ctx->paged) return fail(FTD_ERR_INVALID_ARG, "the context is not paged (page_size 0)");
+    return launch_decode(ctx, q, k_new, v_new, qkv_bias, k_pages, v_pages, block_table, seq_lens, scales, out,
                          static_cast<cudaStream_t>(stream));
 }
 
 ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                const void* qkv_bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
-                               float* scales, float* out, void* stream) {
+                               float* scales, void* out, void* stream) {
     g_last_error.clear();
     if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_host: ctx is NULL");
+    if (ctx->paged) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_host serves contiguous caches only");
     if (!q || !k_new || !v_new || !seq_lens || !out)
         return fail(FTD_ERR_INVALID_ARG, "q, k_new, v_new, seq_lens and out must be non-NULL");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -399,7 +437,7 @@ ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, c
         if (e != cudaSuccess) return cuda_fail(e, "host-to-device copy of the bias");
     }
     ftd_status st = launch_decode(ctx, ctx->st_q, ctx->st_k, ctx->st_v, qkv_bias ? ctx->st_bias : nullptr,
-                                  k_cache, v_cache, ctx->st_lens, scales, ctx->st_out, s);
+                                  k_cache, v_cache, nullptr, ctx->st_lens, scales, ctx->st_out, s);
     if (st != FTD_OK) return st;
     e = cudaMemcpyAsync(out, ctx->st_out, ctx->out_bytes, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return cuda_fail(e, "device-to-host copy of the output");
@@ -425,6 +463,8 @@ ftd_status ftd_get_error(ftd_ctx* ctx) {
         if (e != cudaSuccess) return cuda_fail(e, "clearing the split-K counters");
         return fail(FTD_ERR_DEVICE_TIMEOUT, "a decode kernel gave up waiting for a copy");
     }
+    if (h & ftd::kErrBadPage)
+        return fail(FTD_ERR_BAD_PAGE, "a block-table entry was outside [0, num_pages); those slots are undefined");
     return fail(FTD_ERR_SEQ_OVERFLOW, "some seq_lens[b] >= max_len; those slots were skipped");
 }
 

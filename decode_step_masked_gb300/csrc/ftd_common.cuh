@@ -15,6 +15,7 @@ namespace ftd {
 // Sticky device error bits (read and cleared by ftd_get_error).
 constexpr uint32_t kErrSeqOverflow = 1u;
 constexpr uint32_t kErrTimeout = 2u;
+constexpr uint32_t kErrBadPage = 4u;
 
 // A wait on a copy gives up after this many SM clock cycles (about 2 s).
 constexpr long long kWaitLimitCycles = 4000000000LL;
@@ -36,14 +37,72 @@ struct DecodeParams {
     float* k_scales;      // [B][Hkv][Lmax] (int8 caches)
     float* v_scales;
     const int32_t* seq_lens;  // [B]
-    float* out;           // [B][Hq][D]
+    void* out;            // [B][Hq][D], out_dtype
     float* ws;            // split-K partial slots
     uint32_t* counters;   // one arrival counter per segment, zero between launches
     uint32_t* err;        // sticky error word
     int B, Hq, Hkv, Lmax, group, nhb;
     int qkv_dtype;
     float qscale;         // softmax scale * log2(e): scores live in the log2 domain
+    int out_dtype;        // kF32 / kF16 / kBF16
+    int window;           // > 0: attend only the last `window` positions
+    // paged cache: page p of the pool holds rows [p][Hkv][page_size][D];
+    // block_table[b * pages_per_seq + i] is the page of positions [i*page_size, (i+1)*page_size)
+    const int32_t* block_table;  // nullptr: contiguous [B][Hkv][Lmax][D] cache
+    int pages_per_seq, page_size, num_pages;
 };
+
+// First visible position of a slot with L cached tokens (the window start).
+__device__ __forceinline__ int window_start(int L, int window) {
+    const int ctx = L + 1;
+    return (window > 0 && ctx > window) ? ctx - window : 0;
+}
+
+// Row index (in cache rows of D elements) of position `pos` of (slot b, kv head),
+// contiguous or through the block table.  A page outside [0, num_pages) raises
+// the bad-page error and returns -1 (the caller then skips the access).
+__device__ __forceinline__ long long cache_row(const DecodeParams& p, int b, int kvh, int pos, int page) {
+    if (!p.block_table) return (static_cast<long long>(b) * p.Hkv + kvh) * p.Lmax + pos;
+    if (page < 0 || page >= p.num_pages) return -1;
+    return (static_cast<long long>(page) * p.Hkv + kvh) * p.page_size + pos % p.page_size;
+}
+
+__device__ __forceinline__ int page_of(const DecodeParams& p, int b, int pos) {
+    return p.block_table ? __ldg(p.block_table + static_cast<size_t>(b) * p.pages_per_seq + pos / p.page_size) : 0;
+}
+
+// ---------------------------------------------------------------- output
+__device__ __forceinline__ void st_out1(void* out, size_t i, float v, int dt) {
+    if (dt == kF32) static_cast<float*>(out)[i] = v;
+    else if (dt == kF16) static_cast<__half*>(out)[i] = __float2half_rn(v);
+    else static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);
+}
+
+// Four consecutive outputs starting at element i (i a multiple of 4).
+__device__ __forceinline__ void st_out4(void* out, size_t i, float a, float b, float c, float d, int dt) {
+    if (dt == kF32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = make_float4(a, b, c, d);
+    } else if (dt == kF16) {
+        const __half2 x = __floats2half2_rn(a, b), y = __floats2half2_rn(c, d);
+        uint2 u;
+        memcpy(&u.x, &x, 4);
+        memcpy(&u.y, &y, 4);
+        *reinterpret_cast<uint2*>(static_cast<__half*>(out) + i) = u;
+    } else {
+        const __nv_bfloat162 x = __floats2bfloat162_rn(a, b), y = __floats2bfloat162_rn(c, d);
+        uint2 u;
+        memcpy(&u.x, &x, 4);
+        memcpy(&u.y, &y, 4);
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + i) = u;
+    }
+}
+
+// Zero n outputs starting at element i (i and n multiples of 8), by all threads of a block.
+__device__ __forceinline__ void zero_out(void* out, size_t i, int n, int dt) {
+    const int eb = dt == kF32 ? 4 : 2;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(out) + i * eb);
+    for (int k = threadIdx.x; k < n * eb / 16; k += blockDim.x) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+}
 
 // ---------------------------------------------------------------- PTX
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {

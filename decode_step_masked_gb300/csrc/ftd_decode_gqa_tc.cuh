@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(256, 1)
             const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
             const bool valid = L >= 0 && L < p.Lmax;
             ovf |= (b < p.B) && (L >= p.Lmax);
-            int v = valid ? ((L + TM) / TM) * segs : 0;
+            int v = valid ? ((L + TM) / TM - window_start(L, p.window) / TM) * segs : 0;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const int y = __shfl_up_sync(FULL, v, m);
@@ -274,8 +274,7 @@ __global__ void __launch_bounds__(256, 1)
 
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (P[b + 1] == P[b]) {
-            float4* o4 = reinterpret_cast<float4*>(p.out + static_cast<size_t>(b) * p.Hq * D);
-            for (int i = tid; i < p.Hq * D / 4; i += blockDim.x) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            zero_out(p.out, static_cast<size_t>(b) * p.Hq * D, p.Hq * D, p.out_dtype);
         }
     }
 
@@ -290,12 +289,32 @@ __global__ void __launch_bounds__(256, 1)
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
                 Cursor cu = locate(t_begin, P, p.B, segs);
+                int pg_key = -1, pg_val = 0, pn_key = -1, pn_val = 0;  // block-table entries in hand
                 int k = 0;
                 for (; k < n_my; ++k) {
                     const int s = k % NS;
                     if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag)) break;
                     const int kvh = cu.seg / p.nhb;
-                    const int row0 = (cu.b * p.Hkv + kvh) * p.Lmax + cu.tile * TM;
+                    const int t0 = (window_start(Ls[cu.b], p.window) / TM + cu.tile) * TM;
+                    int page = 0;
+                    if (p.block_table) {
+                        const int key = cu.b * p.pages_per_seq + t0 / p.page_size;
+                        if (key != pg_key) {
+                            pg_val = key == pn_key ? pn_val : __ldg(p.block_table + key);
+                            pg_key = key;
+                            if (t0 / p.page_size + 1 < p.pages_per_seq) {
+                                pn_key = key + 1;
+                                pn_val = __ldg(p.block_table + key + 1);
+                            }
+                        }
+                        page = pg_val;
+                    }
+                    long long rb = cache_row(p, cu.b, kvh, t0, page);
+                    if (rb < 0) {  // bad page: flag it and read row 0 instead (the slot's output is undefined)
+                        atomicOr(p.err, kErrBadPage);
+                        rb = 0;
+                    }
+                    const int row0 = static_cast<int>(rb);
                     const uint32_t st = smem_addr(stages + s * tc::STAGE);
                     mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
                     tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s));
@@ -346,10 +365,23 @@ __global__ void __launch_bounds__(256, 1)
                 if (k > 0 && new_piece && !issue_pv(k - 1)) { ok = false; break; }
                 const bool wf = tc::wait_or_abort(bar(kBarFull + s), (k / NS) & 1, p.err, abort_flag);
                 if (__any_sync(FULL, !wf)) { ok = false; break; }
+                if (cu.tile == 0 && p.window > 0) {
+                    // rows of the first tile before the window start get weight 0; zero
+                    // their staged V so stale or non-finite history cannot reach O
+                    const int nlo = window_start(Ls[cu.b], p.window) % TM;
+                    unsigned char* st = stages + s * tc::STAGE;
+                    for (int c = lane; c < 2 * nlo * 8; c += 32) {
+                        const int box = c / (nlo * 8), rem = c - box * nlo * 8;
+                        *reinterpret_cast<uint4*>(st + 2 * KB + box * KB + (rem >> 3) * 128 + (rem & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    if (nlo > 0) fence_proxy_async_smem();
+                    __syncwarp();
+                }
                 if (last) {
                     // ---- append the new token and zero staged V rows past the end ----
                     const int L = Ls[cu.b];
-                    const int t0 = cu.tile * TM;
+                    const int t0 = (window_start(L, p.window) / TM + cu.tile) * TM;
                     const int n_total = L + 1 - t0;  // 1 .. TM
                     const int nr = n_total - 1;      // row of the new token
                     const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
@@ -386,8 +418,9 @@ __global__ void __launch_bounds__(256, 1)
                                           ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
                     *reinterpret_cast<uint4*>(srow) = wv;
                     if (hb == 0) {
-                        const size_t rowg = (static_cast<size_t>(cu.b) * p.Hkv + kvh) * p.Lmax + L;
-                        *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + (rowg * D + d0) * 2) = wv;
+                        const long long rowg = cache_row(p, cu.b, kvh, L, page_of(p, cu.b, L));
+                        if (rowg >= 0)
+                            *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + (rowg * D + d0) * 2) = wv;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -438,8 +471,10 @@ __global__ void __launch_bounds__(256, 1)
                 const bool new_piece = (k == 0) || (cu.tile == 0);
                 const bool last = cu.tile == cu.nt - 1;
                 const int L = Ls[cu.b];
-                const int t0 = cu.tile * TM;
+                const int pos0 = window_start(L, p.window);
+                const int t0 = (pos0 / TM + cu.tile) * TM;
                 const int n_total = min(TM, L + 1 - t0);
+                const int r_lo = max(0, pos0 - t0);  // rows before the window start are masked
                 const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
                 if (new_piece) {
                     piece_first = cu.tile;
@@ -468,7 +503,7 @@ __global__ void __launch_bounds__(256, 1)
                 __syncwarp();
                 float sv[N];
                 tc::tmem_ld<N>(tmem + lane_base + (k & 1) * N, sv);
-                const bool valid = r < n_total;
+                const bool valid = r >= r_lo && r < n_total;
                 float sc[G];
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
@@ -523,7 +558,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                         for (int j = 0; j < G; ++j) {
                             const int h = kvh * p.group + hb * G + j;
-                            p.out[(static_cast<size_t>(cu.b) * p.Hq + h) * D + r] = o[j] / lt[j];
+                            st_out1(p.out, (static_cast<size_t>(cu.b) * p.Hq + h) * D + r, o[j] / lt[j], p.out_dtype);
                         }
                     } else {
                         float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
@@ -580,7 +615,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                             for (int j = 0; j < G; ++j) {
                                 const int h = kvh * p.group + hb * G + j;
-                                p.out[(static_cast<size_t>(cu.b) * p.Hq + h) * D + r] = Ac[j] / Ls_[j];
+                                st_out1(p.out, (static_cast<size_t>(cu.b) * p.Hq + h) * D + r, Ac[j] / Ls_[j],
+                                        p.out_dtype);
                             }
                             if (r == 0) p.counters[segg] = 0u;
                         }

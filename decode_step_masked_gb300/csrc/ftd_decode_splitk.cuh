@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
             const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
             const bool valid = L >= 0 && L < p.Lmax;
             ovf |= (b < p.B) && (L >= p.Lmax);
-            int v = valid ? ((L + T) / T) * segs : 0;  // ceil((L + 1) / T) tiles per segment
+            // tiles per segment: from the tile holding the window start to ceil((L + 1) / T)
+            int v = valid ? ((L + T) / T - window_start(L, p.window) / T) * segs : 0;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const int y = __shfl_up_sync(FULL, v, m);
@@ -285,8 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     // Slots without work (inactive or overflowing) get a zero output.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (P[b + 1] == P[b]) {
-            float4* o4 = reinterpret_cast<float4*>(p.out + static_cast<size_t>(b) * p.Hq * D);
-            for (int i = threadIdx.x; i < p.Hq * D / 4; i += kThreads) o4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            zero_out(p.out, static_cast<size_t>(b) * p.Hq * D, p.Hq * D, p.out_dtype);
         }
     }
 
@@ -298,15 +298,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     if (n_my <= 0) return;
 
     // ---- bulk copies of one tile (lane 0 only) ----
+    // Paged caches: the page of the tile comes from the block table; the entry
+    // of the current page is kept and the next page's entry is loaded early.
+    int pg_key = -1, pg_val = 0, pn_key = -1, pn_val = 0;
     auto issue = [&](int s, const Cursor& cu) {
         const int L = Ls[cu.b];
-        const int t0 = cu.tile * T;
+        const int t0 = (window_start(L, p.window) / T + cu.tile) * T;
         const int n_total = min(T, L + 1 - t0);
         const int n_cache = (cu.tile == cu.nt - 1) ? n_total - 1 : n_total;
         const int kvh = cu.seg / p.nhb;
-        const size_t rowbase = (static_cast<size_t>(cu.b) * p.Hkv + kvh) * p.Lmax + t0;
-        const uint32_t kb = static_cast<uint32_t>(n_cache) * ROW;
-        const uint32_t sb = I8 ? static_cast<uint32_t>((n_cache * 4 + 15) & ~15) : 0u;
+        int page = 0;
+        if (p.block_table) {
+            const int key = cu.b * p.pages_per_seq + t0 / p.page_size;
+            if (key != pg_key) {
+                pg_val = key == pn_key ? pn_val : __ldg(p.block_table + key);
+                pg_key = key;
+                if (t0 / p.page_size + 1 < p.pages_per_seq) {
+                    pn_key = key + 1;
+                    pn_val = __ldg(p.block_table + key + 1);
+                }
+            }
+            page = pg_val;
+        }
+        const long long rb = cache_row(p, cu.b, kvh, t0, page);
+        if (rb < 0) atomicOr(p.err, kErrBadPage);
+        const size_t rowbase = rb < 0 ? 0 : static_cast<size_t>(rb);
+        const uint32_t kb = rb < 0 ? 0u : static_cast<uint32_t>(n_cache) * ROW;
+        const uint32_t sb = (I8 && rb >= 0) ? static_cast<uint32_t>((n_cache * 4 + 15) & ~15) : 0u;
         unsigned char* st = wbase + s * STAGE;
         const uint32_t bar = smem_addr(&bars[s]);
         fence_proxy_async_smem();
@@ -359,11 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         if (!mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((k / SPW) & 1), p.err)) break;
 
         const int L = Ls[cc.b];
-        const int t0 = cc.tile * T;
+        const int pos0 = window_start(L, p.window);
+        const int t0 = (pos0 / T + cc.tile) * T;
         const int n_total = min(T, L + 1 - t0);
+        const int r_lo = max(0, pos0 - t0);  // rows before the window start are masked
         const bool last_tile = cc.tile == cc.nt - 1;
         const int kvh = cc.seg / p.nhb, hb = cc.seg % p.nhb;
-        const size_t rowbase = (static_cast<size_t>(cc.b) * p.Hkv + kvh) * p.Lmax + t0;
 
         // ---- append: the new token is the last visible row of the last tile ----
         if (last_tile) {
@@ -378,8 +397,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                 x[e] = ld_qkv(src, p.qkv_dtype, si + e);
                 if (p.bias) x[e] += ld_qkv(p.bias, p.qkv_dtype, bi + e);  // one binary32 add
             }
+            const long long rowL = cache_row(p, cc.b, kvh, L, page_of(p, cc.b, L));  // cache row of position L
+            const bool gok = rowL >= 0 && hb == 0;  // the first head block writes the cache
             unsigned char* srow = st + (isv ? TILE : 0) + nr * ROW + c * EPL * EB;
-            unsigned char* grow = (isv ? p.v_cache : p.k_cache) + (rowbase + nr) * ROW + c * EPL * EB;
+            unsigned char* grow = (isv ? p.v_cache : p.k_cache) + (gok ? rowL : 0) * ROW + c * EPL * EB;
             if constexpr (I8) {
                 float amax = 0.f;
 #pragma unroll
@@ -398,18 +419,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                 }
                 if constexpr (EPL == 8) {
                     *reinterpret_cast<uint2*>(srow) = make_uint2(w[0], w[1]);
-                    if (hb == 0) *reinterpret_cast<uint2*>(grow) = make_uint2(w[0], w[1]);
+                    if (gok) *reinterpret_cast<uint2*>(grow) = make_uint2(w[0], w[1]);
                 } else {
                     *reinterpret_cast<uint32_t*>(srow) = w[0];
-                    if (hb == 0) *reinterpret_cast<uint32_t*>(grow) = w[0];
+                    if (gok) *reinterpret_cast<uint32_t*>(grow) = w[0];
                 }
                 if (c == 0) {
                     reinterpret_cast<float*>(st + 2 * TILE + (isv ? SCL : 0))[nr] = qs;
-                    if (hb == 0) (isv ? p.v_scales : p.k_scales)[rowbase + nr] = qs;
+                    if (gok) (isv ? p.v_scales : p.k_scales)[rowL] = qs;
                 }
             } else {
                 cvt_st<CT, EPL>(srow, x);
-                if (hb == 0) cvt_st<CT, EPL>(grow, x);
+                if (gok) cvt_st<CT, EPL>(grow, x);
             }
             __syncwarp();
         }
@@ -446,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
 #pragma unroll
         for (int j = 0; j < G; ++j) {
             float sv = -INFINITY;
-            if (r < n_total) {
+            if (r >= r_lo && r < n_total) {
                 sv = sc[j * T + r];
                 if constexpr (I8) sv *= reinterpret_cast<const float*>(st + 2 * TILE)[r];
             }
@@ -463,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
             m[j] = mnew;
             if (lane < T) {
                 float wgt = pv;
-                if constexpr (I8) wgt = r < n_total ? pv * reinterpret_cast<const float*>(st + 2 * TILE + SCL)[r] : 0.f;
+                if constexpr (I8)
+                    wgt = (r >= r_lo && r < n_total) ? pv * reinterpret_cast<const float*>(st + 2 * TILE + SCL)[r] : 0.f;
                 pb[j * T + r] = wgt;
             }
         }
@@ -477,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
 #pragma unroll
         for (int i = 0; i < R; ++i) {
             const int row = 2 * i + hr;
-            if (row < n_total) {
+            if (row >= r_lo && row < n_total) {
                 float vf[EPL];
                 ld_cvt<CT, EPL>(Vt + row * ROW + c * EPL * EB, vf);
 #pragma unroll
@@ -509,12 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                     for (int j = 0; j < G; ++j) {
                         const int h = kvh * p.group + hb * G + j;
                         const float inv = 1.f / l[j];
-                        float* dst = p.out + (static_cast<size_t>(cc.b) * p.Hq + h) * D + c * EPL;
+                        const size_t dst = (static_cast<size_t>(cc.b) * p.Hq + h) * D + c * EPL;
 #pragma unroll
                         for (int e4 = 0; e4 < EPL / 4; ++e4)
-                            reinterpret_cast<float4*>(dst)[e4] =
-                                make_float4(o[j][4 * e4] * inv, o[j][4 * e4 + 1] * inv, o[j][4 * e4 + 2] * inv,
-                                            o[j][4 * e4 + 3] * inv);
+                            st_out4(p.out, dst + 4 * e4, o[j][4 * e4] * inv, o[j][4 * e4 + 1] * inv,
+                                    o[j][4 * e4 + 2] * inv, o[j][4 * e4 + 3] * inv, p.out_dtype);
                     }
                 }
             } else {
@@ -592,10 +613,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
 #pragma unroll
                     for (int j = 0; j < G; ++j) {
                         const int h = kvh * p.group + hb * G + j;
-                        float* dst = p.out + (static_cast<size_t>(cc.b) * p.Hq + h) * D + lane * DL;
+                        const size_t dst = (static_cast<size_t>(cc.b) * p.Hq + h) * D + lane * DL;
                         const float inv = 1.f / Ls_[j];
+                        if constexpr (DL == 4) {
+                            st_out4(p.out, dst, Ac[j][0] * inv, Ac[j][1] * inv, Ac[j][2] * inv, Ac[j][3] * inv,
+                                    p.out_dtype);
+                        } else {
 #pragma unroll
-                        for (int e = 0; e < DL; ++e) dst[e] = Ac[j][e] * inv;
+                            for (int e = 0; e < DL; ++e) st_out1(p.out, dst + e, Ac[j][e] * inv, p.out_dtype);
+                        }
                     }
                     if (lane == 0) p.counters[segg] = 0u;
                 }

@@ -61,7 +61,7 @@ ftd_status reject(ftd_status s, const char* msg) {
 extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* q, const void* k_new,
                                              const void* v_new, const void* qkv_bias, void* k_cache,
                                              void* v_cache, const int32_t* seq_lens, float* scales,
-                                             float* out, uint32_t* device_err, void* stream) {
+                                             void* out, uint32_t* device_err, void* stream) {
     ftd::set_last_error("");
     if (!cfg) return reject(FTD_ERR_INVALID_ARG, "cfg is NULL");
     const ftd_config c = *cfg;
@@ -75,6 +75,10 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
         return reject(FTD_ERR_UNSUPPORTED, "qkv_dtype must be F32, F16 or BF16");
     if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale))
         return reject(FTD_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    if (c.out_dtype != FTD_F32 && c.out_dtype != FTD_F16 && c.out_dtype != FTD_BF16)
+        return reject(FTD_ERR_UNSUPPORTED, "out_dtype must be F32, F16 or BF16");
+    if (c.window < 0) return reject(FTD_ERR_INVALID_ARG, "window must be >= 0");
+    if (c.page_size != 0) return reject(FTD_ERR_INVALID_ARG, "paged caches need a context (ftd_init)");
     const bool i8 = c.cache_dtype == FTD_I8;
     if (i8 && !scales) return reject(FTD_ERR_INVALID_ARG, "an INT8 cache needs its scales");
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -162,6 +166,8 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
     p.qkv_dtype = static_cast<int>(c.qkv_dtype);
     const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf(static_cast<float>(c.head_dim));
     p.qscale = scale * 1.4426950408889634f;
+    p.out_dtype = static_cast<int>(c.out_dtype);
+    p.window = c.window;
 
     void* args[] = {&p};
     cudaError_t e = cudaLaunchKernel(ki.fn, dim3(ds->sms), dim3(ftd::kThreads), args,

@@ -30,6 +30,19 @@
  * reads kv head h / (Hq / Hkv)) and an INT8 cache with an fp32 scale per
  * (slot, kv head, position) (pptc.cn section 3.1).
  *
+ * Three options the pages name next to the step:
+ *  - out_dtype F16 / BF16: the output is rounded once, to nearest even, from
+ *    the fp32 result, in the precision the following projection reads
+ *    (lpnh.cn section 2.1: the fused kernels run in half precision).
+ *  - window W > 0: sliding-window attention, slot b attends to positions
+ *    max(0, L_b + 1 - W) .. L_b only (pptc.cn section 3.1: keep only the
+ *    recent part of the history in the cache).
+ *  - page_size > 0: a paged cache (intelliparadigm.com section 5.1: the cache
+ *    cut into fixed pages, e.g. 256 tokens each; framerc.cn section 3.2:
+ *    fixed-size blocks mapped like a virtual-memory page table): the cache is
+ *    a pool of pages and a per-slot block table maps positions to pages;
+ *    served by ftd_decode_mha_paged.
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - B = max_batch, Hq = n_q_heads, Hkv = n_kv_heads, D = head_dim,
@@ -43,7 +56,12 @@
  *        cache  [B][Hkv][Lmax][D] cache dtype    (k_cache, v_cache)
  *        scales [2][B][Hkv][Lmax] fp32, plane 0 for K and plane 1 for V
  *                                 (INT8 caches only)
- *        out    [B][Hq][D]        fp32
+ *        out    [B][Hq][D]        out_dtype (fp32 unless the config says)
+ *    A paged context replaces the cache and scale layouts by
+ *        pages  [num_pages][Hkv][page_size][D]  cache dtype (k_pages, v_pages)
+ *        scales [2][num_pages][Hkv][page_size]  fp32 (INT8 caches only)
+ *        block_table [B][ceil(Lmax / page_size)] int32: entry i of slot b is
+ *               the page holding positions i*page_size .. (i+1)*page_size - 1.
  *  - Slots with seq_lens[b] < 0 are inactive: their cache is untouched and
  *    their output is zero.  seq_lens[b] >= Lmax is an overflow: the slot is
  *    skipped the same way and a sticky device error is raised, which
@@ -72,7 +90,8 @@ typedef enum {
     FTD_ERR_OOM = 3,             /* ftd_init could not allocate its pool */
     FTD_ERR_CUDA = 4,            /* a CUDA runtime call failed */
     FTD_ERR_SEQ_OVERFLOW = 5,    /* some seq_lens[b] >= max_len in a past call */
-    FTD_ERR_DEVICE_TIMEOUT = 6   /* a kernel gave up waiting for a copy (bounded wait) */
+    FTD_ERR_DEVICE_TIMEOUT = 6,  /* a kernel gave up waiting for a copy (bounded wait) */
+    FTD_ERR_BAD_PAGE = 7         /* a block-table entry read in a past call was outside [0, num_pages) */
 } ftd_status;
 
 typedef enum { FTD_F32 = 0, FTD_F16 = 1, FTD_BF16 = 2, FTD_I8 = 3 } ftd_dtype;
@@ -86,13 +105,20 @@ typedef struct {
     ftd_dtype qkv_dtype;   /* q, k_new, v_new, bias: F32, F16 or BF16 */
     ftd_dtype cache_dtype; /* F32, F16, BF16 or I8 */
     float softmax_scale;   /* 0 selects 1/sqrt(head_dim) */
+    /* Options; an all-zero tail gives the plain step (fp32 out, full context,
+     * contiguous cache). */
+    ftd_dtype out_dtype;   /* F32 (0), F16 or BF16 */
+    int window;            /* 0: whole context; W > 0: the last W positions */
+    int page_size;         /* 0: contiguous cache; else a multiple of 128 */
+    int num_pages;         /* pages in the pool when page_size > 0 */
 } ftd_config;
 
 typedef struct ftd_ctx ftd_ctx;
 
 /*
  * ftd_init -- validate cfg and pre-allocate the cache pool.
- * One cudaMalloc on the current device holds the K and V caches (zeroed),
+ * One cudaMalloc on the current device holds the K and V caches (zeroed; for
+ * a paged context, num_pages pages of each),
  * the INT8 scale planes, the split-K workspace, the sticky error word and the
  * staging buffers of ftd_decode_mha_host.  Zeroing runs on `stream`.
  * The pool is the pre-allocated buffer of framerc.cn section 3.2 (allocated
@@ -118,15 +144,42 @@ ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** 
  *   seq_lens        : device int32 [B]; read only.
  *   scales          : device fp32 [2][B][Hkv][Lmax] for INT8 caches (NULL
  *                     selects the pool's planes); ignored otherwise.
- *   out             : device fp32 [B][Hq][D]; every element is written.
+ *   out             : device [B][Hq][D] of out_dtype; every element is written.
  *   stream          : cudaStream_t as void*.
  * Launches one kernel; no host synchronisation and no allocation.  Two calls
  * on the same context must not overlap in time (they share the workspace):
  * issue them on one stream, or order their streams with events.
+ * A paged context (page_size > 0) is refused with INVALID_ARG.
  */
 ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                           const void* qkv_bias, void* k_cache, void* v_cache,
-                          const int32_t* seq_lens, float* scales, float* out, void* stream);
+                          const int32_t* seq_lens, float* scales, void* out, void* stream);
+
+/*
+ * ftd_decode_mha_paged -- ftd_decode_mha over a paged cache (intelliparadigm.com
+ * section 5.1, framerc.cn section 3.2: the cache is cut into fixed-size pages
+ * and a block table maps each slot's positions to pages, so the pool holds
+ * the pages in use rather than max_batch x max_len).
+ *   k_pages, v_pages: device pages [num_pages][Hkv][page_size][D]; NULL
+ *                     selects the context's own pool.
+ *   block_table     : device int32 [B][ceil(max_len / page_size)], read only;
+ *                     only entries covering positions 0 .. L_b of active
+ *                     slots are read (the window start's page and on, when a
+ *                     window is set).  The new token goes to position L_b of
+ *                     its page.  Pages must not be shared between the
+ *                     positions that two slots write.
+ *   scales          : device fp32 [2][num_pages][Hkv][page_size] (INT8), NULL
+ *                     selects the pool's planes.
+ * Other arguments as in ftd_decode_mha.  An entry outside [0, num_pages)
+ * raises a sticky device error (FTD_ERR_BAD_PAGE from ftd_get_error); the
+ * kernel then reads nothing through it and writes no cache row for it, and
+ * the output of that slot is undefined.  Refused (INVALID_ARG) on a context
+ * without pages.
+ */
+ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                                const void* qkv_bias, void* k_pages, void* v_pages,
+                                const int32_t* block_table, const int32_t* seq_lens, float* scales,
+                                void* out, void* stream);
 
 /*
  * ftd_decode_mha_host -- the same step for callers whose per-step inputs live
@@ -135,16 +188,17 @@ ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const 
  * caches stay on the device as in ftd_decode_mha (NULL = the pool).  The
  * inputs are copied into the pool's staging buffers on `stream`, the kernel
  * runs, out is copied back, and the call synchronises `stream` before it
- * returns, so out is valid on return.
+ * returns, so out is valid on return.  Contiguous contexts only.
  */
 ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                const void* qkv_bias, void* k_cache, void* v_cache,
-                               const int32_t* seq_lens, float* scales, float* out, void* stream);
+                               const int32_t* seq_lens, float* scales, void* out, void* stream);
 
 /*
  * ftd_get_error -- synchronise the stream of the context's last call, then
  * read and clear the sticky device error word.  Returns FTD_OK,
- * FTD_ERR_SEQ_OVERFLOW, FTD_ERR_DEVICE_TIMEOUT or FTD_ERR_CUDA.
+ * FTD_ERR_SEQ_OVERFLOW, FTD_ERR_BAD_PAGE, FTD_ERR_DEVICE_TIMEOUT or
+ * FTD_ERR_CUDA (the most serious first when several bits are set).
  */
 ftd_status ftd_get_error(ftd_ctx* ctx);
 
@@ -172,7 +226,8 @@ uint64_t ftd_kernel_launches(void);
  * that forbids allocation (which can synchronise the device or fail) after
  * start-up -- and so cannot create a context with ftd_init.
  *
- *   cfg              : shape and dtypes, same rules as ftd_init.
+ *   cfg              : shape, dtypes and options, same rules as ftd_init,
+ *                      except that page_size must be 0 (contiguous caches).
  *   q ... out        : as in ftd_decode_mha, all caller-owned device memory;
  *                      k_cache and v_cache are required (there is no pool), and
  *                      so are scales for an INT8 cache.
@@ -200,7 +255,7 @@ uint64_t ftd_kernel_launches(void);
  */
 ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* q, const void* k_new,
                                   const void* v_new, const void* qkv_bias, void* k_cache,
-                                  void* v_cache, const int32_t* seq_lens, float* scales, float* out,
+                                  void* v_cache, const int32_t* seq_lens, float* scales, void* out,
                                   uint32_t* device_err, void* stream);
 
 #ifdef __cplusplus

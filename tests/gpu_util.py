@@ -27,13 +27,15 @@ def host(t, like):
     return a.view(like.dtype) if a.dtype != like.dtype else a
 
 
-def make_step(w, softmax_scale=0.0, force_cuda_core=False):
-    """A library context; force_cuda_core selects the CUDA-core kernel for grouped caches."""
+def make_step(w, softmax_scale=0.0, force_cuda_core=False, **opts):
+    """A library context; force_cuda_core selects the CUDA-core kernel for grouped caches.
+    opts: out_dtype, window, page_size, num_pages (the config's option fields)."""
     import os
     old = os.environ.get("FTD_FORCE_CUDA_CORE")
     os.environ["FTD_FORCE_CUDA_CORE"] = "1" if force_cuda_core else "0"
     try:
-        return ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, softmax_scale)
+        return ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, softmax_scale,
+                              **opts)
     finally:
         if old is None:
             del os.environ["FTD_FORCE_CUDA_CORE"]
@@ -41,21 +43,26 @@ def make_step(w, softmax_scale=0.0, force_cuda_core=False):
             os.environ["FTD_FORCE_CUDA_CORE"] = old
 
 
-def run_step(w, inp, step=None, softmax_scale=0.0, use_bias=True, force_cuda_core=False):
-    """One decode step on the GPU with caller-owned device buffers."""
+TORCH_OUT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
+
+
+def run_step(w, inp, step=None, softmax_scale=0.0, use_bias=True, force_cuda_core=False, out_dtype="f32",
+             window=0):
+    """One decode step on the GPU with caller-owned device buffers.  The output
+    comes back as float64 (exact for every out_dtype)."""
     import torch
     own = step is None
     if own:
-        step = make_step(w, softmax_scale, force_cuda_core)
+        step = make_step(w, softmax_scale, force_cuda_core, out_dtype=out_dtype, window=window)
     q, kn, vn = dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"])
     bias = dev(inp["bias"]) if (use_bias and inp.get("bias") is not None) else None
     kc, vc, sl = dev(inp["k_cache"]), dev(inp["v_cache"]), dev(inp["seq_lens"])
     sc = dev(inp["scales"]) if inp.get("scales") is not None else None
-    out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=getattr(torch, TORCH_OUT[out_dtype]), device="cuda")
     step(q, kn, vn, sl, out, bias=bias, k_cache=kc, v_cache=vc, scales=sc)
     torch.cuda.synchronize()
     status = step.get_error()
-    res = dict(out=out.cpu().numpy().astype(np.float64), k_cache=host(kc, inp["k_cache"]),
+    res = dict(out=out.double().cpu().numpy(), out_raw=out.cpu(), k_cache=host(kc, inp["k_cache"]),
                v_cache=host(vc, inp["v_cache"]), scales=None if sc is None else sc.cpu().numpy(),
                status=status)
     if own:

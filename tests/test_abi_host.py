@@ -35,14 +35,15 @@ def test_every_declared_symbol_is_exported(lib):
 def test_status_strings(lib):
     for code, name in [(0, "FTD_OK"), (1, "FTD_ERR_INVALID_ARG"), (2, "FTD_ERR_UNSUPPORTED"),
                        (3, "FTD_ERR_OOM"), (4, "FTD_ERR_CUDA"), (5, "FTD_ERR_SEQ_OVERFLOW"),
-                       (6, "FTD_ERR_DEVICE_TIMEOUT")]:
+                       (6, "FTD_ERR_DEVICE_TIMEOUT"), (7, "FTD_ERR_BAD_PAGE")]:
         assert ftd.ftd_status_str(code) == name
     assert ftd.ftd_status_str(99) == "FTD_ERR_UNKNOWN"
 
 
 def cfg(**kw):
     base = dict(max_batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, max_len=256,
-                qkv_dtype=ftd.FTD_BF16, cache_dtype=ftd.FTD_BF16, softmax_scale=0.0)
+                qkv_dtype=ftd.FTD_BF16, cache_dtype=ftd.FTD_BF16, softmax_scale=0.0,
+                out_dtype=ftd.FTD_F32, window=0, page_size=0, num_pages=0)
     base.update(kw)
     return ftd.FtdConfig(*[base[f] for f, _ in ftd.FtdConfig._fields_])
 
@@ -62,6 +63,12 @@ def cfg(**kw):
     (dict(softmax_scale=-1.0), ftd.FTD_ERR_INVALID_ARG),
     (dict(softmax_scale=float("nan")), ftd.FTD_ERR_INVALID_ARG),
     (dict(softmax_scale=float("inf")), ftd.FTD_ERR_INVALID_ARG),
+    (dict(out_dtype=ftd.FTD_I8), ftd.FTD_ERR_UNSUPPORTED),
+    (dict(out_dtype=9), ftd.FTD_ERR_UNSUPPORTED),
+    (dict(window=-1), ftd.FTD_ERR_INVALID_ARG),
+    (dict(page_size=64, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
+    (dict(page_size=-128, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
+    (dict(page_size=128, num_pages=0), ftd.FTD_ERR_INVALID_ARG),
 ])
 def test_init_rejects_bad_config(lib, kw, status):
     st, ctx = ftd.ftd_init(cfg(**kw))
@@ -77,6 +84,7 @@ def test_null_arguments(lib):
     assert out.value is None, "ftd_init must clear *out on failure"
     assert ftd.ftd_decode_mha(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_decode_mha_host(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
+    assert ftd.ftd_decode_mha_paged(0, 16, 16, 16, 0, 16, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_get_error(0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_cache_ptrs(0)[0] == ftd.FTD_ERR_INVALID_ARG
     ftd.ftd_destroy(0)  # no-op
@@ -87,6 +95,23 @@ def test_no_launches_from_host_failures(lib):
     ftd.ftd_init(cfg(max_batch=0))
     ftd.ftd_decode_mha(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0)
     assert ftd.ftd_kernel_launches() == n
+
+
+def test_config_struct_matches_header():
+    """The ctypes mirror lists ftd_config's fields in the header's order."""
+    with open(os.path.join(ROOT, "include", "ftd.h")) as f:
+        text = f.read()
+    body = re.search(r"typedef struct \{(.*?)\} ftd_config;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = re.findall(r"\b([a-z_]+)\s*;", body)
+    assert names == [f for f, _ in ftd.FtdConfig._fields_]
+
+
+def test_noalloc_rejects_paged_and_bad_options(lib):
+    for kw in (dict(page_size=128, num_pages=4), dict(window=-3), dict(out_dtype=ftd.FTD_I8)):
+        st = ftd.ftd_decode_mha_noalloc(cfg(**kw), 16, 16, 16, 0, 16, 16, 16, 0, 16, 0, 0)
+        assert st in (ftd.FTD_ERR_INVALID_ARG, ftd.FTD_ERR_UNSUPPORTED), kw
+        assert ftd.ftd_last_error() != ""
 
 
 def test_missing_library_fails_loudly(tmp_path):
