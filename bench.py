@@ -42,6 +42,12 @@ KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
                   "decode_step_masked_gb300/csrc/ftd_decode_gqa_tc.cuh")
 
 
+# option cases the bench times next to the plain step (half output, window, paged cache)
+OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("13b", dict(page_size=256)),
+                ("70b", dict(out_dtype="bf16")), ("70b", dict(window=1024)), ("70b", dict(page_size=256)),
+                ("int8", dict(page_size=256))]
+
+
 def kernel_name(w) -> str:
     """The kernel one step of workload ``w`` runs (the library's own selection rule)."""
     tc = (w.cache_dtype in ("f16", "bf16") and w.D == 128 and (w.Hq // w.Hkv) % 8 == 0
@@ -50,18 +56,22 @@ def kernel_name(w) -> str:
 
 
 # ---------------------------------------------------------------- workload
-def step_bytes(w, lens) -> dict:
-    """Algorithmic bytes of one step: each cached K/V row once per kv head."""
+def step_bytes(w, lens, window=0, out_dtype="f32") -> dict:
+    """Algorithmic bytes of one step: each visible cached K/V row once per kv head
+    (with a window, only the last ``window`` positions of a slot are visible)."""
     lens = np.asarray(lens, np.int64)
     act = (lens >= 0) & (lens < w.Lmax)
-    ctx = int((lens[act] + 1).sum())
+    vis = lens[act] + 1
+    if window > 0:
+        vis = np.minimum(vis, window)
+    ctx = int(vis.sum())
     nact = int(act.sum())
     eb = EB[w.cache_dtype]
     qeb = EB[w.qkv_dtype]
-    kv_read = 2 * w.Hkv * w.D * eb * int(lens[act].sum())
+    kv_read = 2 * w.Hkv * w.D * eb * (ctx - nact)
     kv_write = 2 * w.Hkv * w.D * eb * nact
     scale_rw = 8 * w.Hkv * ctx if w.cache_dtype == "i8" else 0
-    small = (w.B * w.Hq * w.D + 2 * w.B * w.Hkv * w.D) * qeb + 4 * w.B + 4 * w.B * w.Hq * w.D
+    small = (w.B * w.Hq * w.D + 2 * w.B * w.Hkv * w.D) * qeb + 4 * w.B + EB[out_dtype] * w.B * w.Hq * w.D
     return dict(kv=kv_read + kv_write + scale_rw, total=kv_read + kv_write + scale_rw + small, ctx=ctx)
 
 
@@ -96,17 +106,28 @@ def load_traffic(workload: str):
 
 
 # ---------------------------------------------------------------- device
-def make_pools(w, npools, seed, device):
-    """Seeded synthetic caches drawn on the device (same distributions as the parity inputs)."""
+def page_table(w, page_size, seed):
+    """A paged pool covering every slot to Lmax, pages handed out in a seeded random order."""
+    pps = -(-w.Lmax // page_size)
+    perm = np.random.default_rng([seed, 77]).permutation(w.B * pps).astype(np.int32)
+    return perm.reshape(w.B, pps), w.B * pps
+
+
+def make_pools(w, npools, seed, device, page_size=0):
+    """Seeded synthetic caches drawn on the device (same distributions as the parity inputs);
+    with page_size, each pool is [num_pages][Hkv][page_size][D] (see page_table)."""
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed)
     pools = []
-    shape = (w.B, w.Hkv, w.Lmax, w.D)
+    lead = (w.B, w.Hkv, w.Lmax)
+    if page_size:
+        lead = (page_table(w, page_size, seed)[1], w.Hkv, page_size)
+    shape = lead + (w.D,)
     for _ in range(npools):
         if w.cache_dtype == "i8":
             lo, hi = w.scale_range
-            sc = torch.rand((2, w.B, w.Hkv, w.Lmax), device=device, generator=g) * (hi - lo) + lo
+            sc = torch.rand((2,) + lead, device=device, generator=g) * (hi - lo) + lo
             kc = torch.clamp(torch.round(torch.randn(shape, device=device, generator=g) / sc[0, ..., None]),
                              -128, 127).to(torch.int8)
             vc = torch.clamp(torch.round(torch.randn(shape, device=device, generator=g) / sc[1, ..., None]),
@@ -120,7 +141,7 @@ def make_pools(w, npools, seed, device):
     return pools
 
 
-def make_step_inputs(w, lens, seed, device):
+def make_step_inputs(w, lens, seed, device, out_dtype="f32"):
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed + 1000)
@@ -132,7 +153,8 @@ def make_step_inputs(w, lens, seed, device):
     if w.bias_std is not None:
         bias = (torch.randn(((w.Hq + 2 * w.Hkv) * w.D,), device=device, generator=g) * w.bias_std).to(dt)
     sl = torch.from_numpy(np.asarray(lens, np.int32)).to(device)
-    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=device)
+    odt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[out_dtype]
+    out = torch.empty((w.B, w.Hq, w.D), dtype=odt, device=device)
     return dict(q=q, k_new=kn, v_new=vn, bias=bias, seq_lens=sl, out=out)
 
 
@@ -156,10 +178,14 @@ def run_timed(step, w, pools, inp, steps, warmup, stream, chunk=100):
 
     def one(i):
         kc, vc, sc = pools[i % n]
-        ftd.check(ftd.ftd_decode_mha(step.ctx, inp["q"].data_ptr(), inp["k_new"].data_ptr(),
-                                     inp["v_new"].data_ptr(), 0 if inp["bias"] is None else inp["bias"].data_ptr(),
-                                     kc.data_ptr(), vc.data_ptr(), inp["seq_lens"].data_ptr(),
-                                     0 if sc is None else sc.data_ptr(), inp["out"].data_ptr(), stream.cuda_stream))
+        common = (inp["q"].data_ptr(), inp["k_new"].data_ptr(), inp["v_new"].data_ptr(),
+                  0 if inp["bias"] is None else inp["bias"].data_ptr(), kc.data_ptr(), vc.data_ptr())
+        tail = (inp["seq_lens"].data_ptr(), 0 if sc is None else sc.data_ptr(), inp["out"].data_ptr(),
+                stream.cuda_stream)
+        if inp.get("block_table") is not None:
+            ftd.check(ftd.ftd_decode_mha_paged(step.ctx, *common, inp["block_table"].data_ptr(), *tail))
+        else:
+            ftd.check(ftd.ftd_decode_mha(step.ctx, *common, *tail))
 
     def capture(nsteps):
         g = torch.cuda.CUDAGraph()
@@ -379,14 +405,23 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def measure_config(name, steps, warmup, seed, device, stream):
+def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", window=0, page_size=0):
+    """Time one workload; the options select a half-precision output, a sliding
+    window or a paged cache (one shuffled block table shared by the rotated pools)."""
+    import torch
     import decode_step_masked_gb300 as ftd
     w = WORKLOADS[name]
     lens = gen_seq_lens(w)
-    by = step_bytes(w, lens)
-    pools = make_pools(w, n_pools_for(w, by["kv"]), seed, device)
-    inp = make_step_inputs(w, lens, seed, device)
-    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    by = step_bytes(w, lens, window, out_dtype)
+    # rotation is sized on the bytes a step reads (the visible rows), so each pool leaves L2 between reads
+    pools = make_pools(w, n_pools_for(w, by["kv"]), seed, device, page_size)
+    inp = make_step_inputs(w, lens, seed, device, out_dtype)
+    num_pages = 0
+    if page_size:
+        table, num_pages = page_table(w, page_size, seed)
+        inp["block_table"] = torch.from_numpy(table).to(device)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, out_dtype=out_dtype,
+                          window=window, page_size=page_size, num_pages=num_pages)
     r = run_timed(step, w, pools, inp, steps, warmup, stream)
     step.close()
     us = r["total_ms"] * 1e3 / steps
@@ -472,6 +507,16 @@ def main():
             del pools2
             torch.cuda.empty_cache()
         line["per_config"] = per_cfg
+        # ---- the step's options, each on the workloads of both kernels ----
+        opts = {}
+        for name, kw in OPTION_CASES:
+            w2, _, by2, pools2, _, r2, us2 = measure_config(name, 1000, 50, 99, device, stream, **kw)
+            key = name + ":" + ",".join(f"{k}={v}" for k, v in kw.items())
+            opts[key] = dict(us=us2, gbs=by2["kv"] / us2 / 1e3, frac=by2["kv"] / us2 / 1e3 / peaks["hbm_gbs"],
+                             kv_mb=by2["kv"] / 1e6, kernel=kernel_name(w2))
+            del pools2
+            torch.cuda.empty_cache()
+        line["options"] = opts
         # ---- the float64 oracle on the host cores ----
         cores = os.cpu_count() or 1
         cb = oracle_timing(w, 10.0, cores)

@@ -180,8 +180,8 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
         return fail(FTD_ERR_UNSUPPORTED, "out_dtype %d (F32, F16 or BF16)", static_cast<int>(c.out_dtype));
     if (c.window < 0) return fail(FTD_ERR_INVALID_ARG, "window %d must be >= 0", c.window);
     const bool paged = c.page_size != 0;
-    if (paged && (c.page_size < 0 || c.page_size % 128 != 0 || c.num_pages < 1))
-        return fail(FTD_ERR_INVALID_ARG, "page_size %d must be a positive multiple of 128 with num_pages %d >= 1",
+    if (paged && (c.page_size < 128 || (c.page_size & (c.page_size - 1)) != 0 || c.num_pages < 1))
+        return fail(FTD_ERR_INVALID_ARG, "page_size %d must be a power of two >= 128 with num_pages %d >= 1",
                     c.page_size, c.num_pages);
 
     const int g = c.n_q_heads / c.n_kv_heads;
@@ -363,7 +363,8 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     p.window = c.window;
     p.block_table = ctx->paged ? block_table : nullptr;
     p.pages_per_seq = ctx->pages_per_seq;
-    p.page_size = c.page_size;
+    p.page_shift = 0;
+    while (ctx->paged && (1 << p.page_shift) < c.page_size) ++p.page_shift;
     p.num_pages = c.num_pages;
 
     cudaError_t e;

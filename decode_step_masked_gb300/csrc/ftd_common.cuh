@@ -49,7 +49,7 @@ struct DecodeParams {
     // paged cache: page p of the pool holds rows [p][Hkv][page_size][D];
     // block_table[b * pages_per_seq + i] is the page of positions [i*page_size, (i+1)*page_size)
     const int32_t* block_table;  // nullptr: contiguous [B][Hkv][Lmax][D] cache
-    int pages_per_seq, page_size, num_pages;
+    int pages_per_seq, page_shift, num_pages;  // page_size = 1 << page_shift
 };
 
 // First visible position of a slot with L cached tokens (the window start).
@@ -64,12 +64,34 @@ __device__ __forceinline__ int window_start(int L, int window) {
 __device__ __forceinline__ long long cache_row(const DecodeParams& p, int b, int kvh, int pos, int page) {
     if (!p.block_table) return (static_cast<long long>(b) * p.Hkv + kvh) * p.Lmax + pos;
     if (page < 0 || page >= p.num_pages) return -1;
-    return (static_cast<long long>(page) * p.Hkv + kvh) * p.page_size + pos % p.page_size;
+    return ((static_cast<long long>(page) * p.Hkv + kvh) << p.page_shift) + (pos & ((1 << p.page_shift) - 1));
 }
 
 __device__ __forceinline__ int page_of(const DecodeParams& p, int b, int pos) {
-    return p.block_table ? __ldg(p.block_table + static_cast<size_t>(b) * p.pages_per_seq + pos / p.page_size) : 0;
+    return p.block_table ? __ldg(p.block_table + static_cast<size_t>(b) * p.pages_per_seq + (pos >> p.page_shift))
+                         : 0;
 }
+
+// Block-table entries a copy issuer holds: the entry of the current page and,
+// loaded one page early, the next one, so a tile that starts a page seldom
+// waits for a table load.
+struct PageCursor {
+    int key = -1, val = 0, nkey = -1, nval = 0;
+    __device__ __forceinline__ int page(const DecodeParams& p, int b, int t0) {
+        if (!p.block_table) return 0;
+        const int i = t0 >> p.page_shift;
+        const int k = b * p.pages_per_seq + i;
+        if (k != key) {
+            val = k == nkey ? nval : __ldg(p.block_table + k);
+            key = k;
+            if (i + 1 < p.pages_per_seq) {
+                nkey = k + 1;
+                nval = __ldg(p.block_table + k + 1);
+            }
+        }
+        return val;
+    }
+};
 
 // ---------------------------------------------------------------- output
 __device__ __forceinline__ void st_out1(void* out, size_t i, float v, int dt) {

@@ -289,32 +289,20 @@ __global__ void __launch_bounds__(256, 1)
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
                 Cursor cu = locate(t_begin, P, p.B, segs);
-                int pg_key = -1, pg_val = 0, pn_key = -1, pn_val = 0;  // block-table entries in hand
+                PageCursor pages;
                 int k = 0;
                 for (; k < n_my; ++k) {
                     const int s = k % NS;
-                    if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag)) break;
+                    // the tile's address first: a block-table load then overlaps the wait for a free stage
                     const int kvh = cu.seg / p.nhb;
                     const int t0 = (window_start(Ls[cu.b], p.window) / TM + cu.tile) * TM;
-                    int page = 0;
-                    if (p.block_table) {
-                        const int key = cu.b * p.pages_per_seq + t0 / p.page_size;
-                        if (key != pg_key) {
-                            pg_val = key == pn_key ? pn_val : __ldg(p.block_table + key);
-                            pg_key = key;
-                            if (t0 / p.page_size + 1 < p.pages_per_seq) {
-                                pn_key = key + 1;
-                                pn_val = __ldg(p.block_table + key + 1);
-                            }
-                        }
-                        page = pg_val;
-                    }
-                    long long rb = cache_row(p, cu.b, kvh, t0, page);
+                    long long rb = cache_row(p, cu.b, kvh, t0, pages.page(p, cu.b, t0));
                     if (rb < 0) {  // bad page: flag it and read row 0 instead (the slot's output is undefined)
                         atomicOr(p.err, kErrBadPage);
                         rb = 0;
                     }
                     const int row0 = static_cast<int>(rb);
+                    if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag)) break;
                     const uint32_t st = smem_addr(stages + s * tc::STAGE);
                     mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
                     tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s));

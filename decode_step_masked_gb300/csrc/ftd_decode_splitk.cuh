@@ -300,27 +300,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     // ---- bulk copies of one tile (lane 0 only) ----
     // Paged caches: the page of the tile comes from the block table; the entry
     // of the current page is kept and the next page's entry is loaded early.
-    int pg_key = -1, pg_val = 0, pn_key = -1, pn_val = 0;
+    PageCursor pages;
     auto issue = [&](int s, const Cursor& cu) {
         const int L = Ls[cu.b];
         const int t0 = (window_start(L, p.window) / T + cu.tile) * T;
         const int n_total = min(T, L + 1 - t0);
         const int n_cache = (cu.tile == cu.nt - 1) ? n_total - 1 : n_total;
         const int kvh = cu.seg / p.nhb;
-        int page = 0;
-        if (p.block_table) {
-            const int key = cu.b * p.pages_per_seq + t0 / p.page_size;
-            if (key != pg_key) {
-                pg_val = key == pn_key ? pn_val : __ldg(p.block_table + key);
-                pg_key = key;
-                if (t0 / p.page_size + 1 < p.pages_per_seq) {
-                    pn_key = key + 1;
-                    pn_val = __ldg(p.block_table + key + 1);
-                }
-            }
-            page = pg_val;
-        }
-        const long long rb = cache_row(p, cu.b, kvh, t0, page);
+        const long long rb = cache_row(p, cu.b, kvh, t0, pages.page(p, cu.b, t0));
         if (rb < 0) atomicOr(p.err, kErrBadPage);
         const size_t rowbase = rb < 0 ? 0 : static_cast<size_t>(rb);
         const uint32_t kb = rb < 0 ? 0u : static_cast<uint32_t>(n_cache) * ROW;
@@ -496,18 +483,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         for (int j = 0; j < G; ++j)
 #pragma unroll
             for (int e = 0; e < EPL; ++e) o[j][e] *= alpha[j];
+        auto pv_row = [&](int row) {
+            float vf[EPL];
+            ld_cvt<CT, EPL>(Vt + row * ROW + c * EPL * EB, vf);
 #pragma unroll
-        for (int i = 0; i < R; ++i) {
-            const int row = 2 * i + hr;
-            if (row >= r_lo && row < n_total) {
-                float vf[EPL];
-                ld_cvt<CT, EPL>(Vt + row * ROW + c * EPL * EB, vf);
+            for (int j = 0; j < G; ++j) {
+                const float pj = pb[j * T + row];
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    const float pj = pb[j * T + row];
+                for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pj, vf[e], o[j][e]);
+            }
+        };
+        if (r_lo == 0 && n_total == T) {  // whole tile visible: no per-row test
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pj, vf[e], o[j][e]);
-                }
+            for (int i = 0; i < R; ++i) pv_row(2 * i + hr);
+        } else {  // rows outside [r_lo, n_total) hold stale stage data and are skipped
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                const int row = 2 * i + hr;
+                if (row >= r_lo && row < n_total) pv_row(row);
             }
         }
         __syncwarp();

@@ -109,7 +109,7 @@ typedef struct {
      * contiguous cache). */
     ftd_dtype out_dtype;   /* F32 (0), F16 or BF16 */
     int window;            /* 0: whole context; W > 0: the last W positions */
-    int page_size;         /* 0: contiguous cache; else a multiple of 128 */
+    int page_size;         /* 0: contiguous cache; else a power of two >= 128 */
     int num_pages;         /* pages in the pool when page_size > 0 */
 } ftd_config;
 

@@ -69,6 +69,7 @@ def cfg(**kw):
     (dict(page_size=64, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
     (dict(page_size=-128, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
     (dict(page_size=128, num_pages=0), ftd.FTD_ERR_INVALID_ARG),
+    (dict(page_size=384, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
 ])
 def test_init_rejects_bad_config(lib, kw, status):
     st, ctx = ftd.ftd_init(cfg(**kw))

@@ -34,6 +34,29 @@ def test_gqa_counts_kv_once_per_kv_head():
     assert by["kv"] == 2 * 16 * 8 * 8192 * 128 * 2  # 537 MB: K/V read once per kv head, not per q head
 
 
+def test_step_bytes_window_counts_visible_rows_only():
+    w = WORKLOADS["7b"].with_(B=3)
+    lens = np.array([10, 2047, -1], np.int32)  # short slot, long slot, inactive
+    by = bench.step_bytes(w, lens, window=100)
+    assert by["ctx"] == 11 + 100
+    assert by["kv"] == 2 * w.Hkv * w.D * 2 * (11 + 100)  # reads of visible history + the appended rows
+    assert bench.step_bytes(w, lens, window=0)["ctx"] == 11 + 2048
+
+
+def test_step_bytes_half_output():
+    w = WORKLOADS["70b"]
+    lens = gen_seq_lens(w)
+    assert (bench.step_bytes(w, lens)["total"] - bench.step_bytes(w, lens, out_dtype="bf16")["total"]
+            == 2 * w.B * w.Hq * w.D)
+
+
+def test_page_table_is_a_permutation():
+    w = WORKLOADS["13b"]
+    table, n = bench.page_table(w, 256, 3)
+    assert table.shape == (w.B, w.Lmax // 256) and n == w.B * w.Lmax // 256
+    assert sorted(table.reshape(-1).tolist()) == list(range(n))
+
+
 def test_pool_rotation_exceeds_l2():
     for name in ("7b", "13b", "70b", "int8"):
         w = WORKLOADS[name]
