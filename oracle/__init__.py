@@ -31,7 +31,8 @@ CODES = {"f32": 0, "f16": 1, "bf16": 2, "i8": 3}
 class _Cfg(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int),
                 ("D", ctypes.c_int), ("Lmax", ctypes.c_int), ("qkv_dtype", ctypes.c_int),
-                ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_double), ("window", ctypes.c_int)]
+                ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_double), ("window", ctypes.c_int),
+                ("q_len", ctypes.c_int)]
 
 
 def build(src: str = _SRC, out_dir: Optional[str] = None, defines=()) -> str:
@@ -109,19 +110,22 @@ class Oracle:
                                o.ctypes.data, p.ctypes.data)
         return o, p
 
-    def decode_step(self, w, inputs: dict, nthreads: int = 1, softmax_scale: float = 0.0, window: int = 0):
+    def decode_step(self, w, inputs: dict, nthreads: int = 1, softmax_scale: float = 0.0, window: int = 0,
+                    q_len: Optional[int] = None):
         """Run one decode step on copies of the caches.
 
         ``w`` needs attributes B, Hq, Hkv, D, Lmax, qkv_dtype, cache_dtype
         (a ``synthetic.Workload``).  ``window`` > 0 attends only the last
-        ``window`` positions.  Returns a dict with ``out`` (float64
-        [B,Hq,D]), the updated ``k_cache`` / ``v_cache`` / ``scales`` and the
-        ``overflow`` flag.
+        ``window`` positions.  ``q_len`` > 1 appends that many tokens per slot
+        (q [B,T,Hq,D], k_new / v_new [B,T,Hkv,D]).  Returns a dict with
+        ``out`` (float64 [B,Hq,D], or [B,T,Hq,D] when q_len > 1), the updated
+        ``k_cache`` / ``v_cache`` / ``scales`` and the ``overflow`` flag.
         """
         if w.D > 1024:
             raise ValueError("oracle supports head_dim <= 1024")
+        T = max(1, int(q_len or getattr(w, "q_len", 1)))
         cfg = _Cfg(w.B, w.Hq, w.Hkv, w.D, w.Lmax, CODES[w.qkv_dtype], CODES[w.cache_dtype],
-                   float(softmax_scale), int(window))
+                   float(softmax_scale), int(window), T)
         q = np.ascontiguousarray(inputs["q"])
         kn = np.ascontiguousarray(inputs["k_new"])
         vn = np.ascontiguousarray(inputs["v_new"])
@@ -132,7 +136,9 @@ class Oracle:
         sc = inputs.get("scales")
         sc = None if sc is None else np.array(sc, np.float32, copy=True, order="C")
         lens = np.ascontiguousarray(inputs["seq_lens"], np.int32)
-        out = np.zeros((w.B, w.Hq, w.D), np.float64)
+        if q.size != w.B * T * w.Hq * w.D or kn.size != w.B * T * w.Hkv * w.D:
+            raise ValueError("q / k_new sizes do not match B, q_len and the heads")
+        out = np.zeros((w.B, T, w.Hq, w.D) if T > 1 else (w.B, w.Hq, w.D), np.float64)
         ov = self.lib.oracle_decode_step(
             ctypes.byref(cfg), q.ctypes.data, kn.ctypes.data, vn.ctypes.data,
             None if bias is None else bias.ctypes.data, kc.ctypes.data, vc.ctypes.data,

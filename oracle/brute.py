@@ -63,17 +63,21 @@ def _quant(row):
     return codes, s
 
 
-def decode_step(w, inp, softmax_scale: float = 0.0, window: int = 0):
-    """Same contract as ``Oracle.decode_step`` (returns out, caches, scales, overflow)."""
+def decode_step(w, inp, softmax_scale: float = 0.0, window: int = 0, q_len=None):
+    """Same contract as ``Oracle.decode_step`` (returns out, caches, scales, overflow).
+
+    With q_len = T > 1, q is [B,T,Hq,D] and k_new / v_new [B,T,Hkv,D]: token j
+    goes to position L + j and its query sees positions up to L + j."""
     B, Hq, Hkv, D, Lmax = w.B, w.Hq, w.Hkv, w.D, w.Lmax
+    T = max(1, int(q_len or getattr(w, "q_len", 1)))
     g = Hq // Hkv
     scale = softmax_scale if softmax_scale > 0 else 1.0 / math.sqrt(D)
     kc = np.array(inp["k_cache"], copy=True)
     vc = np.array(inp["v_cache"], copy=True)
     sc = None if inp.get("scales") is None else np.array(inp["scales"], np.float32, copy=True)
-    q = _decode(inp["q"], w.qkv_dtype).astype(np.float32)
-    kn = _decode(inp["k_new"], w.qkv_dtype).astype(np.float32)
-    vn = _decode(inp["v_new"], w.qkv_dtype).astype(np.float32)
+    q = _decode(inp["q"], w.qkv_dtype).astype(np.float32).reshape(B, T, Hq, D)
+    kn = _decode(inp["k_new"], w.qkv_dtype).astype(np.float32).reshape(B, T, Hkv, D)
+    vn = _decode(inp["v_new"], w.qkv_dtype).astype(np.float32).reshape(B, T, Hkv, D)
     bias = inp.get("bias")
     bias = (np.zeros((Hq + 2 * Hkv) * D, np.float32) if bias is None
             else _decode(bias, w.qkv_dtype).astype(np.float32))
@@ -82,15 +86,16 @@ def decode_step(w, inp, softmax_scale: float = 0.0, window: int = 0):
     bv = bias[(Hq + Hkv) * D:].reshape(Hkv, D)
     overflow = False
     for b in range(B):
-        L = int(inp["seq_lens"][b])
-        if L < 0:
+        L0 = int(inp["seq_lens"][b])
+        if L0 < 0:
             continue
-        if L >= Lmax:
+        if L0 + T > Lmax:
             overflow = True
             continue
-        for h in range(Hkv):
-            krow = [np.float32(kn[b, h, d] + bk[h, d]) for d in range(D)]
-            vrow = [np.float32(vn[b, h, d] + bv[h, d]) for d in range(D)]
+        for j, h in ((j, h) for j in range(T) for h in range(Hkv)):
+            L = L0 + j
+            krow = [np.float32(kn[b, j, h, d] + bk[h, d]) for d in range(D)]
+            vrow = [np.float32(vn[b, j, h, d] + bv[h, d]) for d in range(D)]
             if w.cache_dtype == "i8":
                 kq, ks = _quant(krow)
                 vq, vs = _quant(vrow)
@@ -107,14 +112,15 @@ def decode_step(w, inp, softmax_scale: float = 0.0, window: int = 0):
     if w.cache_dtype == "i8":
         K = K * sc[0].astype(np.float64)[..., None]
         V = V * sc[1].astype(np.float64)[..., None]
-    out = np.zeros((B, Hq, D))
+    out = np.zeros((B, T, Hq, D))
     for b in range(B):
-        L = int(inp["seq_lens"][b])
-        if L < 0 or L >= Lmax:
+        L0 = int(inp["seq_lens"][b])
+        if L0 < 0 or L0 + T > Lmax:
             continue
-        for h in range(Hq):
+        for j, h in ((j, h) for j in range(T) for h in range(Hq)):
+            L = L0 + j  # the last position token j sees
             kvh = h // g
-            qv = [float(np.float32(q[b, h, d] + bq[h, d])) for d in range(D)]
+            qv = [float(np.float32(q[b, j, h, d] + bq[h, d])) for d in range(D)]
             lo = max(0, L + 1 - window) if window > 0 else 0
             scores = []
             for t in range(lo, L + 1):
@@ -126,5 +132,7 @@ def decode_step(w, inp, softmax_scale: float = 0.0, window: int = 0):
             ws = [math.exp(s - m) for s in scores]
             tot = sum(ws)
             for d in range(D):
-                out[b, h, d] = sum(ws[i] * float(V[b, kvh, lo + i, d]) for i in range(L + 1 - lo)) / tot
+                out[b, j, h, d] = sum(ws[i] * float(V[b, kvh, lo + i, d]) for i in range(L + 1 - lo)) / tot
+    if T == 1:
+        out = out[:, 0]
     return dict(out=out, k_cache=kc, v_cache=vc, scales=sc, overflow=overflow)

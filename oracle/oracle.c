@@ -39,6 +39,13 @@
  *      pptc.cn section 3.4 on MQA/GQA).  int8 rows are dequantised as
  *      scale[t] * code before use.  Everything after the binary32 bias add is
  *      computed in float64.
+ *   4. Several new tokens per step (q_len = T > 1; pptc.cn section 4.3,
+ *      speculative decoding: the large model checks a run of draft tokens in
+ *      one forward pass).  Token j of slot b is appended at position L + j,
+ *      and its query attends to positions 0 .. L + j (with a window W, from
+ *      max(0, L + j + 1 - W)): each draft token sees the cache and the draft
+ *      tokens before it, as T single-token steps in a row would.  A slot with
+ *      L + T > Lmax is an overflow.
  *
  * Plain loops, no blocking, no fusion: a reader can check each line against
  * the formulas above.
@@ -59,6 +66,7 @@ typedef struct {
     int cache_dtype;  /* OR_F32 / OR_F16 / OR_BF16 / OR_I8 */
     double softmax_scale; /* <= 0 selects 1/sqrt(D) */
     int window;           /* > 0: attend only the last `window` positions (sliding window) */
+    int q_len;            /* new tokens per slot in this step; 0 counts as 1 */
 } oracle_cfg;
 
 /* ---- storage formats (IEEE-754 definitions) ---------------------------- */
@@ -180,14 +188,16 @@ static double dequant(const oracle_cfg* c, const void* cache, const float* scale
     return (double)load_elem(cache, c->cache_dtype, i);
 }
 
-/* Appends k_new/v_new (+ bias) into the caches, then writes out[B][Hq][D].
- * bias: NULL or [(Hq + 2*Hkv) * D] laid out as q | k | v.
+/* Appends k_new/v_new (+ bias) into the caches, then writes out[B][T][Hq][D].
+ * q: [B][T][Hq][D]; k_new, v_new: [B][T][Hkv][D] (T = q_len).
+ * bias: NULL or [(Hq + 2*Hkv) * D] laid out as q | k | v, the same for every token.
  * scales: [2][B][Hkv][Lmax] fp32 when cache_dtype is int8, else ignored.
- * Returns 1 when some slot had seq_lens[b] >= Lmax, else 0. */
+ * Returns 1 when some slot had seq_lens[b] + T > Lmax, else 0. */
 int oracle_decode_step(const oracle_cfg* c, const void* q, const void* k_new, const void* v_new,
                        const void* bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
                        float* scales, double* out, int nthreads) {
     const int B = c->B, Hq = c->Hq, Hkv = c->Hkv, D = c->D, Lmax = c->Lmax;
+    const int T = c->q_len > 1 ? c->q_len : 1;
     const int g = Hq / Hkv;
     const double scale = c->softmax_scale > 0.0 ? c->softmax_scale : 1.0 / sqrt((double)D);
     const size_t plane = (size_t)B * Hkv * Lmax;
@@ -197,12 +207,13 @@ int oracle_decode_step(const oracle_cfg* c, const void* q, const void* k_new, co
     float kf[1024], vf[1024];
     int8_t code[1024];
     for (int b = 0; b < B; ++b) {
-        int L = seq_lens[b];
-        if (L < 0) continue;
-        if (L >= Lmax) { overflow = 1; continue; }
+        if (seq_lens[b] < 0) continue;
+        if (seq_lens[b] > Lmax - T) { overflow = 1; continue; }
+        for (int j = 0; j < T; ++j)
         for (int h = 0; h < Hkv; ++h) {
+            const int L = seq_lens[b] + j; /* position of token j */
             for (int d = 0; d < D; ++d) {
-                size_t i = ((size_t)b * Hkv + h) * D + d;
+                size_t i = (((size_t)b * T + j) * Hkv + h) * D + d;
                 float kb = bias ? load_elem(bias, c->qkv_dtype, (size_t)(Hq + h) * D + d) : 0.0f;
                 float vb = bias ? load_elem(bias, c->qkv_dtype, (size_t)(Hq + Hkv + h) * D + d) : 0.0f;
                 kf[d] = load_elem(k_new, c->qkv_dtype, i) + kb;
@@ -223,21 +234,20 @@ int oracle_decode_step(const oracle_cfg* c, const void* q, const void* k_new, co
         }
     }
 
-    /* step 3: attention per (slot, query head) */
+    /* step 3: attention per (slot, token, query head) */
     const float* ks = scales;
     const float* vs = scales ? scales + plane : NULL;
-    long npairs = (long)B * Hq;
+    long npairs = (long)B * T * Hq;
 #ifdef _OPENMP
     if (nthreads < 1) nthreads = 1;
 #pragma omp parallel for schedule(dynamic) num_threads(nthreads)
 #endif
     for (long bh = 0; bh < npairs; ++bh) {
-        int b = (int)(bh / Hq), h = (int)(bh % Hq), kvh = h / g;
-        int L = seq_lens[b];
+        int b = (int)(bh / ((long)T * Hq)), j = (int)(bh / Hq % T), h = (int)(bh % Hq), kvh = h / g;
         double* o = out + (size_t)bh * D;
         for (int d = 0; d < D; ++d) o[d] = 0.0;
-        if (L < 0 || L >= Lmax) continue;
-        int n = L + 1;
+        if (seq_lens[b] < 0 || seq_lens[b] > Lmax - T) continue;
+        int n = seq_lens[b] + j + 1; /* token j sees positions 0 .. L + j */
         int t_lo = (c->window > 0 && n > c->window) ? n - c->window : 0;
         double qd[1024];
         for (int d = 0; d < D; ++d) {

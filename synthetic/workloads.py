@@ -53,6 +53,7 @@ class Workload:
     scale_range: tuple = (0.01, 0.05)
     seed: int = 0
     description: str = ""
+    q_len: int = 1   # new tokens per slot per step (> 1: a speculative verification step)
     extra: dict = field(default_factory=dict)
 
     @property
@@ -128,11 +129,13 @@ def gen_seq_lens(w: Workload, seed: Optional[int] = None) -> np.ndarray:
 
 
 def gen_qkv(w: Workload, seed: Optional[int] = None):
-    """q [B,Hq,D], k_new / v_new [B,Hkv,D] ~ N(0,1); bias [(Hq+2Hkv)*D] or None."""
+    """q [B,Hq,D], k_new / v_new [B,Hkv,D] ~ N(0,1); bias [(Hq+2Hkv)*D] or None.
+    With q_len T > 1 the token axis follows the slot axis: q [B,T,Hq,D], k_new [B,T,Hkv,D]."""
     seed = w.seed if seed is None else seed
-    q = _rng(seed, _STREAM_Q).standard_normal((w.B, w.Hq, w.D), dtype=np.float32)
-    k = _rng(seed, _STREAM_KNEW).standard_normal((w.B, w.Hkv, w.D), dtype=np.float32)
-    v = _rng(seed, _STREAM_VNEW).standard_normal((w.B, w.Hkv, w.D), dtype=np.float32)
+    tok = (w.q_len,) if w.q_len > 1 else ()
+    q = _rng(seed, _STREAM_Q).standard_normal((w.B,) + tok + (w.Hq, w.D), dtype=np.float32)
+    k = _rng(seed, _STREAM_KNEW).standard_normal((w.B,) + tok + (w.Hkv, w.D), dtype=np.float32)
+    v = _rng(seed, _STREAM_VNEW).standard_normal((w.B,) + tok + (w.Hkv, w.D), dtype=np.float32)
     bias = None
     if w.bias_std is not None:
         n = (w.Hq + 2 * w.Hkv) * w.D

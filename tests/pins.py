@@ -14,7 +14,8 @@ The facts used:
   * invariances: a constant added to every key, permuting positions;
   * softmax weights summing to one; the large-score limit;
   * GQA: kv head h // group, and equality with MHA on repeated K/V;
-  * a pure-Python brute force (``oracle/brute.py``) on tiny decode steps.
+  * a pure-Python brute force (``oracle/brute.py``) on tiny decode steps;
+  * a step of T new tokens equals T single-token steps in a row.
 """
 from __future__ import annotations
 
@@ -144,9 +145,9 @@ def _bf(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def _small(cache="f32", qkv="f32", B=2, Hq=4, Hkv=2, D=8, Lmax=16, lens=(5, 11), bias=0.1, seed=7):
+def _small(cache="f32", qkv="f32", B=2, Hq=4, Hkv=2, D=8, Lmax=16, lens=(5, 11), bias=0.1, seed=7, q_len=1):
     w = Workload("pin", B=B, Hq=Hq, Hkv=Hkv, D=D, Lmax=Lmax, qkv_dtype=qkv, cache_dtype=cache,
-                 lens=("fixed", 0), bias_std=bias, seed=seed)
+                 lens=("fixed", 0), bias_std=bias, seed=seed, q_len=q_len)
     inp = gen_all(w, seed=seed, seq_lens=np.array(lens, np.int32), fill_beyond="nan")
     return w, inp
 
@@ -255,6 +256,59 @@ def pin_sliding_window(o):
         assert np.max(np.abs(a["out"] - bb["out"])) <= 1e-12, f"window {win} vs brute force"
 
 
+def _same_bytes(a, b):
+    return np.array_equal(np.ascontiguousarray(a).view(np.uint8), np.ascontiguousarray(b).view(np.uint8))
+
+
+def pin_multi_token(o):
+    """T new tokens per step: brute force on tiny steps; equal to T single-token steps in a row;
+    the overflow edge L + T = Lmax (fits) vs Lmax + 1 (flagged); a window of 1 returns each
+    token's own V."""
+    cases = [dict(cache="f32", qkv="f32", q_len=2, lens=(5, 13)),
+             dict(cache="bf16", qkv="bf16", q_len=3, lens=(0, 12)),
+             dict(cache="i8", qkv="f16", q_len=4, lens=(7, 1)),
+             dict(cache="f16", qkv="f16", q_len=5, Hq=4, Hkv=1, lens=(10, 3))]
+    for kw in cases:
+        w, inp = _small(**kw)
+        T = w.q_len
+        a = o.decode_step(w, inp)
+        bb = brute.decode_step(w, inp)
+        assert a["out"].shape == (w.B, T, w.Hq, w.D)
+        assert not a["overflow"] and not bb["overflow"], kw
+        assert np.max(np.abs(a["out"] - bb["out"])) <= 1e-12, f"q_len vs brute force {kw}"
+        assert _same_bytes(a["k_cache"], bb["k_cache"]) and _same_bytes(a["v_cache"], bb["v_cache"]), kw
+        for win in (1, 3):
+            aw = o.decode_step(w, inp, window=win)
+            bw = brute.decode_step(w, inp, window=win)
+            assert np.max(np.abs(aw["out"] - bw["out"])) <= 1e-12, f"q_len window {win} {kw}"
+        # T single-token steps, each appending one token and advancing the lengths
+        w1 = w.with_(q_len=1)
+        cur = dict(inp)
+        for j in range(T):
+            step = dict(cur, q=inp["q"][:, j], k_new=inp["k_new"][:, j], v_new=inp["v_new"][:, j],
+                        seq_lens=inp["seq_lens"] + j)
+            r1 = o.decode_step(w1, step)
+            assert np.max(np.abs(r1["out"] - a["out"][:, j])) <= 1e-13, f"token {j} vs single steps {kw}"
+            cur = dict(cur, k_cache=r1["k_cache"], v_cache=r1["v_cache"], scales=r1["scales"])
+        assert _same_bytes(cur["k_cache"], a["k_cache"]) and _same_bytes(cur["v_cache"], a["v_cache"]), kw
+        if w.cache_dtype == "i8":
+            assert _same_bytes(cur["scales"], a["scales"]), kw
+    # the overflow edge: L + T = Lmax fits, Lmax + 1 does not
+    w, inp = _small(cache="bf16", qkv="bf16", q_len=3, lens=(13, 14))
+    r = o.decode_step(w, inp)
+    assert r["overflow"], "L + T > Lmax must raise the overflow flag"
+    assert r["out"][0].any() and not r["out"][1].any(), "slot 0 fits (13 + 3 = 16), slot 1 does not"
+    assert _same_bytes(r["k_cache"][1], inp["k_cache"][1]), "an overflowing slot keeps its cache"
+    # window 1: every token sees only itself
+    w, inp = _small(cache="f32", qkv="f32", q_len=3, lens=(4, 9))
+    one = o.decode_step(w, inp, window=1)
+    kvh = np.arange(w.Hq) // w.group
+    for b, L in enumerate(inp["seq_lens"]):
+        for j in range(3):
+            v = one["v_cache"][b, :, L + j, :].astype(np.float64)
+            assert np.array_equal(one["out"][b, j], v[kvh]), "window 1 -> the token's own V"
+
+
 ALL_PINS = [pin_bf16_rounding, pin_f16_rounding, pin_quant_i8, pin_attend_closed_forms,
             pin_attend_invariants, pin_brute_force, pin_append_semantics, pin_gqa_mapping,
-            pin_golden, pin_workload_tiny, pin_sliding_window]
+            pin_golden, pin_workload_tiny, pin_sliding_window, pin_multi_token]

@@ -15,8 +15,15 @@ MUTANTS = {
     "no_softmax_scale": [("s *= scale;", "s *= 1.0;")],
     "default_scale_1_over_D": [("1.0 / sqrt((double)D)", "1.0 / (double)D")],
     "kv_head_modulo": [("kvh = h / g;", "kvh = h % Hkv;")],
-    "mask_excludes_new_token": [("int n = L + 1;", "int n = L;")],
-    "mask_one_past": [("int n = L + 1;", "int n = L + 2;")],
+    "mask_excludes_new_token": [("int n = seq_lens[b] + j + 1;", "int n = seq_lens[b] + j;")],
+    "mask_one_past": [("int n = seq_lens[b] + j + 1;", "int n = seq_lens[b] + j + 2;")],
+    "multi_all_tokens_see_all": [("int n = seq_lens[b] + j + 1;", "int n = seq_lens[b] + T;")],
+    "multi_tokens_see_first_only": [("int n = seq_lens[b] + j + 1;", "int n = seq_lens[b] + 1;")],
+    "multi_append_one_row": [("const int L = seq_lens[b] + j; /* position of token j */",
+                              "const int L = seq_lens[b]; /* position of token j */")],
+    "multi_knew_ignores_token": [("size_t i = (((size_t)b * T + j) * Hkv + h) * D + d;",
+                                  "size_t i = (((size_t)b * T) * Hkv + h) * D + d;")],
+    "multi_token_index_swapped": [("j = (int)(bh / Hq % T)", "j = (int)(bh % T)")],
     "window_off_by_one": [("n - c->window : 0;", "n - c->window + 1 : 0;")],
     "window_ignored": [("int t_lo = (c->window > 0 && n > c->window) ? n - c->window : 0;", "int t_lo = 0;")],
     "no_k_bias": [("kf[d] = load_elem(k_new, c->qkv_dtype, i) + kb;",
@@ -42,8 +49,8 @@ MUTANTS = {
                                 "return (((size_t)b * c->Hkv + h) * c->D + d) * c->Lmax + pos;")],
     "append_one_row_early": [("store_elem(k_cache, c->cache_dtype, cache_index(c, b, h, L, d), kf[d]);",
                               "store_elem(k_cache, c->cache_dtype, cache_index(c, b, h, L > 0 ? L - 1 : 0, d), kf[d]);")],
-    "overflow_not_flagged": [("if (L >= Lmax) { overflow = 1; continue; }",
-                              "if (L >= Lmax) { overflow = 0; continue; }")],
+    "overflow_not_flagged": [("if (seq_lens[b] > Lmax - T) { overflow = 1; continue; }",
+                              "if (seq_lens[b] > Lmax - T) { overflow = 0; continue; }")],
     "i8_dequant_ignores_scale": [("return s * (double)((const int8_t*)cache)[i];",
                                   "return (double)((const int8_t*)cache)[i];")],
     "i8_v_scale_from_k_plane": [("oracle_quant_i8(vf, D, code, &scales[plane + si]);",
