@@ -45,33 +45,37 @@ KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
 # option cases the bench times next to the plain step (half output, window, paged cache)
 OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("13b", dict(page_size=256)),
                 ("70b", dict(out_dtype="bf16")), ("70b", dict(window=1024)), ("70b", dict(page_size=256)),
-                ("int8", dict(page_size=256))]
+                ("int8", dict(page_size=256)), ("7b", dict(q_len=4)), ("7b", dict(q_len=8)),
+                ("70b", dict(q_len=4))]
 
 
-def kernel_name(w) -> str:
+def kernel_name(w, q_len=1) -> str:
     """The kernel one step of workload ``w`` runs (the library's own selection rule)."""
-    tc = (w.cache_dtype in ("f16", "bf16") and w.D == 128 and (w.Hq // w.Hkv) % 8 == 0
+    tc = (w.cache_dtype in ("f16", "bf16") and w.D == 128 and (max(1, q_len) * w.Hq // w.Hkv) % 8 == 0
           and os.environ.get("FTD_FORCE_CUDA_CORE", "0") != "1")
     return "decode_gqa_tc_kernel" if tc else "decode_splitk_kernel"
 
 
 # ---------------------------------------------------------------- workload
-def step_bytes(w, lens, window=0, out_dtype="f32") -> dict:
+def step_bytes(w, lens, window=0, out_dtype="f32", q_len=1) -> dict:
     """Algorithmic bytes of one step: each visible cached K/V row once per kv head
-    (with a window, only the last ``window`` positions of a slot are visible)."""
+    (with a window, only rows some new token still sees), plus the q_len appended
+    rows per slot."""
     lens = np.asarray(lens, np.int64)
-    act = (lens >= 0) & (lens < w.Lmax)
-    vis = lens[act] + 1
+    T = max(1, int(q_len))
+    act = (lens >= 0) & (lens + T <= w.Lmax)
+    vis = lens[act] + T                       # history rows read + new rows written
     if window > 0:
-        vis = np.minimum(vis, window)
+        vis = np.minimum(vis, window + T - 1)
     ctx = int(vis.sum())
     nact = int(act.sum())
     eb = EB[w.cache_dtype]
     qeb = EB[w.qkv_dtype]
-    kv_read = 2 * w.Hkv * w.D * eb * (ctx - nact)
-    kv_write = 2 * w.Hkv * w.D * eb * nact
+    kv_read = 2 * w.Hkv * w.D * eb * (ctx - T * nact)
+    kv_write = 2 * w.Hkv * w.D * eb * T * nact
     scale_rw = 8 * w.Hkv * ctx if w.cache_dtype == "i8" else 0
-    small = (w.B * w.Hq * w.D + 2 * w.B * w.Hkv * w.D) * qeb + 4 * w.B + EB[out_dtype] * w.B * w.Hq * w.D
+    small = ((w.B * w.Hq * w.D + 2 * w.B * w.Hkv * w.D) * qeb * T + 4 * w.B
+             + EB[out_dtype] * w.B * T * w.Hq * w.D)
     return dict(kv=kv_read + kv_write + scale_rw, total=kv_read + kv_write + scale_rw + small, ctx=ctx)
 
 
@@ -141,20 +145,21 @@ def make_pools(w, npools, seed, device, page_size=0):
     return pools
 
 
-def make_step_inputs(w, lens, seed, device, out_dtype="f32"):
+def make_step_inputs(w, lens, seed, device, out_dtype="f32", q_len=1):
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed + 1000)
     dt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[w.qkv_dtype]
-    q = torch.randn((w.B, w.Hq, w.D), device=device, generator=g).to(dt)
-    kn = torch.randn((w.B, w.Hkv, w.D), device=device, generator=g).to(dt)
-    vn = torch.randn((w.B, w.Hkv, w.D), device=device, generator=g).to(dt)
+    tok = (q_len,) if q_len > 1 else ()
+    q = torch.randn((w.B,) + tok + (w.Hq, w.D), device=device, generator=g).to(dt)
+    kn = torch.randn((w.B,) + tok + (w.Hkv, w.D), device=device, generator=g).to(dt)
+    vn = torch.randn((w.B,) + tok + (w.Hkv, w.D), device=device, generator=g).to(dt)
     bias = None
     if w.bias_std is not None:
         bias = (torch.randn(((w.Hq + 2 * w.Hkv) * w.D,), device=device, generator=g) * w.bias_std).to(dt)
     sl = torch.from_numpy(np.asarray(lens, np.int32)).to(device)
     odt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[out_dtype]
-    out = torch.empty((w.B, w.Hq, w.D), dtype=odt, device=device)
+    out = torch.empty((w.B,) + tok + (w.Hq, w.D), dtype=odt, device=device)
     return dict(q=q, k_new=kn, v_new=vn, bias=bias, seq_lens=sl, out=out)
 
 
@@ -405,23 +410,25 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", window=0, page_size=0):
+def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", window=0, page_size=0, q_len=1):
     """Time one workload; the options select a half-precision output, a sliding
-    window or a paged cache (one shuffled block table shared by the rotated pools)."""
+    window, a paged cache (one shuffled block table shared by the rotated pools)
+    or several new tokens per slot (the cached lengths drop by q_len - 1 so the
+    step's last position stays where the plain workload's is)."""
     import torch
     import decode_step_masked_gb300 as ftd
     w = WORKLOADS[name]
-    lens = gen_seq_lens(w)
-    by = step_bytes(w, lens, window, out_dtype)
+    lens = gen_seq_lens(w) - (q_len - 1)
+    by = step_bytes(w, lens, window, out_dtype, q_len)
     # rotation is sized on the bytes a step reads (the visible rows), so each pool leaves L2 between reads
     pools = make_pools(w, n_pools_for(w, by["kv"]), seed, device, page_size)
-    inp = make_step_inputs(w, lens, seed, device, out_dtype)
+    inp = make_step_inputs(w, lens, seed, device, out_dtype, q_len)
     num_pages = 0
     if page_size:
         table, num_pages = page_table(w, page_size, seed)
         inp["block_table"] = torch.from_numpy(table).to(device)
     step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, out_dtype=out_dtype,
-                          window=window, page_size=page_size, num_pages=num_pages)
+                          window=window, page_size=page_size, num_pages=num_pages, q_len=q_len)
     r = run_timed(step, w, pools, inp, steps, warmup, stream)
     step.close()
     us = r["total_ms"] * 1e3 / steps
@@ -513,7 +520,7 @@ def main():
             w2, _, by2, pools2, _, r2, us2 = measure_config(name, 1000, 50, 99, device, stream, **kw)
             key = name + ":" + ",".join(f"{k}={v}" for k, v in kw.items())
             opts[key] = dict(us=us2, gbs=by2["kv"] / us2 / 1e3, frac=by2["kv"] / us2 / 1e3 / peaks["hbm_gbs"],
-                             kv_mb=by2["kv"] / 1e6, kernel=kernel_name(w2))
+                             kv_mb=by2["kv"] / 1e6, kernel=kernel_name(w2, kw.get("q_len", 1)))
             del pools2
             torch.cuda.empty_cache()
         line["options"] = opts

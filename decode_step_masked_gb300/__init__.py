@@ -40,7 +40,7 @@ class FtdConfig(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("max_len", ctypes.c_int), ("qkv_dtype", ctypes.c_int),
                 ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("out_dtype", ctypes.c_int), ("window", ctypes.c_int), ("page_size", ctypes.c_int),
-                ("num_pages", ctypes.c_int)]
+                ("num_pages", ctypes.c_int), ("q_len", ctypes.c_int)]
 
 
 class FtdError(RuntimeError):
@@ -170,11 +170,11 @@ class DecodeStep:
 
     def __init__(self, max_batch, n_q_heads, n_kv_heads, head_dim, max_len, qkv_dtype="bf16",
                  cache_dtype="bf16", softmax_scale=0.0, stream: Optional[int] = None, out_dtype="f32",
-                 window=0, page_size=0, num_pages=0):
+                 window=0, page_size=0, num_pages=0, q_len=1):
         import torch
         self.cfg = FtdConfig(max_batch, n_q_heads, n_kv_heads, head_dim, max_len, DTYPES[qkv_dtype],
                              DTYPES[cache_dtype], float(softmax_scale), DTYPES[out_dtype], int(window),
-                             int(page_size), int(num_pages))
+                             int(page_size), int(num_pages), int(q_len))
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         st, ctx = ftd_init(self.cfg, s)
         check(st)

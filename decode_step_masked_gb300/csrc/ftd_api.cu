@@ -128,6 +128,7 @@ struct ftd_ctx {
     void* st_out = nullptr;
     size_t q_bytes = 0, kv_new_bytes = 0, bias_bytes = 0, out_bytes = 0;
     size_t rows = 0;         // cache rows (of head_dim elements) in the pool
+    int nq = 1;              // new tokens per slot per step
     bool paged = false;
     int pages_per_seq = 0;
     cudaStream_t last_stream = nullptr;
@@ -179,15 +180,19 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     if (c.out_dtype != FTD_F32 && c.out_dtype != FTD_F16 && c.out_dtype != FTD_BF16)
         return fail(FTD_ERR_UNSUPPORTED, "out_dtype %d (F32, F16 or BF16)", static_cast<int>(c.out_dtype));
     if (c.window < 0) return fail(FTD_ERR_INVALID_ARG, "window %d must be >= 0", c.window);
+    if (c.q_len < 0 || c.q_len > ftd::kMaxQLen)
+        return fail(FTD_ERR_INVALID_ARG, "q_len %d outside 0..%d", c.q_len, ftd::kMaxQLen);
     const bool paged = c.page_size != 0;
     if (paged && (c.page_size < 128 || (c.page_size & (c.page_size - 1)) != 0 || c.num_pages < 1))
         return fail(FTD_ERR_INVALID_ARG, "page_size %d must be a power of two >= 128 with num_pages %d >= 1",
                     c.page_size, c.num_pages);
 
     const int g = c.n_q_heads / c.n_kv_heads;
+    const int nq = c.q_len > 1 ? c.q_len : 1;
+    const int rows_q = nq * g;  // query rows per kv head: every new token's heads of the group
     int G = 8;
-    while (g % G) G >>= 1;
-    const int nhb = g / G;
+    while (rows_q % G) G >>= 1;
+    const int nhb = rows_q / G;
 
     ftd::KernelInfo ki{};
     switch (c.cache_dtype) {
@@ -219,18 +224,19 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     const size_t cache_bytes = rows * D * elem_bytes(c.cache_dtype);
     const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * rows * sizeof(float) : 0;
 
-    // Grouped-query fp16/bf16 caches with head_dim 128 and groups of 8 or 16
-    // query heads use the tensor-core kernel; FTD_FORCE_CUDA_CORE=1 in the
-    // environment at ftd_init selects the CUDA-core kernel instead.
+    // fp16/bf16 caches with head_dim 128 whose kv heads carry a multiple of 8
+    // query rows (group x new tokens) use the tensor-core kernel;
+    // FTD_FORCE_CUDA_CORE=1 in the environment at ftd_init selects the
+    // CUDA-core kernel instead.
     const char* force = getenv("FTD_FORCE_CUDA_CORE");
     const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
-                         g % 8 == 0 && !(force && force[0] == '1');
+                         rows_q % 8 == 0 && !(force && force[0] == '1');
     ftd::TcKernelInfo tki{};
     int tc_nhb = 1;
     if (want_tc && encode_tiled()) {
-        const int Gt = g % 16 == 0 ? 16 : 8;
-        tki = ftd::select_tc(c.cache_dtype == FTD_BF16, Gt);
-        tc_nhb = g / Gt;
+        const int Gt = rows_q % 16 == 0 ? 16 : 8;
+        tki = ftd::select_tc(c.cache_dtype == FTD_BF16, Gt, nq > 1);
+        tc_nhb = rows_q / Gt;
         e = cudaFuncSetAttribute(tki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tki.smem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (tensor-core kernel)");
     }
@@ -253,10 +259,11 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     ctx->tc_nhb = tc_nhb;
     const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf(static_cast<float>(D));
     ctx->qscale = scale * 1.4426950408889634f;
-    ctx->q_bytes = B * Hq * D * qeb;
-    ctx->kv_new_bytes = B * Hkv * D * qeb;
+    ctx->nq = nq;
+    ctx->q_bytes = B * nq * Hq * D * qeb;
+    ctx->kv_new_bytes = B * nq * Hkv * D * qeb;
     ctx->bias_bytes = (Hq + 2 * Hkv) * D * qeb;
-    ctx->out_bytes = B * Hq * D * static_cast<size_t>(elem_bytes(c.out_dtype));
+    ctx->out_bytes = B * nq * Hq * D * static_cast<size_t>(elem_bytes(c.out_dtype));
     ctx->rows = rows;
     ctx->paged = paged;
     ctx->pages_per_seq = paged ? (c.max_len + c.page_size - 1) / c.page_size : 0;
@@ -361,6 +368,7 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     p.qscale = ctx->qscale;
     p.out_dtype = static_cast<int>(c.out_dtype);
     p.window = c.window;
+    p.nq = ctx->nq;
     p.block_table = ctx->paged ? block_table : nullptr;
     p.pages_per_seq = ctx->pages_per_seq;
     p.page_shift = 0;
@@ -466,7 +474,7 @@ ftd_status ftd_get_error(ftd_ctx* ctx) {
     }
     if (h & ftd::kErrBadPage)
         return fail(FTD_ERR_BAD_PAGE, "a block-table entry was outside [0, num_pages); those slots are undefined");
-    return fail(FTD_ERR_SEQ_OVERFLOW, "some seq_lens[b] >= max_len; those slots were skipped");
+    return fail(FTD_ERR_SEQ_OVERFLOW, "some seq_lens[b] + q_len > max_len; those slots were skipped");
 }
 
 void ftd_destroy(ftd_ctx* ctx) {

@@ -17,6 +17,9 @@ constexpr uint32_t kErrSeqOverflow = 1u;
 constexpr uint32_t kErrTimeout = 2u;
 constexpr uint32_t kErrBadPage = 4u;
 
+// Most new tokens per slot in one step (speculative verification runs).
+constexpr int kMaxQLen = 64;
+
 // A wait on a copy gives up after this many SM clock cycles (about 2 s).
 constexpr long long kWaitLimitCycles = 4000000000LL;
 
@@ -46,6 +49,7 @@ struct DecodeParams {
     float qscale;         // softmax scale * log2(e): scores live in the log2 domain
     int out_dtype;        // kF32 / kF16 / kBF16
     int window;           // > 0: attend only the last `window` positions
+    int nq;               // new tokens per slot (q [B][nq][Hq][D]); query rows per kv head = nq * group
     // paged cache: page p of the pool holds rows [p][Hkv][page_size][D];
     // block_table[b * pages_per_seq + i] is the page of positions [i*page_size, (i+1)*page_size)
     const int32_t* block_table;  // nullptr: contiguous [B][Hkv][Lmax][D] cache
@@ -56,6 +60,14 @@ struct DecodeParams {
 __device__ __forceinline__ int window_start(int L, int window) {
     const int ctx = L + 1;
     return (window > 0 && ctx > window) ? ctx - window : 0;
+}
+
+// Query row qi of a kv head (qi = head block * G + j, token-major: qi = token * group + head in
+// group) -> its token, and its row in q / out ([B][nq][Hq] rows of D elements).
+__device__ __forceinline__ int q_token(const DecodeParams& p, int qi) { return qi / p.group; }
+__device__ __forceinline__ size_t q_row(const DecodeParams& p, int b, int kvh, int qi) {
+    const int tok = qi / p.group;
+    return (static_cast<size_t>(b) * p.nq + tok) * p.Hq + kvh * p.group + (qi - tok * p.group);
 }
 
 // Row index (in cache rows of D elements) of position `pos` of (slot b, kv head),

@@ -205,7 +205,9 @@ __device__ __forceinline__ float from_ct<__half>(__half x) { return __half2float
 enum : int { kBarFull = 0, kBarEmpty = 3, kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarQReady = 12,
              kNumBars = 13 };
 
-template <typename CT, int G>
+// MQ: several new tokens per slot (q_len > 1), so the columns of S carry
+// their own causal limits; without it every column shares one row range.
+template <typename CT, int G, bool MQ>
 __global__ void __launch_bounds__(256, 1)
     decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
@@ -249,9 +251,9 @@ __global__ void __launch_bounds__(256, 1)
         for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
             const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
-            const bool valid = L >= 0 && L < p.Lmax;
-            ovf |= (b < p.B) && (L >= p.Lmax);
-            int v = valid ? ((L + TM) / TM - window_start(L, p.window) / TM) * segs : 0;
+            const bool valid = L >= 0 && L <= p.Lmax - p.nq;
+            ovf |= (b < p.B) && (L > p.Lmax - p.nq);
+            int v = valid ? ((L + p.nq - 1) / TM + 1 - window_start(L, p.window) / TM) * segs : 0;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const int y = __shfl_up_sync(FULL, v, m);
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(256, 1)
 
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (P[b + 1] == P[b]) {
-            zero_out(p.out, static_cast<size_t>(b) * p.Hq * D, p.Hq * D, p.out_dtype);
+            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
         }
     }
 
@@ -349,7 +351,6 @@ __global__ void __launch_bounds__(256, 1)
             for (int k = 0; k < n_my; ++k) {
                 const int s = k % NS;
                 const bool new_piece = (k == 0) || (cu.tile == 0);
-                const bool last = cu.tile == cu.nt - 1;
                 if (k > 0 && new_piece && !issue_pv(k - 1)) { ok = false; break; }
                 const bool wf = tc::wait_or_abort(bar(kBarFull + s), (k / NS) & 1, p.err, abort_flag);
                 if (__any_sync(FULL, !wf)) { ok = false; break; }
@@ -366,12 +367,15 @@ __global__ void __launch_bounds__(256, 1)
                     if (nlo > 0) fence_proxy_async_smem();
                     __syncwarp();
                 }
-                if (last) {
-                    // ---- append the new token and zero staged V rows past the end ----
+                // a single new token sits in the last tile; several may start a tile earlier
+                bool has_new = cu.tile == cu.nt - 1;
+                if constexpr (MQ)
+                    has_new = Ls[cu.b] < (window_start(Ls[cu.b], p.window) / TM + cu.tile + 1) * TM;
+                if (has_new) {
+                    // ---- append the new tokens (rows L - t0 ..) and zero staged V rows past the end ----
                     const int L = Ls[cu.b];
                     const int t0 = (window_start(L, p.window) / TM + cu.tile) * TM;
-                    const int n_total = L + 1 - t0;  // 1 .. TM
-                    const int nr = n_total - 1;      // row of the new token
+                    const int n_total = min(TM, L + p.nq - t0);  // rows holding data
                     const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
                     unsigned char* st = stages + s * tc::STAGE;
                     const int nz = (TM - n_total) * 8;
@@ -381,34 +385,37 @@ __global__ void __launch_bounds__(256, 1)
                         *reinterpret_cast<uint4*>(st + 2 * KB + box * KB + r * 128 + (rem & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
-                    const bool isv = lane >= 16;  // lanes 0-15: K row, 16-31: V row, 8 elements each
-                    const int d0 = (lane & 15) * 8;
-                    const void* src = isv ? p.v_new : p.k_new;
-                    const size_t si = (static_cast<size_t>(cu.b) * p.Hkv + kvh) * D + d0;
-                    const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + d0;
-                    uint32_t w[4];
+                    for (int nr = max(0, L - t0); nr < n_total; ++nr) {
+                        const int tok = t0 + nr - L, pos = t0 + nr;
+                        const bool isv = lane >= 16;  // lanes 0-15: K row, 16-31: V row, 8 elements each
+                        const int d0 = (lane & 15) * 8;
+                        const void* src = isv ? p.v_new : p.k_new;
+                        const size_t si = ((static_cast<size_t>(cu.b) * p.nq + tok) * p.Hkv + kvh) * D + d0;
+                        const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + d0;
+                        uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float x0 = ld_qkv(src, p.qkv_dtype, si + 2 * e);
-                        float x1 = ld_qkv(src, p.qkv_dtype, si + 2 * e + 1);
-                        if (p.bias) {
-                            x0 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e);
-                            x1 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e + 1);
+                        for (int e = 0; e < 4; ++e) {
+                            float x0 = ld_qkv(src, p.qkv_dtype, si + 2 * e);
+                            float x1 = ld_qkv(src, p.qkv_dtype, si + 2 * e + 1);
+                            if (p.bias) {
+                                x0 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e);
+                                x1 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e + 1);
+                            }
+                            const CT y0 = tc::to_ct<CT>(x0), y1 = tc::to_ct<CT>(x1);
+                            uint16_t u0, u1;
+                            memcpy(&u0, &y0, 2);
+                            memcpy(&u1, &y1, 2);
+                            w[e] = static_cast<uint32_t>(u0) | (static_cast<uint32_t>(u1) << 16);
                         }
-                        const CT y0 = tc::to_ct<CT>(x0), y1 = tc::to_ct<CT>(x1);
-                        uint16_t u0, u1;
-                        memcpy(&u0, &y0, 2);
-                        memcpy(&u1, &y1, 2);
-                        w[e] = static_cast<uint32_t>(u0) | (static_cast<uint32_t>(u1) << 16);
-                    }
-                    const uint4 wv = make_uint4(w[0], w[1], w[2], w[3]);
-                    unsigned char* srow = st + (isv ? 2 * KB : 0) + (d0 >> 6) * KB + nr * 128 +
-                                          ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
-                    *reinterpret_cast<uint4*>(srow) = wv;
-                    if (hb == 0) {
-                        const long long rowg = cache_row(p, cu.b, kvh, L, page_of(p, cu.b, L));
-                        if (rowg >= 0)
-                            *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + (rowg * D + d0) * 2) = wv;
+                        const uint4 wv = make_uint4(w[0], w[1], w[2], w[3]);
+                        unsigned char* srow = st + (isv ? 2 * KB : 0) + (d0 >> 6) * KB + nr * 128 +
+                                              ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
+                        *reinterpret_cast<uint4*>(srow) = wv;
+                        if (hb == 0) {
+                            const long long rowg = cache_row(p, cu.b, kvh, pos, page_of(p, cu.b, pos));
+                            if (rowg >= 0)
+                                *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + (rowg * D + d0) * 2) = wv;
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -442,6 +449,12 @@ __global__ void __launch_bounds__(256, 1)
             const int q4 = warp - 4;
             Cursor cu = locate(t_begin, P, p.B, segs);
             float m[G], l[G], o[G], al[G];
+            int tk[G];  // token of each query column (0 unless several new tokens per step)
+            // output row of query row qi of a kv head
+            auto orow = [&](int b, int kvh, int qi) -> size_t {
+                if constexpr (MQ) return q_row(p, b, kvh, qi);
+                return static_cast<size_t>(b) * p.Hq + kvh * p.group + qi;
+            };
             bool pending = false;
             int piece_first = cu.tile;
             auto acc_o = [&](int kk) -> bool {
@@ -461,15 +474,24 @@ __global__ void __launch_bounds__(256, 1)
                 const int L = Ls[cu.b];
                 const int pos0 = window_start(L, p.window);
                 const int t0 = (pos0 / TM + cu.tile) * TM;
-                const int n_total = min(TM, L + 1 - t0);
-                const int r_lo = max(0, pos0 - t0);  // rows before the window start are masked
                 const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
                 if (new_piece) {
                     piece_first = cu.tile;
 #pragma unroll
                     for (int j = 0; j < G; ++j) {
-                        const int h = kvh * p.group + hb * G + j;
-                        float x = ld_qkv(p.q, p.qkv_dtype, (static_cast<size_t>(cu.b) * p.Hq + h) * D + r);
+                        // q row of column j; several tokens per step interleave tokens and heads
+                        size_t qrow;
+                        int h;
+                        if constexpr (MQ) {
+                            tk[j] = q_token(p, hb * G + j);
+                            h = kvh * p.group + (hb * G + j - tk[j] * p.group);
+                            qrow = (static_cast<size_t>(cu.b) * p.nq + tk[j]) * p.Hq + h;
+                        } else {
+                            tk[j] = 0;
+                            h = kvh * p.group + hb * G + j;
+                            qrow = static_cast<size_t>(cu.b) * p.Hq + h;
+                        }
+                        float x = ld_qkv(p.q, p.qkv_dtype, qrow * D + r);
                         if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + r);
                         x *= p.qscale;
                         const CT hi = tc::to_ct<CT>(x);
@@ -491,10 +513,14 @@ __global__ void __launch_bounds__(256, 1)
                 __syncwarp();
                 float sv[N];
                 tc::tmem_ld<N>(tmem + lane_base + (k & 1) * N, sv);
-                const bool valid = r >= r_lo && r < n_total;
+                // column j sees rows [lo0 + tk[j], hi0 + tk[j]): positions up to L + tk[j], from
+                // its own window start on
+                const int hi0 = L + 1 - t0, lo0 = p.window > 0 ? L + 1 - p.window - t0 : -(1 << 30);
+                const bool valid0 = r >= lo0 && r < hi0;  // the rows every column sees (single token)
                 float sc[G];
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
+                    const bool valid = MQ ? (r >= lo0 + tk[j] && r < hi0 + tk[j]) : valid0;
                     sc[j] = valid ? sv[j] + sv[G + j] : -INFINITY;
                     float v = sc[j];
 #pragma unroll
@@ -508,8 +534,16 @@ __global__ void __launch_bounds__(256, 1)
                 for (int j = 0; j < G; ++j) {
                     const float tmax = fmaxf(fmaxf(red_max[j], red_max[G + j]), fmaxf(red_max[2 * G + j], red_max[3 * G + j]));
                     const float mnew = fmaxf(m[j], tmax);
-                    alpha[j] = exp2f(m[j] - mnew);
-                    const float pj = valid ? exp2f(sc[j] - mnew) : 0.f;
+                    float pj;
+                    if constexpr (MQ) {
+                        // a column with no visible row yet keeps m = -inf; 0 stands in as the reference
+                        const float mref = mnew == -INFINITY ? 0.f : mnew;
+                        alpha[j] = exp2f(m[j] - mref);
+                        pj = exp2f(sc[j] - mref);
+                    } else {
+                        alpha[j] = exp2f(m[j] - mnew);
+                        pj = valid0 ? exp2f(sc[j] - mnew) : 0.f;
+                    }
                     l[j] = l[j] * alpha[j] + pj;
                     m[j] = mnew;
                     const CT hi = tc::to_ct<CT>(pj);
@@ -544,10 +578,8 @@ __global__ void __launch_bounds__(256, 1)
                     const int segg = cu.b * segs + cu.seg;
                     if (piece_first == 0 && last) {
 #pragma unroll
-                        for (int j = 0; j < G; ++j) {
-                            const int h = kvh * p.group + hb * G + j;
-                            st_out1(p.out, (static_cast<size_t>(cu.b) * p.Hq + h) * D + r, o[j] / lt[j], p.out_dtype);
-                        }
+                        for (int j = 0; j < G; ++j)
+                            st_out1(p.out, orow(cu.b, kvh, hb * G + j) * D + r, o[j] / lt[j], p.out_dtype);
                     } else {
                         float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
                         if (r == 0) {
@@ -594,18 +626,17 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                                 for (int j = 0; j < G; ++j) {
                                     const float mn = fmaxf(Mx[j], mw[j]);
-                                    const float a = exp2f(Mx[j] - mn), bb = exp2f(mw[j] - mn);
+                                    const float mref = (MQ && mn == -INFINITY) ? 0.f : mn;
+                                    const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[j] - mref);
                                     Ls_[j] = Ls_[j] * a + lw[j] * bb;
                                     Ac[j] = Ac[j] * a + ow[j] * bb;
                                     Mx[j] = mn;
                                 }
                             }
 #pragma unroll
-                            for (int j = 0; j < G; ++j) {
-                                const int h = kvh * p.group + hb * G + j;
-                                st_out1(p.out, (static_cast<size_t>(cu.b) * p.Hq + h) * D + r, Ac[j] / Ls_[j],
+                            for (int j = 0; j < G; ++j)
+                                st_out1(p.out, orow(cu.b, kvh, hb * G + j) * D + r, Ac[j] / Ls_[j],
                                         p.out_dtype);
-                            }
                             if (r == 0) p.counters[segg] = 0u;
                         }
                         tc::named_bar_sync(1, 128);
@@ -634,12 +665,12 @@ struct TcKernelInfo {
     int G;
 };
 
-template <typename CT, int G>
+template <typename CT, int G, bool MQ>
 TcKernelInfo tc_kernel_info() {
     using LY = tc::Layout<G>;
-    return TcKernelInfo{reinterpret_cast<const void*>(&decode_gqa_tc_kernel<CT, G>), LY::SMEM, LY::SLOT, G};
+    return TcKernelInfo{reinterpret_cast<const void*>(&decode_gqa_tc_kernel<CT, G, MQ>), LY::SMEM, LY::SLOT, G};
 }
 
-TcKernelInfo select_tc(bool bf16, int G);
+TcKernelInfo select_tc(bool bf16, int G, bool multi_token);
 
 }  // namespace ftd

@@ -262,10 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
             const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
-            const bool valid = L >= 0 && L < p.Lmax;
-            ovf |= (b < p.B) && (L >= p.Lmax);
-            // tiles per segment: from the tile holding the window start to ceil((L + 1) / T)
-            int v = valid ? ((L + T) / T - window_start(L, p.window) / T) * segs : 0;
+            const bool valid = L >= 0 && L <= p.Lmax - p.nq;
+            ovf |= (b < p.B) && (L > p.Lmax - p.nq);
+            // tiles per segment: from the tile holding the window start to the tile of position L + nq - 1
+            int v = valid ? ((L + p.nq - 1) / T + 1 - window_start(L, p.window) / T) * segs : 0;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const int y = __shfl_up_sync(FULL, v, m);
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     // Slots without work (inactive or overflowing) get a zero output.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (P[b + 1] == P[b]) {
-            zero_out(p.out, static_cast<size_t>(b) * p.Hq * D, p.Hq * D, p.out_dtype);
+            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
         }
     }
 
@@ -304,8 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     auto issue = [&](int s, const Cursor& cu) {
         const int L = Ls[cu.b];
         const int t0 = (window_start(L, p.window) / T + cu.tile) * T;
-        const int n_total = min(T, L + 1 - t0);
-        const int n_cache = (cu.tile == cu.nt - 1) ? n_total - 1 : n_total;
+        const int n_cache = min(T, max(0, L - t0));  // rows before the new tokens come from the cache
         const int kvh = cu.seg / p.nhb;
         const long long rb = cache_row(p, cu.b, kvh, t0, pages.page(p, cu.b, t0));
         if (rb < 0) atomicOr(p.err, kErrBadPage);
@@ -337,15 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     }
 
     float qr[G][EPL], o[G][EPL], m[G], l[G];
+    int tk[G];  // token of each query row (0 unless several new tokens per step)
     auto begin_segment = [&](const Cursor& cu) {
         const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            const int h = kvh * p.group + hb * G + j;
+            const size_t qrow = q_row(p, cu.b, kvh, hb * G + j);
+            tk[j] = q_token(p, hb * G + j);
+            const int h = kvh * p.group + (hb * G + j - tk[j] * p.group);
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
                 const int d = c * EPL + e;
-                float x = ld_qkv(p.q, p.qkv_dtype, (static_cast<size_t>(cu.b) * p.Hq + h) * D + d);
+                float x = ld_qkv(p.q, p.qkv_dtype, qrow * D + d);
                 if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + d);
                 qr[j][e] = x * p.qscale;
                 o[j][e] = 0.f;
@@ -364,19 +366,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         if (!mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((k / SPW) & 1), p.err)) break;
 
         const int L = Ls[cc.b];
-        const int pos0 = window_start(L, p.window);
+        const int pos0 = window_start(L, p.window);  // window start of the first new token
         const int t0 = (pos0 / T + cc.tile) * T;
-        const int n_total = min(T, L + 1 - t0);
-        const int r_lo = max(0, pos0 - t0);  // rows before the window start are masked
+        const int n_total = min(T, L + p.nq - t0);   // rows holding data (history or new tokens)
+        const int r_lo = max(0, pos0 - t0);          // rows before the window start are masked
         const bool last_tile = cc.tile == cc.nt - 1;
         const int kvh = cc.seg / p.nhb, hb = cc.seg % p.nhb;
 
-        // ---- append: the new token is the last visible row of the last tile ----
-        if (last_tile) {
-            const int nr = n_total - 1;  // its row inside the tile (position L)
+        // ---- append: rows at positions L .. L + nq - 1 are the new tokens ----
+        for (int nr = max(0, L - t0); nr < n_total; ++nr) {
+            const int tok = t0 + nr - L;  // token of this row
+            const int pos = t0 + nr;
             const bool isv = hr != 0;   // half-warp 0 writes K, half-warp 1 writes V
             const void* src = isv ? p.v_new : p.k_new;
-            const size_t si = (static_cast<size_t>(cc.b) * p.Hkv + kvh) * D + c * EPL;
+            const size_t si = ((static_cast<size_t>(cc.b) * p.nq + tok) * p.Hkv + kvh) * D + c * EPL;
             const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + c * EPL;
             float x[EPL];
 #pragma unroll
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                 x[e] = ld_qkv(src, p.qkv_dtype, si + e);
                 if (p.bias) x[e] += ld_qkv(p.bias, p.qkv_dtype, bi + e);  // one binary32 add
             }
-            const long long rowL = cache_row(p, cc.b, kvh, L, page_of(p, cc.b, L));  // cache row of position L
+            const long long rowL = cache_row(p, cc.b, kvh, pos, page_of(p, cc.b, pos));  // cache row of pos
             const bool gok = rowL >= 0 && hb == 0;  // the first head block writes the cache
             unsigned char* srow = st + (isv ? TILE : 0) + nr * ROW + c * EPL * EB;
             unsigned char* grow = (isv ? p.v_cache : p.k_cache) + (gok ? rowL : 0) * ROW + c * EPL * EB;
@@ -451,10 +454,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         // ---- online softmax over the tile (log2 domain) ----
         float alpha[G];
         const int r = lane % T;
+        // query row j sees rows [lo_j, hi_j) of the tile: positions up to L + tk[j], and from
+        // its own window start on
+        const int hi0 = L + 1 - t0, lo0 = p.window > 0 ? L + 1 - p.window - t0 : -(1 << 30);
+        const bool full = hi0 + tk[0] >= T && lo0 + tk[G - 1] <= 0;  // every query row sees every row
 #pragma unroll
         for (int j = 0; j < G; ++j) {
             float sv = -INFINITY;
-            if (r >= r_lo && r < n_total) {
+            if (full || (r >= lo0 + tk[j] && r < hi0 + tk[j])) {
                 sv = sc[j * T + r];
                 if constexpr (I8) sv *= reinterpret_cast<const float*>(st + 2 * TILE)[r];
             }
@@ -462,8 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
 #pragma unroll
             for (int mm = T / 2; mm >= 1; mm >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(FULL, tmax, mm));
             const float mnew = fmaxf(m[j], tmax);
-            alpha[j] = exp2f(m[j] - mnew);
-            const float pv = exp2f(sv - mnew);
+            // a query row with no visible row yet keeps m = -inf; 0 stands in as the reference
+            const float mref = (!full && mnew == -INFINITY) ? 0.f : mnew;
+            alpha[j] = exp2f(m[j] - mref);
+            const float pv = exp2f(sv - mref);
             float tsum = pv;
 #pragma unroll
             for (int mm = T / 2; mm >= 1; mm >>= 1) tsum += __shfl_xor_sync(FULL, tsum, mm);
@@ -522,9 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                 if (hr == 0) {
 #pragma unroll
                     for (int j = 0; j < G; ++j) {
-                        const int h = kvh * p.group + hb * G + j;
                         const float inv = 1.f / l[j];
-                        const size_t dst = (static_cast<size_t>(cc.b) * p.Hq + h) * D + c * EPL;
+                        const size_t dst = q_row(p, cc.b, kvh, hb * G + j) * D + c * EPL;
 #pragma unroll
                         for (int e4 = 0; e4 < EPL / 4; ++e4)
                             st_out4(p.out, dst + 4 * e4, o[j][4 * e4] * inv, o[j][4 * e4 + 1] * inv,
@@ -595,8 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                         }
 #pragma unroll
                         for (int j = 0; j < G; ++j) {
+                            // a piece whose tiles a query row could not see yet left m = -inf
                             const float mn = fmaxf(Mx[j], mw[j]);
-                            const float a = exp2f(Mx[j] - mn), bb = exp2f(mw[j] - mn);
+                            const float mref = mn == -INFINITY ? 0.f : mn;
+                            const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[j] - mref);
                             Ls_[j] = Ls_[j] * a + lw[j] * bb;
 #pragma unroll
                             for (int e = 0; e < DL; ++e) Ac[j][e] = Ac[j][e] * a + ow[j][e] * bb;
@@ -605,8 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                     }
 #pragma unroll
                     for (int j = 0; j < G; ++j) {
-                        const int h = kvh * p.group + hb * G + j;
-                        const size_t dst = (static_cast<size_t>(cc.b) * p.Hq + h) * D + lane * DL;
+                        const size_t dst = q_row(p, cc.b, kvh, hb * G + j) * D + lane * DL;
                         const float inv = 1.f / Ls_[j];
                         if constexpr (DL == 4) {
                             st_out4(p.out, dst, Ac[j][0] * inv, Ac[j][1] * inv, Ac[j][2] * inv, Ac[j][3] * inv,

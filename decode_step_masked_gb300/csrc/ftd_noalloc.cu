@@ -79,6 +79,7 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
         return reject(FTD_ERR_UNSUPPORTED, "out_dtype must be F32, F16 or BF16");
     if (c.window < 0) return reject(FTD_ERR_INVALID_ARG, "window must be >= 0");
     if (c.page_size != 0) return reject(FTD_ERR_INVALID_ARG, "paged caches need a context (ftd_init)");
+    if (c.q_len < 0 || c.q_len > ftd::kMaxQLen) return reject(FTD_ERR_INVALID_ARG, "q_len outside 0..64");
     const bool i8 = c.cache_dtype == FTD_I8;
     if (i8 && !scales) return reject(FTD_ERR_INVALID_ARG, "an INT8 cache needs its scales");
     auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
@@ -86,9 +87,10 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
         return reject(FTD_ERR_INVALID_ARG, "caches, scales and out must be 16-byte aligned");
 
     const int g = c.n_q_heads / c.n_kv_heads;
+    const int nq = c.q_len > 1 ? c.q_len : 1;
     int G = 8;
-    while (g % G) G >>= 1;
-    const int nhb = g / G;
+    while ((nq * g) % G) G >>= 1;
+    const int nhb = nq * g / G;
     ftd::KernelInfo ki{};
     switch (c.cache_dtype) {
         case FTD_F32: ki = ftd::select_f32(c.head_dim, G); break;
@@ -168,6 +170,7 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
     p.qscale = scale * 1.4426950408889634f;
     p.out_dtype = static_cast<int>(c.out_dtype);
     p.window = c.window;
+    p.nq = nq;
 
     void* args[] = {&p};
     cudaError_t e = cudaLaunchKernel(ki.fn, dim3(ds->sms), dim3(ftd::kThreads), args,

@@ -42,6 +42,12 @@
  *    fixed-size blocks mapped like a virtual-memory page table): the cache is
  *    a pool of pages and a per-slot block table maps positions to pages;
  *    served by ftd_decode_mha_paged.
+ *  - q_len T > 1: T new tokens per slot in one step, as a speculative
+ *    verification pass checks a run of draft tokens (pptc.cn section 4.3).
+ *    Token j of slot b is appended at position L_b + j and its query attends
+ *    to positions 0 .. L_b + j (with a window, the last W of them).  The
+ *    caller then advances seq_lens[b] by the number of tokens it accepts;
+ *    rows written past that are overwritten by the next step.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -49,21 +55,21 @@
  *    Lmax = max_len.  L_b = seq_lens[b] is the number of tokens already in
  *    the cache for slot b; the new token is written at position L_b and
  *    attends to positions 0 .. L_b inclusive.
- *  - Layouts are dense and row-major:
- *        q      [B][Hq][D]        qkv dtype
- *        k_new  [B][Hkv][D]       qkv dtype      v_new likewise
+ *  - Layouts are dense and row-major (T = q_len, 1 unless set):
+ *        q      [B][T][Hq][D]     qkv dtype
+ *        k_new  [B][T][Hkv][D]    qkv dtype      v_new likewise
  *        bias   [(Hq + 2*Hkv)*D]  qkv dtype, the q part, then k, then v
  *        cache  [B][Hkv][Lmax][D] cache dtype    (k_cache, v_cache)
  *        scales [2][B][Hkv][Lmax] fp32, plane 0 for K and plane 1 for V
  *                                 (INT8 caches only)
- *        out    [B][Hq][D]        out_dtype (fp32 unless the config says)
+ *        out    [B][T][Hq][D]     out_dtype (fp32 unless the config says)
  *    A paged context replaces the cache and scale layouts by
  *        pages  [num_pages][Hkv][page_size][D]  cache dtype (k_pages, v_pages)
  *        scales [2][num_pages][Hkv][page_size]  fp32 (INT8 caches only)
  *        block_table [B][ceil(Lmax / page_size)] int32: entry i of slot b is
  *               the page holding positions i*page_size .. (i+1)*page_size - 1.
  *  - Slots with seq_lens[b] < 0 are inactive: their cache is untouched and
- *    their output is zero.  seq_lens[b] >= Lmax is an overflow: the slot is
+ *    their output is zero.  seq_lens[b] + T > Lmax is an overflow: the slot is
  *    skipped the same way and a sticky device error is raised, which
  *    ftd_get_error() reports as FTD_ERR_SEQ_OVERFLOW.  Nothing traps.
  *  - Device pointers must be 16-byte aligned.  All device work goes to the
@@ -89,7 +95,7 @@ typedef enum {
     FTD_ERR_UNSUPPORTED = 2,     /* dtype / head_dim combination not built */
     FTD_ERR_OOM = 3,             /* ftd_init could not allocate its pool */
     FTD_ERR_CUDA = 4,            /* a CUDA runtime call failed */
-    FTD_ERR_SEQ_OVERFLOW = 5,    /* some seq_lens[b] >= max_len in a past call */
+    FTD_ERR_SEQ_OVERFLOW = 5,    /* some seq_lens[b] + q_len > max_len in a past call */
     FTD_ERR_DEVICE_TIMEOUT = 6,  /* a kernel gave up waiting for a copy (bounded wait) */
     FTD_ERR_BAD_PAGE = 7         /* a block-table entry read in a past call was outside [0, num_pages) */
 } ftd_status;
@@ -111,6 +117,7 @@ typedef struct {
     int window;            /* 0: whole context; W > 0: the last W positions */
     int page_size;         /* 0: contiguous cache; else a power of two >= 128 */
     int num_pages;         /* pages in the pool when page_size > 0 */
+    int q_len;             /* new tokens per slot per step, 0 or 1 .. 64 (0 = 1) */
 } ftd_config;
 
 typedef struct ftd_ctx ftd_ctx;
@@ -144,7 +151,7 @@ ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** 
  *   seq_lens        : device int32 [B]; read only.
  *   scales          : device fp32 [2][B][Hkv][Lmax] for INT8 caches (NULL
  *                     selects the pool's planes); ignored otherwise.
- *   out             : device [B][Hq][D] of out_dtype; every element is written.
+ *   out             : device [B][T][Hq][D] of out_dtype; every element is written.
  *   stream          : cudaStream_t as void*.
  * Launches one kernel; no host synchronisation and no allocation.  Two calls
  * on the same context must not overlap in time (they share the workspace):
@@ -232,7 +239,7 @@ uint64_t ftd_kernel_launches(void);
  *                      k_cache and v_cache are required (there is no pool), and
  *                      so are scales for an INT8 cache.
  *   device_err       : device uint32, or NULL.  When given, the kernel ORs its
- *                      error bits into it (1 = some seq_lens[b] >= max_len,
+ *                      error bits into it (1 = some seq_lens[b] + q_len > max_len,
  *                      2 = a bounded wait gave up); the caller reads and clears
  *                      it.  When NULL those bits are dropped (overflowing slots
  *                      still get a zero output).

@@ -49,16 +49,19 @@ TORCH_OUT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
 def run_step(w, inp, step=None, softmax_scale=0.0, use_bias=True, force_cuda_core=False, out_dtype="f32",
              window=0):
     """One decode step on the GPU with caller-owned device buffers.  The output
-    comes back as float64 (exact for every out_dtype)."""
+    comes back as float64 (exact for every out_dtype), [B,Hq,D] or, with
+    w.q_len > 1, [B,T,Hq,D]."""
     import torch
     own = step is None
+    T = getattr(w, "q_len", 1)
     if own:
-        step = make_step(w, softmax_scale, force_cuda_core, out_dtype=out_dtype, window=window)
+        step = make_step(w, softmax_scale, force_cuda_core, out_dtype=out_dtype, window=window, q_len=T)
     q, kn, vn = dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"])
     bias = dev(inp["bias"]) if (use_bias and inp.get("bias") is not None) else None
     kc, vc, sl = dev(inp["k_cache"]), dev(inp["v_cache"]), dev(inp["seq_lens"])
     sc = dev(inp["scales"]) if inp.get("scales") is not None else None
-    out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=getattr(torch, TORCH_OUT[out_dtype]), device="cuda")
+    shape = (w.B, T, w.Hq, w.D) if T > 1 else (w.B, w.Hq, w.D)
+    out = torch.full(shape, float("nan"), dtype=getattr(torch, TORCH_OUT[out_dtype]), device="cuda")
     step(q, kn, vn, sl, out, bias=bias, k_cache=kc, v_cache=vc, scales=sc)
     torch.cuda.synchronize()
     status = step.get_error()
@@ -124,3 +127,53 @@ def fill_device_scales(w, seed, lens, fill_beyond="nan"):
         t[0, b].copy_(dev(gen_scales_slot(w, seed, "k", b, int(lens[b]), fill_beyond)))
         t[1, b].copy_(dev(gen_scales_slot(w, seed, "v", b, int(lens[b]), fill_beyond)))
     return t
+
+
+# ------------------------------------------------------------ paged caches
+def page_layout(w, lens, page_size, spare, seed, q_len=1):
+    """A shuffled page pool: every slot gets the pages covering positions 0 .. L_b;
+    unused table entries hold an out-of-range sentinel the kernel must not read."""
+    rng = np.random.default_rng(seed)
+    pps = -(-w.Lmax // page_size)
+    need = [(-(-(int(L) + q_len) // page_size) if 0 <= L <= w.Lmax - q_len else 0) for L in lens]
+    num_pages = sum(need) + spare
+    perm = rng.permutation(num_pages)
+    table = np.full((w.B, pps), 1 << 30, np.int32)
+    k = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[k:k + n]
+        k += n
+    return table, num_pages, perm[k:]
+
+
+def to_pages(w, arr, table, num_pages, page_size, fill):
+    """Scatter a contiguous [B][Hkv][Lmax](...) array into pages [num_pages][Hkv][page_size](...)."""
+    tail = arr.shape[3:]
+    pages = np.full((num_pages, w.Hkv, page_size) + tail, fill, dtype=arr.dtype)
+    for b in range(w.B):
+        for i, pg in enumerate(table[b]):
+            if 0 <= pg < num_pages:
+                lo = i * page_size
+                n = min(page_size, w.Lmax - lo)
+                pages[pg, :, :n] = arr[b, :, lo:lo + n]
+    return pages
+
+
+def from_pages(w, pages, table, page_size, lens, q_len=1):
+    """Gather positions 0 .. L_b + q_len - 1 of each active slot back to a contiguous array (rest zero)."""
+    out = np.zeros((w.B, w.Hkv, w.Lmax) + pages.shape[3:], dtype=pages.dtype)
+    for b, L in enumerate(lens):
+        if not 0 <= L <= w.Lmax - q_len:
+            continue
+        for t0 in range(0, int(L) + q_len, page_size):
+            n = min(page_size, int(L) + q_len - t0)
+            out[b, :, t0:t0 + n] = pages[table[b, t0 // page_size], :, :n]
+    return out
+
+
+def valid_rows(w, arr, lens, q_len=1):
+    out = np.zeros_like(arr)
+    for b, L in enumerate(lens):
+        if 0 <= L <= w.Lmax - q_len:
+            out[b, :, :L + q_len] = arr[b, :, :L + q_len]
+    return out

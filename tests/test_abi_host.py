@@ -43,7 +43,7 @@ def test_status_strings(lib):
 def cfg(**kw):
     base = dict(max_batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, max_len=256,
                 qkv_dtype=ftd.FTD_BF16, cache_dtype=ftd.FTD_BF16, softmax_scale=0.0,
-                out_dtype=ftd.FTD_F32, window=0, page_size=0, num_pages=0)
+                out_dtype=ftd.FTD_F32, window=0, page_size=0, num_pages=0, q_len=0)
     base.update(kw)
     return ftd.FtdConfig(*[base[f] for f, _ in ftd.FtdConfig._fields_])
 
@@ -70,6 +70,8 @@ def cfg(**kw):
     (dict(page_size=-128, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
     (dict(page_size=128, num_pages=0), ftd.FTD_ERR_INVALID_ARG),
     (dict(page_size=384, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
+    (dict(q_len=-1), ftd.FTD_ERR_INVALID_ARG),
+    (dict(q_len=65), ftd.FTD_ERR_INVALID_ARG),
 ])
 def test_init_rejects_bad_config(lib, kw, status):
     st, ctx = ftd.ftd_init(cfg(**kw))
@@ -109,7 +111,7 @@ def test_config_struct_matches_header():
 
 
 def test_noalloc_rejects_paged_and_bad_options(lib):
-    for kw in (dict(page_size=128, num_pages=4), dict(window=-3), dict(out_dtype=ftd.FTD_I8)):
+    for kw in (dict(page_size=128, num_pages=4), dict(window=-3), dict(out_dtype=ftd.FTD_I8), dict(q_len=99)):
         st = ftd.ftd_decode_mha_noalloc(cfg(**kw), 16, 16, 16, 0, 16, 16, 16, 0, 16, 0, 0)
         assert st in (ftd.FTD_ERR_INVALID_ARG, ftd.FTD_ERR_UNSUPPORTED), kw
         assert ftd.ftd_last_error() != ""

@@ -50,6 +50,17 @@ def test_step_bytes_half_output():
             == 2 * w.B * w.Hq * w.D)
 
 
+def test_step_bytes_several_new_tokens():
+    w = WORKLOADS["7b"].with_(B=2)
+    lens = np.array([100, 4093], np.int32)  # 4093 + 4 > Lmax 4096: overflow, no work
+    by = bench.step_bytes(w, lens, q_len=4)
+    assert by["ctx"] == 104
+    assert by["kv"] == 2 * w.Hkv * w.D * 2 * 104  # 100 history rows read + 4 rows appended
+    by_w = bench.step_bytes(w, lens, window=10, q_len=4)
+    assert by_w["ctx"] == 13  # rows some token sees: positions 91 .. 103
+    assert bench.kernel_name(w, 8) == "decode_gqa_tc_kernel" and bench.kernel_name(w, 4) == "decode_splitk_kernel"
+
+
 def test_page_table_is_a_permutation():
     w = WORKLOADS["13b"]
     table, n = bench.page_table(w, 256, 3)

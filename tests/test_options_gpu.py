@@ -21,8 +21,8 @@ import pytest
 import decode_step_masked_gb300 as ftd
 import oracle
 from synthetic import Workload, gen_all, to_storage
-from tests.gpu_util import (TOL_MAXABS, TOL_MAXABS_I8, assert_close, assert_same_bytes, dev, make_step,
-                            run_step)
+from tests.gpu_util import (TOL_MAXABS, TOL_MAXABS_I8, assert_close, assert_same_bytes, dev, from_pages,
+                            make_step, page_layout, run_step, to_pages, valid_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -167,55 +167,6 @@ def test_window_with_half_output_and_consecutive_steps():
 
 
 # --------------------------------------------------------------- paged
-def _page_layout(w, lens, page_size, spare, seed):
-    """A shuffled page pool: every slot gets the pages covering positions 0 .. L_b;
-    unused table entries hold an out-of-range sentinel the kernel must not read."""
-    rng = np.random.default_rng(seed)
-    pps = -(-w.Lmax // page_size)
-    need = [(-(-(int(L) + 1) // page_size) if 0 <= L < w.Lmax else 0) for L in lens]
-    num_pages = sum(need) + spare
-    perm = rng.permutation(num_pages)
-    table = np.full((w.B, pps), 1 << 30, np.int32)
-    k = 0
-    for b, n in enumerate(need):
-        table[b, :n] = perm[k:k + n]
-        k += n
-    return table, num_pages, perm[k:]
-
-
-def _to_pages(w, arr, table, num_pages, page_size, fill):
-    """Scatter a contiguous [B][Hkv][Lmax](...) array into pages [num_pages][Hkv][page_size](...)."""
-    tail = arr.shape[3:]
-    pages = np.full((num_pages, w.Hkv, page_size) + tail, fill, dtype=arr.dtype)
-    for b in range(w.B):
-        for i, pg in enumerate(table[b]):
-            if 0 <= pg < num_pages:
-                lo = i * page_size
-                n = min(page_size, w.Lmax - lo)
-                pages[pg, :, :n] = arr[b, :, lo:lo + n]
-    return pages
-
-
-def _from_pages(w, pages, table, page_size, lens):
-    """Gather positions 0 .. L_b of each active slot back to a contiguous array (rest zero)."""
-    out = np.zeros((w.B, w.Hkv, w.Lmax) + pages.shape[3:], dtype=pages.dtype)
-    for b, L in enumerate(lens):
-        if not 0 <= L < w.Lmax:
-            continue
-        for t0 in range(0, int(L) + 1, page_size):
-            n = min(page_size, int(L) + 1 - t0)
-            out[b, :, t0:t0 + n] = pages[table[b, t0 // page_size], :, :n]
-    return out
-
-
-def _valid_rows(w, arr, lens):
-    out = np.zeros_like(arr)
-    for b, L in enumerate(lens):
-        if 0 <= L < w.Lmax:
-            out[b, :, :L + 1] = arr[b, :, :L + 1]
-    return out
-
-
 PAGED = {
     "mha_bf16_p128": ("bf16", "bf16", 5, 8, 8, 128, 768, [0, 127, 128, 500, 767], 128, False),
     "mha_f16_p256": ("f16", "f16", 4, 8, 8, 128, 1024, [255, 256, 700, 1023], 256, False),
@@ -231,11 +182,11 @@ def _run_paged(w, inp, table, num_pages, page_size, cc, window=0, out_dtype="f32
     import torch
     nanv = {"f32": np.float32(np.nan), "f16": np.float16(np.nan), "bf16": np.uint16(0x7FC0),
             "i8": np.int8(127)}[w.cache_dtype]
-    kp = _to_pages(w, inp["k_cache"], table, num_pages, page_size, nanv)
-    vp = _to_pages(w, inp["v_cache"], table, num_pages, page_size, nanv)
+    kp = to_pages(w, inp["k_cache"], table, num_pages, page_size, nanv)
+    vp = to_pages(w, inp["v_cache"], table, num_pages, page_size, nanv)
     sp = None
     if inp.get("scales") is not None:
-        sp = np.stack([_to_pages(w, inp["scales"][i][..., None], table, num_pages, page_size, np.nan)[..., 0]
+        sp = np.stack([to_pages(w, inp["scales"][i][..., None], table, num_pages, page_size, np.nan)[..., 0]
                        for i in range(2)])
     step = make_step(w, force_cuda_core=cc, out_dtype=out_dtype, window=window, page_size=page_size,
                      num_pages=num_pages)
@@ -259,20 +210,20 @@ def _run_paged(w, inp, table, num_pages, page_size, cc, window=0, out_dtype="f32
 def test_paged_cache(shape):
     cache, qkv, B, Hq, Hkv, D, Lmax, lens, ps, cc = PAGED[shape]
     w, inp = case(cache, qkv, B, Hq, Hkv, D, Lmax, lens)
-    table, num_pages, spare = _page_layout(w, inp["seq_lens"], ps, spare=3, seed=5)
+    table, num_pages, spare = page_layout(w, inp["seq_lens"], ps, spare=3, seed=5)
     ref = oracle.load().decode_step(w, inp, nthreads=8)
     got = _run_paged(w, inp, table, num_pages, ps, cc)
     assert_close(got["out"], ref["out"], i8=cache == "i8", what=shape)
     L = inp["seq_lens"]
     # the appended rows landed in their pages, and every other held row is unchanged
     for name, key in (("K", "k"), ("V", "v")):
-        assert_same_bytes(_from_pages(w, got[f"{key}_pages"], table, ps, L),
-                          _valid_rows(w, ref[f"{key}_cache"], L), f"{shape} {name} pages after append")
+        assert_same_bytes(from_pages(w, got[f"{key}_pages"], table, ps, L),
+                          valid_rows(w, ref[f"{key}_cache"], L), f"{shape} {name} pages after append")
         assert_same_bytes(got[f"{key}_pages"][spare], got[f"{key}_in"][spare], f"{shape} spare {name} pages")
     if cache == "i8":
         for i in range(2):
-            g = _from_pages(w, got["scales"][i][..., None], table, ps, L)[..., 0]
-            assert_same_bytes(g, _valid_rows(w, ref["scales"][i], L), f"{shape} scale plane {i}")
+            g = from_pages(w, got["scales"][i][..., None], table, ps, L)[..., 0]
+            assert_same_bytes(g, valid_rows(w, ref["scales"][i], L), f"{shape} scale plane {i}")
 
 
 @pytest.mark.parametrize("window", [100, 256, 300])
@@ -281,7 +232,7 @@ def test_paged_with_window_reads_only_window_pages(shape, window):
     """Entries of pages wholly before the window start are never read: they hold the sentinel."""
     cache, qkv, B, Hq, Hkv, D, Lmax, lens, ps, cc = PAGED[shape]
     w, inp = case(cache, qkv, B, Hq, Hkv, D, Lmax, lens)
-    table, num_pages, _ = _page_layout(w, inp["seq_lens"], ps, spare=1, seed=6)
+    table, num_pages, _ = page_layout(w, inp["seq_lens"], ps, spare=1, seed=6)
     for b, L in enumerate(inp["seq_lens"]):
         if 0 <= L < w.Lmax:
             start = max(0, int(L) + 1 - window)
@@ -297,7 +248,7 @@ def test_paged_with_window_reads_only_window_pages(shape, window):
 def test_bad_page_is_reported(shape):
     cache, qkv, B, Hq, Hkv, D, Lmax, lens, ps, cc = PAGED[shape]
     w, inp = case(cache, qkv, B, Hq, Hkv, D, Lmax, lens)
-    table, num_pages, _ = _page_layout(w, inp["seq_lens"], ps, spare=0, seed=7)
+    table, num_pages, _ = page_layout(w, inp["seq_lens"], ps, spare=0, seed=7)
     table[2, 1] = num_pages  # slot 2 holds more than one page; one past the pool
     got = _run_paged(w, inp, table, num_pages, ps, cc, expect=ftd.FTD_ERR_BAD_PAGE)
     ref = oracle.load().decode_step(w, inp, nthreads=8)
