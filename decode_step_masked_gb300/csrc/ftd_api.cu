@@ -322,6 +322,25 @@ ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** 
     return FTD_OK;
 }
 
+// Launch with programmatic stream serialisation: when the previous operation on
+// the stream is a kernel, this grid's blocks may be placed while it drains and
+// wait in griddepcontrol.wait (the kernels' grid_dep_wait) for its completion,
+// which hides the launch gap between back-to-back decode steps.
+static cudaError_t launch_overlapped(const void* fn, int grid, int threads, int smem, void** args,
+                                     cudaStream_t stream) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                 const void* bias, void* k_cache, void* v_cache, const int32_t* block_table,
                                 const int32_t* seq_lens, float* scales, void* out, cudaStream_t stream) {
@@ -391,12 +410,10 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
         }
         p.nhb = ctx->tc_nhb;
         void* args[] = {&ctx->tmk, &ctx->tmv, &p};
-        e = cudaLaunchKernel(ctx->tki.fn, dim3(ctx->grid), dim3(256), args, static_cast<size_t>(ctx->tki.smem),
-                             stream);
+        e = launch_overlapped(ctx->tki.fn, ctx->grid, 256, ctx->tki.smem, args, stream);
     } else {
         void* args[] = {&p};
-        e = cudaLaunchKernel(ctx->ki.fn, dim3(ctx->grid), dim3(ftd::kThreads), args,
-                             static_cast<size_t>(ctx->ki.smem), stream);
+        e = launch_overlapped(ctx->ki.fn, ctx->grid, ftd::kThreads, ctx->ki.smem, args, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     g_launches.fetch_add(1);

@@ -139,6 +139,27 @@ __device__ __forceinline__ void zero_out(void* out, size_t i, int n, int dt) {
 }
 
 // ---------------------------------------------------------------- PTX
+// Programmatic dependent launch.  grid_dep_wait blocks until the grid this
+// launch was allowed to overlap has finished and its writes are visible (it
+// returns at once after an ordinary launch); every global read of the step's
+// inputs comes after it.  grid_dep_launch lets the next launch on the stream
+// start placing its blocks on SMs this grid frees; those blocks then wait in
+// their own grid_dep_wait.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Split-K arrival on a segment counter: an acquire-release add at GPU scope.
+// The release publishes the partial that the calling warp or block stored
+// before it (those stores are ordered before the caller by a warp or block
+// barrier); the acquire orders the merge reads that follow, which the caller
+// extends to its warp or block with another barrier.  Unlike a full fence it
+// does not wait for every outstanding memory operation of the thread.
+__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t* ctr, uint32_t n) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ctr), "r"(n) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -245,6 +245,8 @@ __global__ void __launch_bounds__(256, 1)
                      "r"(LY::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    grid_dep_wait();    // inputs, caches and lengths may come from the previous launch
+    grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
     if (warp == 0) {
         int carry = 0;
         bool ovf = false;
@@ -591,16 +593,16 @@ __global__ void __launch_bounds__(256, 1)
                         }
 #pragma unroll
                         for (int j = 0; j < G; ++j) slot[LY::OOFF + j * D + r] = o[j];
-                        __threadfence();
+                        // the barrier orders the 128 threads' partial stores before thread 0's release
                         tc::named_bar_sync(1, 128);
                         const uint32_t piece_tiles = static_cast<uint32_t>(cu.tile - piece_first + 1);
                         if (r == 0) {
-                            const uint32_t prev = atomicAdd(&p.counters[segg], piece_tiles);
+                            const uint32_t prev = arrive_acq_rel(&p.counters[segg], piece_tiles);
                             bcast[0] = (prev + piece_tiles == static_cast<uint32_t>(cu.nt)) ? 1 : 0;
                         }
+                        // and thread 0's acquire before every thread's merge reads
                         tc::named_bar_sync(1, 128);
                         if (bcast[0]) {
-                            __threadfence();
                             const long long S0 = P[cu.b] + static_cast<long long>(cu.seg) * cu.nt;
                             const int wf = worker_of(S0, U, W);
                             const int wl = worker_of(S0 + cu.nt - 1, U, W);

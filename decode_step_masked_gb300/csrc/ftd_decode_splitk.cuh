@@ -255,6 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
 #pragma unroll
         for (int s = 0; s < SPW; ++s) mbar_init(smem_addr(&bars[s]), 1);
     }
+    grid_dep_wait();    // inputs, caches and lengths may come from the previous launch
+    grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
     // Tiles per slot and their prefix; overflowing slots raise the sticky flag.
     if (warp == 0) {
         int carry = 0;
@@ -327,12 +329,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         }
     };
 
+    // When the copy cursor enters a segment, pull that segment's q rows and new
+    // K/V rows into L1: the compute cursor reaches them SPW tiles later and then
+    // finds them on chip instead of stalling on a global round trip mid-stream.
+    // (The issue-bound INT8 instantiation does better without the extra work.)
+    const int qeb = p.qkv_dtype == kF32 ? 4 : 2;
+    auto prefetch_segment = [&](const Cursor& cu) {
+        const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
+        const int lines = D * qeb / 128;  // 128-byte lines per row
+        const int nlines = (G + 2 * p.nq) * lines;
+        for (int i = lane; i < nlines; i += 32) {
+            const int row = i / lines, part = i - row * lines;
+            const unsigned char* base;
+            if (row < G) {
+                base = static_cast<const unsigned char*>(p.q) + q_row(p, cu.b, kvh, hb * G + row) * D * qeb;
+            } else {
+                const int tok = (row - G) % p.nq;
+                const void* src = row < G + p.nq ? p.k_new : p.v_new;
+                base = static_cast<const unsigned char*>(src) +
+                       ((static_cast<size_t>(cu.b) * p.nq + tok) * p.Hkv + kvh) * D * qeb;
+            }
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(base + part * 128));
+        }
+    };
+
     Cursor ci = locate(t_begin, P, p.B, segs);
     Cursor cc = ci;
     const int npre = min(SPW, n_my);
     for (int k = 0; k < npre; ++k) {
         if (lane == 0) issue(k, ci);
-        if (k + 1 < n_my) advance(ci, P, segs);
+        if (k + 1 < n_my) {
+            advance(ci, P, segs);
+            if (!I8 && ci.tile == 0) prefetch_segment(ci);
+        }
     }
 
     float qr[G][EPL], o[G][EPL], m[G], l[G];
@@ -359,11 +388,90 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     begin_segment(cc);
     int piece_first = cc.tile;
 
+    // Log-sum-exp merge of all partials of segment mc, by the worker whose
+    // arrival completed its tile count; then the counter is reset for the next launch.
+    auto merge_segment = [&](const Cursor& mc) {
+        const int segg = mc.b * segs + mc.seg;
+        const int kvh = mc.seg / p.nhb, hb = mc.seg % p.nhb;
+        const long long S0 = P[mc.b] + static_cast<long long>(mc.seg) * mc.nt;
+        const int wf = worker_of(S0, U, W);
+        const int wl = worker_of(S0 + mc.nt - 1, U, W);
+        auto has_piece = [&](int w) { return (w * U) / W < ((w + 1) * U) / W; };
+        // one pass over the pieces with a running log-sum-exp per head;
+        // the loads of a piece are independent (one L2 round trip each)
+        constexpr int DL = D / 32;
+        float Mx[G], Ls_[G], Ac[G][DL];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            Mx[j] = -INFINITY;
+            Ls_[j] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DL; ++e) Ac[j][e] = 0.f;
+        }
+        for (int w = wf; w <= wl; ++w) {
+            if (!has_piece(w)) continue;
+            const float* sl = p.ws + static_cast<size_t>(segg + w) * TL::SLOT;
+            float mw[G], lw[G], ow[G][DL];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                mw[j] = __ldcg(sl + j);
+                lw[j] = __ldcg(sl + G + j);
+                const float* ov = sl + TL::OOFF + j * D + lane * DL;
+                if constexpr (DL == 4) {
+                    const float4 u = __ldcg(reinterpret_cast<const float4*>(ov));
+                    ow[j][0] = u.x; ow[j][1] = u.y; ow[j][2] = u.z; ow[j][3] = u.w;
+                } else {
+                    const float2 u = __ldcg(reinterpret_cast<const float2*>(ov));
+                    ow[j][0] = u.x; ow[j][1] = u.y;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                // a piece whose tiles a query row could not see yet left m = -inf
+                const float mn = fmaxf(Mx[j], mw[j]);
+                const float mref = mn == -INFINITY ? 0.f : mn;
+                const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[j] - mref);
+                Ls_[j] = Ls_[j] * a + lw[j] * bb;
+#pragma unroll
+                for (int e = 0; e < DL; ++e) Ac[j][e] = Ac[j][e] * a + ow[j][e] * bb;
+                Mx[j] = mn;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            const size_t dst = q_row(p, mc.b, kvh, hb * G + j) * D + lane * DL;
+            const float inv = 1.f / Ls_[j];
+            if constexpr (DL == 4) {
+                st_out4(p.out, dst, Ac[j][0] * inv, Ac[j][1] * inv, Ac[j][2] * inv, Ac[j][3] * inv,
+                        p.out_dtype);
+            } else {
+#pragma unroll
+                for (int e = 0; e < DL; ++e) st_out1(p.out, dst + e, Ac[j][e] * inv, p.out_dtype);
+            }
+        }
+        if (lane == 0) p.counters[segg] = 0u;
+    };
+    // Read lane 0's arrival result; the arrival that completes the count merges.
+    auto resolve = [&](uint32_t r0, const Cursor& mc, uint32_t tiles) {
+        const uint32_t prev = __shfl_sync(FULL, r0, 0);
+        if (prev + tiles == static_cast<uint32_t>(mc.nt)) {
+            __syncwarp();  // lane 0's acquire orders every lane's merge reads
+            merge_segment(mc);
+        }
+    };
+    bool pend = false;  // a mid-stream arrival whose answer is still to be read
+    uint32_t pend_ret = 0, pend_tiles = 0;
+    Cursor pend_cu{};
+
     int k = 0;
     for (; k < n_my; ++k) {
         const int s = k % SPW;
         unsigned char* st = wbase + s * STAGE;
         if (!mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((k / SPW) & 1), p.err)) break;
+        if (pend) {  // the arrival of the piece that ended one tile ago has returned by now
+            resolve(pend_ret, pend_cu, pend_tiles);
+            pend = false;
+        }
 
         const int L = Ls[cc.b];
         const int pos0 = window_start(L, p.window);  // window start of the first new token
@@ -517,7 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         // ---- refill this stage with the tile SPW ahead ----
         if (k + SPW < n_my) {
             if (lane == 0) issue(s, ci);
-            if (k + SPW + 1 < n_my) advance(ci, P, segs);
+            if (k + SPW + 1 < n_my) {
+                advance(ci, P, segs);
+                if (!I8 && ci.tile == 0) prefetch_segment(ci);
+            }
         }
 
         // ---- end of a piece: final output, or partial + merge by the last arrival ----
@@ -558,74 +669,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
                                 make_float4(o[j][4 * e4], o[j][4 * e4 + 1], o[j][4 * e4 + 2], o[j][4 * e4 + 3]);
                     }
                 }
-                __threadfence();
-                __syncwarp();
+                __syncwarp();  // every lane's partial stores come before lane 0's release
                 // The counter accumulates tiles, not pieces: when U < W some
                 // workers own no tile, so the number of pieces is not wf..wl.
                 const uint32_t piece_tiles = static_cast<uint32_t>(cc.tile - piece_first + 1);
-                uint32_t prev = 0;
-                if (lane == 0) prev = atomicAdd(&p.counters[segg], piece_tiles);
-                prev = __shfl_sync(FULL, prev, 0);
-                if (prev + piece_tiles == static_cast<uint32_t>(cc.nt)) {
-                    // last piece of this segment: log-sum-exp merge of all partials
-                    __threadfence();
-                    const long long S0 = P[cc.b] + static_cast<long long>(cc.seg) * cc.nt;
-                    const int wf = worker_of(S0, U, W);
-                    const int wl = worker_of(S0 + cc.nt - 1, U, W);
-                    auto has_piece = [&](int w) { return (w * U) / W < ((w + 1) * U) / W; };
-                    // one pass over the pieces with a running log-sum-exp per head;
-                    // the loads of a piece are independent (one L2 round trip each)
-                    constexpr int DL = D / 32;
-                    float Mx[G], Ls_[G], Ac[G][DL];
-#pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        Mx[j] = -INFINITY;
-                        Ls_[j] = 0.f;
-#pragma unroll
-                        for (int e = 0; e < DL; ++e) Ac[j][e] = 0.f;
-                    }
-                    for (int w = wf; w <= wl; ++w) {
-                        if (!has_piece(w)) continue;
-                        const float* sl = p.ws + static_cast<size_t>(segg + w) * TL::SLOT;
-                        float mw[G], lw[G], ow[G][DL];
-#pragma unroll
-                        for (int j = 0; j < G; ++j) {
-                            mw[j] = __ldcg(sl + j);
-                            lw[j] = __ldcg(sl + G + j);
-                            const float* ov = sl + TL::OOFF + j * D + lane * DL;
-                            if constexpr (DL == 4) {
-                                const float4 u = __ldcg(reinterpret_cast<const float4*>(ov));
-                                ow[j][0] = u.x; ow[j][1] = u.y; ow[j][2] = u.z; ow[j][3] = u.w;
-                            } else {
-                                const float2 u = __ldcg(reinterpret_cast<const float2*>(ov));
-                                ow[j][0] = u.x; ow[j][1] = u.y;
-                            }
-                        }
-#pragma unroll
-                        for (int j = 0; j < G; ++j) {
-                            // a piece whose tiles a query row could not see yet left m = -inf
-                            const float mn = fmaxf(Mx[j], mw[j]);
-                            const float mref = mn == -INFINITY ? 0.f : mn;
-                            const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[j] - mref);
-                            Ls_[j] = Ls_[j] * a + lw[j] * bb;
-#pragma unroll
-                            for (int e = 0; e < DL; ++e) Ac[j][e] = Ac[j][e] * a + ow[j][e] * bb;
-                            Mx[j] = mn;
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        const size_t dst = q_row(p, cc.b, kvh, hb * G + j) * D + lane * DL;
-                        const float inv = 1.f / Ls_[j];
-                        if constexpr (DL == 4) {
-                            st_out4(p.out, dst, Ac[j][0] * inv, Ac[j][1] * inv, Ac[j][2] * inv, Ac[j][3] * inv,
-                                    p.out_dtype);
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < DL; ++e) st_out1(p.out, dst + e, Ac[j][e] * inv, p.out_dtype);
-                        }
-                    }
-                    if (lane == 0) p.counters[segg] = 0u;
+                uint32_t ret = 0;
+                if (lane == 0) ret = arrive_acq_rel(&p.counters[segg], piece_tiles);
+                if (k == n_my - 1) {
+                    resolve(ret, cc, piece_tiles);
+                } else {
+                    // the worker streams on; the atomic's answer is read after the next tile
+                    pend = true;
+                    pend_ret = ret;
+                    pend_cu = cc;
+                    pend_tiles = piece_tiles;
                 }
             }
             if (k + 1 < n_my) {
