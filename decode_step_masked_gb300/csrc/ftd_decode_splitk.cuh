@@ -397,8 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         const int wf = worker_of(S0, U, W);
         const int wl = worker_of(S0 + mc.nt - 1, U, W);
         auto has_piece = [&](int w) { return (w * U) / W < ((w + 1) * U) / W; };
-        // one pass over the pieces with a running log-sum-exp per head;
-        // the loads of a piece are independent (one L2 round trip each)
+        // one pass over the pieces with a running log-sum-exp per query row
         constexpr int DL = D / 32;
         float Mx[G], Ls_[G], Ac[G][DL];
 #pragma unroll
@@ -408,33 +407,77 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
 #pragma unroll
             for (int e = 0; e < DL; ++e) Ac[j][e] = 0.f;
         }
-        for (int w = wf; w <= wl; ++w) {
-            if (!has_piece(w)) continue;
-            const float* sl = p.ws + static_cast<size_t>(segg + w) * TL::SLOT;
-            float mw[G], lw[G], ow[G][DL];
+        // pieces in batches of NB: the loads of a batch are issued together, so a merge
+        // costs one L2 round trip per batch rather than one per piece
+        constexpr int NB = G >= 8 ? 1 : 8 / G;
+        if constexpr (NB == 1) {  // eight query rows: one piece at a time keeps registers in budget
+            for (int w = wf; w <= wl; ++w) {
+                if (!has_piece(w)) continue;
+                const float* sl = p.ws + static_cast<size_t>(segg + w) * TL::SLOT;
+                float mw[G], lw[G], ow[G][DL];
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                mw[j] = __ldcg(sl + j);
-                lw[j] = __ldcg(sl + G + j);
-                const float* ov = sl + TL::OOFF + j * D + lane * DL;
-                if constexpr (DL == 4) {
-                    const float4 u = __ldcg(reinterpret_cast<const float4*>(ov));
-                    ow[j][0] = u.x; ow[j][1] = u.y; ow[j][2] = u.z; ow[j][3] = u.w;
-                } else {
-                    const float2 u = __ldcg(reinterpret_cast<const float2*>(ov));
-                    ow[j][0] = u.x; ow[j][1] = u.y;
+                for (int j = 0; j < G; ++j) {
+                    mw[j] = __ldcg(sl + j);
+                    lw[j] = __ldcg(sl + G + j);
+                    const float* ov = sl + TL::OOFF + j * D + lane * DL;
+                    if constexpr (DL == 4) {
+                        const float4 u = __ldcg(reinterpret_cast<const float4*>(ov));
+                        ow[j][0] = u.x; ow[j][1] = u.y; ow[j][2] = u.z; ow[j][3] = u.w;
+                    } else {
+                        const float2 u = __ldcg(reinterpret_cast<const float2*>(ov));
+                        ow[j][0] = u.x; ow[j][1] = u.y;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    const float mn = fmaxf(Mx[j], mw[j]);
+                    const float mref = mn == -INFINITY ? 0.f : mn;
+                    const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[j] - mref);
+                    Ls_[j] = Ls_[j] * a + lw[j] * bb;
+#pragma unroll
+                    for (int e = 0; e < DL; ++e) Ac[j][e] = Ac[j][e] * a + ow[j][e] * bb;
+                    Mx[j] = mn;
                 }
             }
+        } else {
+            for (int w0 = wf; w0 <= wl; w0 += NB) {
+                float mw[NB][G], lw[NB][G], ow[NB][G][DL];
 #pragma unroll
-            for (int j = 0; j < G; ++j) {
-                // a piece whose tiles a query row could not see yet left m = -inf
-                const float mn = fmaxf(Mx[j], mw[j]);
-                const float mref = mn == -INFINITY ? 0.f : mn;
-                const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[j] - mref);
-                Ls_[j] = Ls_[j] * a + lw[j] * bb;
+                for (int i = 0; i < NB; ++i) {
+                    const int w = w0 + i;
+                    const bool ok = w <= wl && has_piece(w);
+                    const float* sl = p.ws + static_cast<size_t>(segg + (ok ? w : wf)) * TL::SLOT;
 #pragma unroll
-                for (int e = 0; e < DL; ++e) Ac[j][e] = Ac[j][e] * a + ow[j][e] * bb;
-                Mx[j] = mn;
+                    for (int j = 0; j < G; ++j) {
+                        mw[i][j] = ok ? __ldcg(sl + j) : -INFINITY;
+                        lw[i][j] = ok ? __ldcg(sl + G + j) : 0.f;
+                        const float* ov = sl + TL::OOFF + j * D + lane * DL;
+                        if constexpr (DL == 4) {
+                            float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (ok) u = __ldcg(reinterpret_cast<const float4*>(ov));
+                            ow[i][j][0] = u.x; ow[i][j][1] = u.y; ow[i][j][2] = u.z; ow[i][j][3] = u.w;
+                        } else {
+                            float2 u = make_float2(0.f, 0.f);
+                            if (ok) u = __ldcg(reinterpret_cast<const float2*>(ov));
+                            ow[i][j][0] = u.x; ow[i][j][1] = u.y;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < NB; ++i) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        // a piece whose tiles a query row could not see yet (or an empty batch
+                        // entry) has m = -inf and contributes nothing
+                        const float mn = fmaxf(Mx[j], mw[i][j]);
+                        const float mref = mn == -INFINITY ? 0.f : mn;
+                        const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[i][j] - mref);
+                        Ls_[j] = Ls_[j] * a + lw[i][j] * bb;
+#pragma unroll
+                        for (int e = 0; e < DL; ++e) Ac[j][e] = Ac[j][e] * a + ow[i][j][e] * bb;
+                        Mx[j] = mn;
+                    }
+                }
             }
         }
 #pragma unroll
