@@ -133,11 +133,12 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
     }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                            uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(pol)
         : "memory");
 }
 
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) {
                 Cursor cu = locate(t_begin, P, p.B, segs);
                 PageCursor pages;
+                const uint64_t l2pol = l2_stream_policy();
                 int k = 0;
                 for (; k < n_my; ++k) {
                     const int s = k % NS;
@@ -309,10 +311,10 @@ __global__ void __launch_bounds__(256, 1)
                     if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag)) break;
                     const uint32_t st = smem_addr(stages + s * tc::STAGE);
                     mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
-                    tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s));
-                    tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s));
-                    tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s));
-                    tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s));
+                    tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s), l2pol);
+                    tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
+                    tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
+                    tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
                     if (k + 1 < n_my) advance(cu, P, segs);
                 }
                 if (k < n_my) {

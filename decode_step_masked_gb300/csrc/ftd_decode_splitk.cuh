@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     // Paged caches: the page of the tile comes from the block table; the entry
     // of the current page is kept and the next page's entry is loaded early.
     PageCursor pages;
+    const uint64_t l2pol = l2_stream_policy();
     auto issue = [&](int s, const Cursor& cu) {
         const int L = Ls[cu.b];
         const int t0 = (window_start(L, p.window) / T + cu.tile) * T;
@@ -318,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, 2 * kb + 2 * sb);
         if (kb) {
-            bulk_g2s(smem_addr(st), p.k_cache + rowbase * ROW, kb, bar);
-            bulk_g2s(smem_addr(st + TILE), p.v_cache + rowbase * ROW, kb, bar);
+            bulk_g2s_hint(smem_addr(st), p.k_cache + rowbase * ROW, kb, bar, l2pol);
+            bulk_g2s_hint(smem_addr(st + TILE), p.v_cache + rowbase * ROW, kb, bar, l2pol);
         }
         if constexpr (I8) {
             if (sb) {
-                bulk_g2s(smem_addr(st + 2 * TILE), p.k_scales + rowbase, sb, bar);
-                bulk_g2s(smem_addr(st + 2 * TILE + SCL), p.v_scales + rowbase, sb, bar);
+                bulk_g2s_hint(smem_addr(st + 2 * TILE), p.k_scales + rowbase, sb, bar, l2pol);
+                bulk_g2s_hint(smem_addr(st + 2 * TILE + SCL), p.v_scales + rowbase, sb, bar, l2pol);
             }
         }
     };
@@ -355,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
 
     Cursor ci = locate(t_begin, P, p.B, segs);
     Cursor cc = ci;
+    if (!I8) prefetch_segment(ci);  // the first segment's new K/V rows are needed at its last tile
     const int npre = min(SPW, n_my);
     for (int k = 0; k < npre; ++k) {
         if (lane == 0) issue(k, ci);
