@@ -242,7 +242,7 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     }
     const bool use_tc = tki.fn != nullptr;
     const size_t n_seg = use_tc ? B * Hkv * tc_nhb : B * Hkv * nhb;
-    const size_t n_slots = n_seg + static_cast<size_t>(grid) * (use_tc ? 1 : ftd::kWarps);
+    const size_t n_slots = n_seg + static_cast<size_t>(grid) * (use_tc ? 1 : ki.warps);
     const size_t ws_bytes = n_slots * (use_tc ? tki.slot_floats : ki.slot_floats) * sizeof(float);
     const int qeb = elem_bytes(c.qkv_dtype);
 
@@ -413,7 +413,7 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
         e = launch_overlapped(ctx->tki.fn, ctx->grid, 256, ctx->tki.smem, args, stream);
     } else {
         void* args[] = {&p};
-        e = launch_overlapped(ctx->ki.fn, ctx->grid, ftd::kThreads, ctx->ki.smem, args, stream);
+        e = launch_overlapped(ctx->ki.fn, ctx->grid, ctx->ki.warps * 32, ctx->ki.smem, args, stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     g_launches.fetch_add(1);

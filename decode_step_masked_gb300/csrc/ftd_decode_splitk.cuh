@@ -66,12 +66,17 @@ struct Tiling {
     static constexpr int TILE = T * ROW;
     static constexpr int SCL = I8 ? T * 4 : 0;                 // per-row scales of one tile
     static constexpr int STAGE = 2 * TILE + 2 * SCL;
-    static constexpr int SPW = cmax(2, cmin(4, 26624 / STAGE));  // ring stages per warp
+    // Workers per CTA.  The INT8 tile loop issues more instructions per byte than
+    // 8 warps can hide, so INT8 with small query blocks runs 12 workers of 2
+    // stages each: the same bytes in flight per SM, 1.5x the warps to issue from
+    // (and at most 170 registers a thread, which those instantiations fit).
+    static constexpr int WARPS = (I8 && G <= 2) ? 12 : kWarps;
+    static constexpr int SPW = WARPS > 8 ? 2 : cmax(2, cmin(4, 26624 / STAGE));  // ring stages per warp
     static constexpr int RB = cmax(1, cmin(R, 16 / G));        // rows per reduce-scatter batch
     static constexpr int SCRATCH = 2 * G * T * 4;              // scores + probabilities
     static constexpr int WARP_BYTES = round_up(SPW * STAGE + SCRATCH + SPW * 8, 128);
     static constexpr int PREFIX_BYTES = round_up((2 * kMaxBatch + 1) * 4, 128);
-    static constexpr int SMEM = PREFIX_BYTES + kWarps * WARP_BYTES;
+    static constexpr int SMEM = PREFIX_BYTES + WARPS * WARP_BYTES;
     static constexpr int OOFF = round_up(2 * G, 4);            // o offset in a partial slot
     static constexpr int SLOT = OOFF + G * D;                  // floats per partial slot
     static_assert(D % 16 == 0 && (EPL == 4 || EPL == 8), "head_dim 64 or 128");
@@ -232,7 +237,7 @@ __device__ __forceinline__ int worker_of(long long t, long long U, long long W) 
 
 // ================================================================ kernel
 template <typename CT, int D, int G>
-__global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk_kernel(const DecodeParams p) {
     using TL = Tiling<CT, D, G>;
     constexpr int T = TL::T, R = TL::R, EPL = TL::EPL, ROW = TL::ROW, SPW = TL::SPW, RB = TL::RB;
     constexpr int TILE = TL::TILE, SCL = TL::SCL, STAGE = TL::STAGE, EB = TL::EB;
@@ -293,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_splitk_kernel(const Decode
     }
 
     const long long U = P[p.B];
-    const long long W = static_cast<long long>(gridDim.x) * kWarps;
-    const int wid = blockIdx.x * kWarps + warp;
+    const long long W = static_cast<long long>(gridDim.x) * TL::WARPS;
+    const int wid = blockIdx.x * TL::WARPS + warp;
     const int t_begin = static_cast<int>(wid * U / W);
     const int n_my = static_cast<int>((wid + 1) * U / W) - t_begin;
     if (n_my <= 0) return;
@@ -757,12 +762,14 @@ struct KernelInfo {
     int T;
     int slot_floats;
     int G;
+    int warps;  // workers (warps) per CTA; the launch uses warps * 32 threads
 };
 
 template <typename CT, int D, int G>
 KernelInfo kernel_info() {
     using TL = Tiling<CT, D, G>;
-    return KernelInfo{reinterpret_cast<const void*>(&decode_splitk_kernel<CT, D, G>), TL::SMEM, TL::T, TL::SLOT, G};
+    return KernelInfo{reinterpret_cast<const void*>(&decode_splitk_kernel<CT, D, G>), TL::SMEM, TL::T, TL::SLOT, G,
+                      TL::WARPS};
 }
 
 template <typename CT>

@@ -127,7 +127,7 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
 
     // Scratch layout: [error word | counters | split-K partial slots], 256-byte aligned parts.
     const size_t n_seg = static_cast<size_t>(c.max_batch) * c.n_kv_heads * nhb;
-    const size_t n_slots = n_seg + static_cast<size_t>(ds->sms) * ftd::kWarps;
+    const size_t n_slots = n_seg + static_cast<size_t>(ds->sms) * ki.warps;
     const size_t cnt_off = 256;
     const size_t ws_off = cnt_off + (n_seg * sizeof(uint32_t) + 255) / 256 * 256;
     const size_t need = ws_off + n_slots * static_cast<size_t>(ki.slot_floats) * sizeof(float);
@@ -173,7 +173,7 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
     p.nq = nq;
 
     void* args[] = {&p};
-    cudaError_t e = cudaLaunchKernel(ki.fn, dim3(ds->sms), dim3(ftd::kThreads), args,
+    cudaError_t e = cudaLaunchKernel(ki.fn, dim3(ds->sms), dim3(ki.warps * 32), args,
                                      static_cast<size_t>(ki.smem), s);
     if (e != cudaSuccess) return reject(FTD_ERR_CUDA, cudaGetErrorString(e));
     ftd::note_launch();
