@@ -175,24 +175,24 @@ __device__ __forceinline__ void cvt_st(unsigned char* p, const float (&x)[N]) {
 // half of the live values to the partner lane and keeps the other half, so
 // after log2(N) rounds every lane holds one fully reduced value, whose index
 // is returned in idx; remaining rounds are plain butterflies.
-template <int N, int MASK>
+template <int N, int MASK, typename V = float>
 struct ReduceScatter {
-    static __device__ __forceinline__ void run(float* v, int c, int& idx) {
+    static __device__ __forceinline__ void run(V* v, int c, int& idx) {
         if constexpr (MASK == 0) {
             return;
         } else if constexpr (N > 1) {
             const bool up = (c & MASK) != 0;
 #pragma unroll
             for (int k = 0; k < N / 2; ++k) {
-                const float send = up ? v[k] : v[k + N / 2];
-                const float keep = up ? v[k + N / 2] : v[k];
+                const V send = up ? v[k] : v[k + N / 2];
+                const V keep = up ? v[k + N / 2] : v[k];
                 v[k] = keep + __shfl_xor_sync(0xffffffffu, send, MASK);
             }
             if (up) idx += N / 2;
-            ReduceScatter<N / 2, MASK / 2>::run(v, c, idx);
+            ReduceScatter<N / 2, MASK / 2, V>::run(v, c, idx);
         } else {
             v[0] += __shfl_xor_sync(0xffffffffu, v[0], MASK);
-            ReduceScatter<1, MASK / 2>::run(v, c, idx);
+            ReduceScatter<1, MASK / 2, V>::run(v, c, idx);
         }
     }
 };
@@ -373,6 +373,12 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
 
     float qr[G][EPL], o[G][EPL], m[G], l[G];
     int tk[G];  // token of each query row (0 unless several new tokens per step)
+    // INT8 caches: the scaled query as two int8 levels, q ~ s1 * hi + (s1 / 254) * lo, so
+    // q . k runs as dp4a integer dot products with the int8 codes (four products per
+    // instruction) and needs no per-byte conversion; relative error about 1.5e-5 of max |q|,
+    // the same budget as the tensor-core kernel's hi/lo split.  qsc = s1 / 254.
+    uint32_t qh[G][I8 ? EPL / 4 : 1], ql[G][I8 ? EPL / 4 : 1];
+    float qsc[G];
     auto begin_segment = [&](const Cursor& cu) {
         const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
 #pragma unroll
@@ -390,6 +396,30 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
             }
             m[j] = -INFINITY;
             l[j] = 0.f;
+            if constexpr (I8) {
+                float amax = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(qr[j][e]));
+#pragma unroll
+                for (int mm = 8; mm >= 1; mm >>= 1) amax = fmaxf(amax, __shfl_xor_sync(FULL, amax, mm));
+                const float s1 = amax > 0.f ? amax / 127.f : 1.f;
+                const float inv1 = 1.f / s1, inv2 = 254.f / s1;
+#pragma unroll
+                for (int w = 0; w < EPL / 4; ++w) {
+                    uint32_t hw = 0u, lw = 0u;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float x = qr[j][4 * w + k];
+                        const int hi = max(-127, min(127, __float2int_rn(x * inv1)));
+                        const int lo = max(-127, min(127, __float2int_rn((x - static_cast<float>(hi) * s1) * inv2)));
+                        hw |= (static_cast<uint32_t>(hi) & 0xffu) << (8 * k);
+                        lw |= (static_cast<uint32_t>(lo) & 0xffu) << (8 * k);
+                    }
+                    qh[j][w] = hw;
+                    ql[j][w] = lw;
+                }
+                qsc[j] = s1 / 254.f;
+            }
         }
     };
     begin_segment(cc);
@@ -588,24 +618,55 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
         const unsigned char* Vt = st + TILE;
 #pragma unroll
         for (int ib = 0; ib < R / RB; ++ib) {
-            float part[G * RB];
+            if constexpr (I8) {
+                // integer partial sums 254 * (hi . k) + (lo . k): |value| < 2^31 for D <= 128
+                int part[G * RB];
 #pragma unroll
-            for (int i = 0; i < RB; ++i) {
-                const int row = 2 * (ib * RB + i) + hr;
-                float kf[EPL];
-                ld_cvt<CT, EPL>(Kt + row * ROW + c * EPL * EB, kf);
+                for (int i = 0; i < RB; ++i) {
+                    const int row = 2 * (ib * RB + i) + hr;
+                    uint32_t kw[EPL / 4];
+                    if constexpr (EPL == 8) {
+                        const uint2 u = *reinterpret_cast<const uint2*>(Kt + row * ROW + c * EPL);
+                        kw[0] = u.x;
+                        kw[EPL / 4 - 1] = u.y;
+                    } else {
+                        kw[0] = *reinterpret_cast<const uint32_t*>(Kt + row * ROW + c * EPL);
+                    }
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    float a = 0.f;
+                    for (int j = 0; j < G; ++j) {
+                        int ah = 0, al = 0;
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) a = fmaf(qr[j][e], kf[e], a);
-                    part[j * RB + i] = a;
+                        for (int w = 0; w < EPL / 4; ++w) {
+                            ah = __dp4a(static_cast<int>(kw[w]), static_cast<int>(qh[j][w]), ah);
+                            al = __dp4a(static_cast<int>(kw[w]), static_cast<int>(ql[j][w]), al);
+                        }
+                        part[j * RB + i] = ah * 254 + al;
+                    }
                 }
+                int idx = 0;
+                ReduceScatter<G * RB, 8, int>::run(part, c, idx);
+                const int j = idx / RB, i = idx % RB;
+                sc[j * T + 2 * (ib * RB + i) + hr] = static_cast<float>(part[0]) * qsc[j];
+            } else {
+                float part[G * RB];
+#pragma unroll
+                for (int i = 0; i < RB; ++i) {
+                    const int row = 2 * (ib * RB + i) + hr;
+                    float kf[EPL];
+                    ld_cvt<CT, EPL>(Kt + row * ROW + c * EPL * EB, kf);
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        float a = 0.f;
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) a = fmaf(qr[j][e], kf[e], a);
+                        part[j * RB + i] = a;
+                    }
+                }
+                int idx = 0;
+                ReduceScatter<G * RB, 8>::run(part, c, idx);
+                const int j = idx / RB, i = idx % RB;
+                sc[j * T + 2 * (ib * RB + i) + hr] = part[0];
             }
-            int idx = 0;
-            ReduceScatter<G * RB, 8>::run(part, c, idx);
-            const int j = idx / RB, i = idx % RB;
-            sc[j * T + 2 * (ib * RB + i) + hr] = part[0];
         }
         __syncwarp();
 
