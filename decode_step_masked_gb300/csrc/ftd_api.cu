@@ -410,7 +410,7 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
         }
         p.nhb = ctx->tc_nhb;
         void* args[] = {&ctx->tmk, &ctx->tmv, &p};
-        e = launch_overlapped(ctx->tki.fn, ctx->grid, 256, ctx->tki.smem, args, stream);
+        e = launch_overlapped(ctx->tki.fn, ctx->grid, ctx->tki.threads, ctx->tki.smem, args, stream);
     } else {
         void* args[] = {&p};
         e = launch_overlapped(ctx->ki.fn, ctx->grid, ctx->ki.warps * 32, ctx->ki.smem, args, stream);

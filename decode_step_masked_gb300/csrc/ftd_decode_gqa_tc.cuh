@@ -47,6 +47,12 @@ constexpr int NS = 3;     // K/V stages
 constexpr int KB = 16384; // one 64-column box of 128 rows (bytes)
 constexpr int STAGE = 4 * KB;  // K (2 boxes) + V (2 boxes)
 
+// The softmax is the per-tile critical path.  With 8 or more query columns two
+// groups of four warps split the columns (each thread handles half of them),
+// so a CTA runs 384 threads: warps 0-3 for copies and MMA, warps 4-11 softmax.
+constexpr int softmax_groups(int G) { return G >= 8 ? 2 : 1; }
+constexpr int threads_for(int G) { return 128 + 128 * softmax_groups(G); }
+
 template <int G>
 struct Layout {
     static constexpr int N = 2 * G;                // hi and lo parts
@@ -107,6 +113,28 @@ __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence:
 
 template <int NC>
 __device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[NC]);
+
+template <>
+__device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, float (&v)[4]) {
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&v)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 
 template <>
 __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16]) {
@@ -209,11 +237,14 @@ enum : int { kBarFull = 0, kBarEmpty = 3, kBarSFull = 6, kBarPFull = 8, kBarOFul
 // MQ: several new tokens per slot (q_len > 1), so the columns of S carry
 // their own causal limits; without it every column shares one row range.
 template <typename CT, int G, bool MQ>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(tc::threads_for(G), 1)
     decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
     using LY = tc::Layout<G>;
     constexpr int N = LY::N, TM = tc::TM, D = tc::D, NS = tc::NS, KB = tc::KB;
+    constexpr int SH = tc::softmax_groups(G);  // softmax warp groups, splitting the query columns
+    constexpr int GH = G / SH;                  // query columns per softmax thread
+    constexpr int SMX = 128 * SH;               // softmax threads
     constexpr int PSZ = round_up(LY::QS, 1024);
     constexpr bool BF = std::is_same_v<CT, __nv_bfloat16>;
     constexpr unsigned FULL = 0xffffffffu;
@@ -448,28 +479,38 @@ __global__ void __launch_bounds__(256, 1)
             if (ok) issue_pv(n_my - 1);
         } else if (warp >= 4) {
             // ------------------------------------------------ softmax and output
-            const int r = tid - 128;  // TMEM lane = row of S = dimension of O
-            const uint32_t lane_base = static_cast<uint32_t>((warp - 4) * 32) << 16;
-            const int q4 = warp - 4;
+            // SH groups of four warps; group ch owns query columns [ch * GH, (ch + 1) * GH)
+            // and thread r of a group owns row r of S (TMEM lane r) and dimension r of O.
+            const int sw = warp - 4;
+            const int ch = sw >> 2, q4 = sw & 3;
+            const int r = (tid - 128) & 127;
+            const int c0 = ch * GH;
+            const bool leader = ch == 0 && r == 0;  // the thread that arrives on the count-1 barriers
+            const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
             Cursor cu = locate(t_begin, P, p.B, segs);
-            float m[G], l[G], o[G], al[G];
-            int tk[G];  // token of each query column (0 unless several new tokens per step)
+            float m[GH], l[GH], o[GH], al[GH];
+            int tk[GH];  // token of each owned query column (0 unless several new tokens per step)
             // output row of query row qi of a kv head
             auto orow = [&](int b, int kvh, int qi) -> size_t {
                 if constexpr (MQ) return q_row(p, b, kvh, qi);
                 return static_cast<size_t>(b) * p.Hq + kvh * p.group + qi;
             };
+            // the owned columns of a hi / lo pair of N-column TMEM blocks starting at col
+            auto ld_cols = [&](uint32_t col, float (&hi)[GH], float (&lo)[GH]) {
+                tc::tmem_ld<GH>(tmem + lane_base + col + c0, hi);
+                tc::tmem_ld<GH>(tmem + lane_base + col + G + c0, lo);
+            };
             bool pending = false;
             int piece_first = cu.tile;
             auto acc_o = [&](int kk) -> bool {
                 const bool okw = tc::wait_or_abort(bar(kBarOFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
-                if (tc::bar_any(2, 128, !okw)) return false;
+                if (tc::bar_any(2, SMX, !okw)) return false;
                 tc::tc_fence_after();
                 __syncwarp();
-                float ov[N];
-                tc::tmem_ld<N>(tmem + lane_base + 2 * N + (kk & 1) * N, ov);
+                float oh[GH], ol[GH];
+                ld_cols(2 * N + (kk & 1) * N, oh, ol);
 #pragma unroll
-                for (int j = 0; j < G; ++j) o[j] = al[j] * o[j] + (ov[j] + ov[G + j]);
+                for (int j = 0; j < GH; ++j) o[j] = al[j] * o[j] + (oh[j] + ol[j]);
                 return true;
             };
             for (int k = 0; k < n_my; ++k) {
@@ -482,16 +523,17 @@ __global__ void __launch_bounds__(256, 1)
                 if (new_piece) {
                     piece_first = cu.tile;
 #pragma unroll
-                    for (int j = 0; j < G; ++j) {
+                    for (int jj = 0; jj < GH; ++jj) {
+                        const int j = c0 + jj;
                         // q row of column j; several tokens per step interleave tokens and heads
                         size_t qrow;
                         int h;
                         if constexpr (MQ) {
-                            tk[j] = q_token(p, hb * G + j);
-                            h = kvh * p.group + (hb * G + j - tk[j] * p.group);
-                            qrow = (static_cast<size_t>(cu.b) * p.nq + tk[j]) * p.Hq + h;
+                            tk[jj] = q_token(p, hb * G + j);
+                            h = kvh * p.group + (hb * G + j - tk[jj] * p.group);
+                            qrow = (static_cast<size_t>(cu.b) * p.nq + tk[jj]) * p.Hq + h;
                         } else {
-                            tk[j] = 0;
+                            tk[jj] = 0;
                             h = kvh * p.group + hb * G + j;
                             qrow = static_cast<size_t>(cu.b) * p.Hq + h;
                         }
@@ -502,54 +544,55 @@ __global__ void __launch_bounds__(256, 1)
                         const CT lo = tc::to_ct<CT>(x - tc::from_ct<CT>(hi));
                         *reinterpret_cast<CT*>(Qs + tc::sw128_offset(j, r, N)) = hi;
                         *reinterpret_cast<CT*>(Qs + tc::sw128_offset(G + j, r, N)) = lo;
-                        m[j] = -INFINITY;
-                        l[j] = 0.f;
-                        o[j] = 0.f;
+                        m[jj] = -INFINITY;
+                        l[jj] = 0.f;
+                        o[jj] = 0.f;
                     }
                     fence_proxy_async_smem();
-                    tc::named_bar_sync(1, 128);
-                    if (r == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarQReady)) : "memory");
+                    tc::named_bar_sync(1, SMX);
+                    if (leader) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarQReady)) : "memory");
                 }
                 // ---- scores of this tile ----
                 const bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag);
-                if (tc::bar_any(2, 128, !oks)) break;
+                if (tc::bar_any(2, SMX, !oks)) break;
                 tc::tc_fence_after();
                 __syncwarp();
-                float sv[N];
-                tc::tmem_ld<N>(tmem + lane_base + (k & 1) * N, sv);
+                float sh[GH], sl_[GH];
+                ld_cols((k & 1) * N, sh, sl_);
                 // column j sees rows [lo0 + tk[j], hi0 + tk[j]): positions up to L + tk[j], from
                 // its own window start on
                 const int hi0 = L + 1 - t0, lo0 = p.window > 0 ? L + 1 - p.window - t0 : -(1 << 30);
                 const bool valid0 = r >= lo0 && r < hi0;  // the rows every column sees (single token)
-                float sc[G];
+                float sc[GH];
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    const bool valid = MQ ? (r >= lo0 + tk[j] && r < hi0 + tk[j]) : valid0;
-                    sc[j] = valid ? sv[j] + sv[G + j] : -INFINITY;
-                    float v = sc[j];
+                for (int jj = 0; jj < GH; ++jj) {
+                    const bool valid = MQ ? (r >= lo0 + tk[jj] && r < hi0 + tk[jj]) : valid0;
+                    sc[jj] = valid ? sh[jj] + sl_[jj] : -INFINITY;
+                    float v = sc[jj];
 #pragma unroll
                     for (int mm = 16; mm >= 1; mm >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, mm));
-                    if (lane == 0) red_max[q4 * G + j] = v;
+                    if (lane == 0) red_max[q4 * G + c0 + jj] = v;
                 }
-                tc::named_bar_sync(1, 128);
-                float alpha[G];
+                tc::named_bar_sync(1, SMX);
+                float alpha[GH];
                 unsigned char* pb = Ps + (k & 1) * PSZ;
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
+                for (int jj = 0; jj < GH; ++jj) {
+                    const int j = c0 + jj;
                     const float tmax = fmaxf(fmaxf(red_max[j], red_max[G + j]), fmaxf(red_max[2 * G + j], red_max[3 * G + j]));
-                    const float mnew = fmaxf(m[j], tmax);
+                    const float mnew = fmaxf(m[jj], tmax);
                     float pj;
                     if constexpr (MQ) {
                         // a column with no visible row yet keeps m = -inf; 0 stands in as the reference
                         const float mref = mnew == -INFINITY ? 0.f : mnew;
-                        alpha[j] = exp2f(m[j] - mref);
-                        pj = exp2f(sc[j] - mref);
+                        alpha[jj] = exp2f(m[jj] - mref);
+                        pj = exp2f(sc[jj] - mref);
                     } else {
-                        alpha[j] = exp2f(m[j] - mnew);
-                        pj = valid0 ? exp2f(sc[j] - mnew) : 0.f;
+                        alpha[jj] = exp2f(m[jj] - mnew);
+                        pj = valid0 ? exp2f(sc[jj] - mnew) : 0.f;
                     }
-                    l[j] = l[j] * alpha[j] + pj;
-                    m[j] = mnew;
+                    l[jj] = l[jj] * alpha[jj] + pj;
+                    m[jj] = mnew;
                     const CT hi = tc::to_ct<CT>(pj);
                     const CT lo = tc::to_ct<CT>(pj - tc::from_ct<CT>(hi));
                     *reinterpret_cast<CT*>(pb + tc::sw128_offset(j, r, N)) = hi;
@@ -557,11 +600,11 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 fence_proxy_async_smem();
                 tc::tc_fence_before();
-                tc::named_bar_sync(1, 128);
-                if (r == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + (k & 1))) : "memory");
+                tc::named_bar_sync(1, SMX);
+                if (leader) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + (k & 1))) : "memory");
                 if (pending && !acc_o(k - 1)) break;
 #pragma unroll
-                for (int j = 0; j < G; ++j) al[j] = alpha[j];
+                for (int jj = 0; jj < GH; ++jj) al[jj] = alpha[jj];
                 pending = true;
 
                 if (last || k == n_my - 1) {
@@ -569,81 +612,84 @@ __global__ void __launch_bounds__(256, 1)
                     pending = false;
                     // ---- end of a piece ----
 #pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        float v = l[j];
+                    for (int jj = 0; jj < GH; ++jj) {
+                        float v = l[jj];
 #pragma unroll
                         for (int mm = 16; mm >= 1; mm >>= 1) v += __shfl_xor_sync(FULL, v, mm);
-                        if (lane == 0) red_sum[q4 * G + j] = v;
+                        if (lane == 0) red_sum[q4 * G + c0 + jj] = v;
                     }
-                    tc::named_bar_sync(1, 128);
-                    float lt[G];
+                    tc::named_bar_sync(1, SMX);
+                    float lt[GH];
 #pragma unroll
-                    for (int j = 0; j < G; ++j) lt[j] = red_sum[j] + red_sum[G + j] + red_sum[2 * G + j] + red_sum[3 * G + j];
+                    for (int jj = 0; jj < GH; ++jj) {
+                        const int j = c0 + jj;
+                        lt[jj] = red_sum[j] + red_sum[G + j] + red_sum[2 * G + j] + red_sum[3 * G + j];
+                    }
                     const int segg = cu.b * segs + cu.seg;
                     if (piece_first == 0 && last) {
 #pragma unroll
-                        for (int j = 0; j < G; ++j)
-                            st_out1(p.out, orow(cu.b, kvh, hb * G + j) * D + r, o[j] / lt[j], p.out_dtype);
+                        for (int jj = 0; jj < GH; ++jj)
+                            st_out1(p.out, orow(cu.b, kvh, hb * G + c0 + jj) * D + r, o[jj] / lt[jj], p.out_dtype);
                     } else {
                         float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
                         if (r == 0) {
 #pragma unroll
-                            for (int j = 0; j < G; ++j) {
-                                slot[j] = m[j];
-                                slot[G + j] = lt[j];
+                            for (int jj = 0; jj < GH; ++jj) {
+                                slot[c0 + jj] = m[jj];
+                                slot[G + c0 + jj] = lt[jj];
                             }
                         }
 #pragma unroll
-                        for (int j = 0; j < G; ++j) slot[LY::OOFF + j * D + r] = o[j];
-                        // the barrier orders the 128 threads' partial stores before thread 0's release
-                        tc::named_bar_sync(1, 128);
+                        for (int jj = 0; jj < GH; ++jj) slot[LY::OOFF + (c0 + jj) * D + r] = o[jj];
+                        // the barrier orders the softmax threads' partial stores before the leader's release
+                        tc::named_bar_sync(1, SMX);
                         const uint32_t piece_tiles = static_cast<uint32_t>(cu.tile - piece_first + 1);
-                        if (r == 0) {
+                        if (leader) {
                             const uint32_t prev = arrive_acq_rel(&p.counters[segg], piece_tiles);
                             bcast[0] = (prev + piece_tiles == static_cast<uint32_t>(cu.nt)) ? 1 : 0;
                         }
-                        // and thread 0's acquire before every thread's merge reads
-                        tc::named_bar_sync(1, 128);
+                        // and the leader's acquire before every thread's merge reads
+                        tc::named_bar_sync(1, SMX);
                         if (bcast[0]) {
                             const long long S0 = P[cu.b] + static_cast<long long>(cu.seg) * cu.nt;
                             const int wf = worker_of(S0, U, W);
                             const int wl = worker_of(S0 + cu.nt - 1, U, W);
                             // one pass over the pieces with a running log-sum-exp; all loads
                             // of a piece are independent, so each piece costs one L2 round trip
-                            float Mx[G], Ls_[G], Ac[G];
+                            float Mx[GH], Ls_[GH], Ac[GH];
 #pragma unroll
-                            for (int j = 0; j < G; ++j) {
-                                Mx[j] = -INFINITY;
-                                Ls_[j] = 0.f;
-                                Ac[j] = 0.f;
+                            for (int jj = 0; jj < GH; ++jj) {
+                                Mx[jj] = -INFINITY;
+                                Ls_[jj] = 0.f;
+                                Ac[jj] = 0.f;
                             }
                             for (int w = wf; w <= wl; ++w) {
                                 if (!((w * U) / W < ((w + 1) * U) / W)) continue;
                                 const float* sl = p.ws + static_cast<size_t>(segg + w) * LY::SLOT;
-                                float mw[G], lw[G], ow[G];
+                                float mw[GH], lw[GH], ow[GH];
 #pragma unroll
-                                for (int j = 0; j < G; ++j) {
-                                    mw[j] = __ldcg(sl + j);
-                                    lw[j] = __ldcg(sl + G + j);
-                                    ow[j] = __ldcg(sl + LY::OOFF + j * D + r);
+                                for (int jj = 0; jj < GH; ++jj) {
+                                    mw[jj] = __ldcg(sl + c0 + jj);
+                                    lw[jj] = __ldcg(sl + G + c0 + jj);
+                                    ow[jj] = __ldcg(sl + LY::OOFF + (c0 + jj) * D + r);
                                 }
 #pragma unroll
-                                for (int j = 0; j < G; ++j) {
-                                    const float mn = fmaxf(Mx[j], mw[j]);
+                                for (int jj = 0; jj < GH; ++jj) {
+                                    const float mn = fmaxf(Mx[jj], mw[jj]);
                                     const float mref = (MQ && mn == -INFINITY) ? 0.f : mn;
-                                    const float a = exp2f(Mx[j] - mref), bb = exp2f(mw[j] - mref);
-                                    Ls_[j] = Ls_[j] * a + lw[j] * bb;
-                                    Ac[j] = Ac[j] * a + ow[j] * bb;
-                                    Mx[j] = mn;
+                                    const float a = exp2f(Mx[jj] - mref), bb = exp2f(mw[jj] - mref);
+                                    Ls_[jj] = Ls_[jj] * a + lw[jj] * bb;
+                                    Ac[jj] = Ac[jj] * a + ow[jj] * bb;
+                                    Mx[jj] = mn;
                                 }
                             }
 #pragma unroll
-                            for (int j = 0; j < G; ++j)
-                                st_out1(p.out, orow(cu.b, kvh, hb * G + j) * D + r, Ac[j] / Ls_[j],
+                            for (int jj = 0; jj < GH; ++jj)
+                                st_out1(p.out, orow(cu.b, kvh, hb * G + c0 + jj) * D + r, Ac[jj] / Ls_[jj],
                                         p.out_dtype);
-                            if (r == 0) p.counters[segg] = 0u;
+                            if (leader) p.counters[segg] = 0u;
                         }
-                        tc::named_bar_sync(1, 128);
+                        tc::named_bar_sync(1, SMX);
                     }
                 }
                 if (k + 1 < n_my) advance(cu, P, segs);
@@ -667,12 +713,14 @@ struct TcKernelInfo {
     int smem;
     int slot_floats;
     int G;
+    int threads;  // threads per CTA (tc::threads_for(G))
 };
 
 template <typename CT, int G, bool MQ>
 TcKernelInfo tc_kernel_info() {
     using LY = tc::Layout<G>;
-    return TcKernelInfo{reinterpret_cast<const void*>(&decode_gqa_tc_kernel<CT, G, MQ>), LY::SMEM, LY::SLOT, G};
+    return TcKernelInfo{reinterpret_cast<const void*>(&decode_gqa_tc_kernel<CT, G, MQ>), LY::SMEM, LY::SLOT, G,
+                        tc::threads_for(G)};
 }
 
 TcKernelInfo select_tc(bool bf16, int G, bool multi_token);
