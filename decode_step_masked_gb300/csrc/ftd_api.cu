@@ -106,6 +106,7 @@ struct ftd_ctx {
     bool use_tc = false;       // grouped-query fp16/bf16 caches run on the tensor cores
     ftd::TcKernelInfo tki{};
     int tc_nhb = 1;
+    int tc_qblk = 8;         // real query rows per tensor-core block
     CUtensorMap tmk;  // the type carries its own alignment
     CUtensorMap tmv;
     const void* tm_k_base = nullptr;
@@ -224,19 +225,21 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     const size_t cache_bytes = rows * D * elem_bytes(c.cache_dtype);
     const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * rows * sizeof(float) : 0;
 
-    // fp16/bf16 caches with head_dim 128 whose kv heads carry a multiple of 8
-    // query rows (group x new tokens) use the tensor-core kernel;
-    // FTD_FORCE_CUDA_CORE=1 in the environment at ftd_init selects the
-    // CUDA-core kernel instead.
+    // fp16/bf16 caches with head_dim 128 whose kv heads carry a multiple of 4
+    // query rows (group x new tokens) use the tensor-core kernel, in blocks of
+    // 16 or 8 rows (blocks of 4 fill half of an 8-column block, since the MMA
+    // needs N >= 16 with the hi/lo split); FTD_FORCE_CUDA_CORE=1 in the
+    // environment at ftd_init selects the CUDA-core kernel instead.
     const char* force = getenv("FTD_FORCE_CUDA_CORE");
     const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
-                         rows_q % 8 == 0 && !(force && force[0] == '1');
+                         rows_q % 4 == 0 && !(force && force[0] == '1');
     ftd::TcKernelInfo tki{};
-    int tc_nhb = 1;
+    int tc_nhb = 1, tc_qblk = 8;
     if (want_tc && encode_tiled()) {
         const int Gt = rows_q % 16 == 0 ? 16 : 8;
+        tc_qblk = rows_q % 8 == 0 ? Gt : 4;
         tki = ftd::select_tc(c.cache_dtype == FTD_BF16, Gt, nq > 1);
-        tc_nhb = rows_q / Gt;
+        tc_nhb = rows_q / tc_qblk;
         e = cudaFuncSetAttribute(tki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tki.smem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (tensor-core kernel)");
     }
@@ -257,6 +260,7 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     ctx->use_tc = use_tc;
     ctx->tki = tki;
     ctx->tc_nhb = tc_nhb;
+    ctx->tc_qblk = tc_qblk;
     const float scale = c.softmax_scale > 0.f ? c.softmax_scale : 1.0f / sqrtf(static_cast<float>(D));
     ctx->qscale = scale * 1.4426950408889634f;
     ctx->nq = nq;
@@ -409,6 +413,7 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
             ctx->tm_v_base = v_cache;
         }
         p.nhb = ctx->tc_nhb;
+        p.qblk = ctx->tc_qblk;
         void* args[] = {&ctx->tmk, &ctx->tmv, &p};
         e = launch_overlapped(ctx->tki.fn, ctx->grid, ctx->tki.threads, ctx->tki.smem, args, stream);
     } else {

@@ -50,6 +50,7 @@ struct DecodeParams {
     int out_dtype;        // kF32 / kF16 / kBF16
     int window;           // > 0: attend only the last `window` positions
     int nq;               // new tokens per slot (q [B][nq][Hq][D]); query rows per kv head = nq * group
+    int qblk;             // query rows per tensor-core block (<= its G; the rest of the block is zero)
     // paged cache: page p of the pool holds rows [p][Hkv][page_size][D];
     // block_table[b * pages_per_seq + i] is the page of positions [i*page_size, (i+1)*page_size)
     const int32_t* block_table;  // nullptr: contiguous [B][Hkv][Lmax][D] cache

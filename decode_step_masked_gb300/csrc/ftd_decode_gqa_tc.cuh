@@ -486,6 +486,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
             const int r = (tid - 128) & 127;
             const int c0 = ch * GH;
             const bool leader = ch == 0 && r == 0;  // the thread that arrives on the count-1 barriers
+            const int QB = p.qblk;  // real query rows of a block; columns QB .. G-1 carry a zero query
             const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
             Cursor cu = locate(t_begin, P, p.B, segs);
             float m[GH], l[GH], o[GH], al[GH];
@@ -529,17 +530,20 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         size_t qrow;
                         int h;
                         if constexpr (MQ) {
-                            tk[jj] = q_token(p, hb * G + j);
-                            h = kvh * p.group + (hb * G + j - tk[jj] * p.group);
+                            tk[jj] = j < QB ? q_token(p, hb * QB + j) : 0;
+                            h = kvh * p.group + (hb * QB + j - tk[jj] * p.group);
                             qrow = (static_cast<size_t>(cu.b) * p.nq + tk[jj]) * p.Hq + h;
                         } else {
                             tk[jj] = 0;
-                            h = kvh * p.group + hb * G + j;
+                            h = kvh * p.group + hb * QB + j;
                             qrow = static_cast<size_t>(cu.b) * p.Hq + h;
                         }
-                        float x = ld_qkv(p.q, p.qkv_dtype, qrow * D + r);
-                        if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + r);
-                        x *= p.qscale;
+                        float x = 0.f;
+                        if (j < QB) {
+                            x = ld_qkv(p.q, p.qkv_dtype, qrow * D + r);
+                            if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + r);
+                            x *= p.qscale;
+                        }
                         const CT hi = tc::to_ct<CT>(x);
                         const CT lo = tc::to_ct<CT>(x - tc::from_ct<CT>(hi));
                         *reinterpret_cast<CT*>(Qs + tc::sw128_offset(j, r, N)) = hi;
@@ -629,7 +633,9 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                     if (piece_first == 0 && last) {
 #pragma unroll
                         for (int jj = 0; jj < GH; ++jj)
-                            st_out1(p.out, orow(cu.b, kvh, hb * G + c0 + jj) * D + r, o[jj] / lt[jj], p.out_dtype);
+                            if (c0 + jj < QB)
+                                st_out1(p.out, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r, o[jj] / lt[jj],
+                                        p.out_dtype);
                     } else {
                         float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
                         if (r == 0) {
@@ -685,8 +691,9 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                             }
 #pragma unroll
                             for (int jj = 0; jj < GH; ++jj)
-                                st_out1(p.out, orow(cu.b, kvh, hb * G + c0 + jj) * D + r, Ac[jj] / Ls_[jj],
-                                        p.out_dtype);
+                                if (c0 + jj < QB)
+                                    st_out1(p.out, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r, Ac[jj] / Ls_[jj],
+                                            p.out_dtype);
                             if (leader) p.counters[segg] = 0u;
                         }
                         tc::named_bar_sync(1, SMX);

@@ -58,7 +58,8 @@ def test_step_bytes_several_new_tokens():
     assert by["kv"] == 2 * w.Hkv * w.D * 2 * 104  # 100 history rows read + 4 rows appended
     by_w = bench.step_bytes(w, lens, window=10, q_len=4)
     assert by_w["ctx"] == 13  # rows some token sees: positions 91 .. 103
-    assert bench.kernel_name(w, 8) == "decode_gqa_tc_kernel" and bench.kernel_name(w, 4) == "decode_splitk_kernel"
+    assert bench.kernel_name(w, 8) == "decode_gqa_tc_kernel" and bench.kernel_name(w, 4) == "decode_gqa_tc_kernel"
+    assert bench.kernel_name(w, 2) == "decode_splitk_kernel"
 
 
 def test_page_table_is_a_permutation():
