@@ -127,6 +127,10 @@ struct ftd_ctx {
     void* st_bias = nullptr;
     int32_t* st_lens = nullptr;
     void* st_out = nullptr;
+    // ftd_decode_mha_host: the host buffers of the last call, and their device
+    // addresses when they are GPU-addressable pinned memory (null otherwise)
+    const void* hp[6] = {};
+    void* hd[6] = {};
     size_t q_bytes = 0, kv_new_bytes = 0, bias_bytes = 0, out_bytes = 0;
     size_t rows = 0;         // cache rows (of head_dim elements) in the pool
     int nq = 1;              // new tokens per slot per step
@@ -446,6 +450,42 @@ ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, 
                          static_cast<cudaStream_t>(stream));
 }
 
+// Copies the step's inputs from GPU-addressable (pinned) host memory into the
+// context's staging buffers in one launch, in place of one copy call per
+// buffer: 16-byte words for q, k_new, v_new and the bias, 4-byte words for the
+// lengths.  On Grace systems the reads cross NVLink-C2C.
+struct GatherArgs {
+    const uint4* src[4];
+    uint4* dst[4];
+    uint32_t n16[4];
+    const int32_t* lens_src;
+    int32_t* lens_dst;
+    uint32_t n_lens;
+};
+
+__global__ void __launch_bounds__(256) gather_step_inputs(GatherArgs a) {
+    // the decode launch that follows may place its blocks now (they hold no shared
+    // memory of ours); they wait in griddepcontrol.wait until this grid has finished
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        for (uint32_t i = t; i < a.n16[k]; i += stride) a.dst[k][i] = a.src[k][i];
+    for (uint32_t i = t; i < a.n_lens; i += stride) a.lens_dst[i] = a.lens_src[i];
+}
+
+// Device address of host pointer p when the GPU can address it (pinned and mapped), else null.
+static void* device_alias(const void* p) {
+    if (!p) return nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                const void* qkv_bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
                                float* scales, void* out, void* stream) {
@@ -457,6 +497,49 @@ ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t B = ctx->cfg.max_batch;
     cudaError_t e;
+
+    // Pinned, GPU-addressable host buffers (looked up once per set of pointers): one
+    // gather launch brings the inputs in, and the kernel writes out straight to the host.
+    const void* hp[6] = {q, k_new, v_new, qkv_bias, seq_lens, out};
+    bool same = true;
+    for (int i = 0; i < 6; ++i) same = same && hp[i] == ctx->hp[i];
+    if (!same) {
+        for (int i = 0; i < 6; ++i) {
+            ctx->hp[i] = hp[i];
+            ctx->hd[i] = device_alias(hp[i]);
+        }
+    }
+    bool direct = true;
+    for (int i = 0; i < 6; ++i) {
+        if (i == 3 && !qkv_bias) continue;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(ctx->hd[i]);
+        direct = direct && a != 0 && (a & (i == 4 ? 3u : 15u)) == 0;
+    }
+    if (direct) {
+        GatherArgs ga{};
+        const void* srcs[4] = {ctx->hd[0], ctx->hd[1], ctx->hd[2], ctx->hd[3]};
+        void* dsts[4] = {ctx->st_q, ctx->st_k, ctx->st_v, ctx->st_bias};
+        const size_t bytes[4] = {ctx->q_bytes, ctx->kv_new_bytes, ctx->kv_new_bytes, qkv_bias ? ctx->bias_bytes : 0};
+        for (int i = 0; i < 4; ++i) {
+            ga.src[i] = static_cast<const uint4*>(srcs[i]);
+            ga.dst[i] = static_cast<uint4*>(dsts[i]);
+            ga.n16[i] = static_cast<uint32_t>(bytes[i] / 16);
+        }
+        ga.lens_src = static_cast<const int32_t*>(ctx->hd[4]);
+        ga.lens_dst = ctx->st_lens;
+        ga.n_lens = static_cast<uint32_t>(B);
+        gather_step_inputs<<<ctx->grid, 256, 0, s>>>(ga);
+        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "input gather launch");
+        g_launches.fetch_add(1);
+        ftd_status st = launch_decode(ctx, ctx->st_q, ctx->st_k, ctx->st_v, qkv_bias ? ctx->st_bias : nullptr,
+                                      k_cache, v_cache, nullptr, ctx->st_lens, scales, ctx->hd[5], s);
+        if (st != FTD_OK) return st;
+        e = cudaStreamSynchronize(s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+        return FTD_OK;
+    }
+
+    // Pageable (or unaligned) host buffers: copies through the staging buffers.
     if ((e = cudaMemcpyAsync(ctx->st_q, q, ctx->q_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
         (e = cudaMemcpyAsync(ctx->st_k, k_new, ctx->kv_new_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
         (e = cudaMemcpyAsync(ctx->st_v, v_new, ctx->kv_new_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||

@@ -198,6 +198,36 @@ def test_pool_pointers_and_host_entry_point():
     step.close()
 
 
+def test_host_entry_point_with_pinned_buffers():
+    """Pinned host buffers take the direct path (one gather launch, output written to the host
+    by the kernel); the result matches the oracle and the caches get the appended rows."""
+    import torch
+    w, inp = small("bf16", "bf16", B=3, Hq=16, Hkv=2, D=128, Lmax=256, lens=[0, 130, 255])
+    ref = oracle.load().decode_step(w, inp)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    kc, vc = dev(inp["k_cache"]), dev(inp["v_cache"])
+
+    def pinned(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).pin_memory()
+
+    hq, hk, hv, hb, hl = (pinned(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens"))
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    for rep in range(2):  # the second call reuses the looked-up device addresses
+        kcur, vcur = kc.clone(), vc.clone()
+        n0 = ftd.ftd_kernel_launches()
+        ftd.check(ftd.ftd_decode_mha_host(step.ctx, hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), hb.data_ptr(),
+                                          kcur.data_ptr(), vcur.data_ptr(), hl.data_ptr(), 0, out.data_ptr(), s))
+        assert ftd.ftd_kernel_launches() - n0 == 2, "pinned buffers should take the gather + decode path"
+        assert_close(out.numpy().astype(np.float64), ref["out"], what=f"pinned host entry point, call {rep}")
+        assert_same_bytes(kcur.cpu().numpy().view(np.uint16), ref["k_cache"], "K after append")
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+
+
 # ------------------------------------------------------------- full size
 SAMPLED = {"7b": [(0, 0), (3, 17), (7, 31)], "13b": [(0, 5), (11, 39), (31, 0), (17, 22)],
            "70b": [(0, 0), (5, 37), (15, 63)], "int8": [(0, 1), (33, 30), (63, 31)]}
