@@ -147,3 +147,52 @@ def test_multi_token_paged_across_pages(cc):
     got_v = from_pages(w, vd.cpu().numpy().view(np.uint16), table, ps, L, q_len=T)
     assert_same_bytes(got_v, valid_rows(w, ref["v_cache"], L, q_len=T), "V pages after append")
     assert_same_bytes(kd.cpu().numpy().view(np.uint16)[spare], kp[spare], "spare pages untouched")
+
+
+# every option at once: paged cache, sliding window, several tokens per step, half output
+COMBINED = {
+    "i8_cc": ("i8", "f16", 3, 8, 8, 128, 512, [126, 0, 380], 3, False),
+    "bf16_tc": ("bf16", "bf16", 3, 32, 4, 128, 1024, [126, 700, 1000], 2, False),
+    "bf16_cc": ("bf16", "bf16", 3, 32, 4, 128, 1024, [126, 700, 1000], 2, True),
+    "f16_mha_tc": ("f16", "f16", 2, 4, 4, 128, 512, [250, 100], 4, False),
+}
+
+
+@pytest.mark.parametrize("window", [0, 200])
+@pytest.mark.parametrize("name", list(COMBINED))
+def test_all_options_together(name, window):
+    import torch
+    cache, qkv, B, Hq, Hkv, D, Lmax, lens, T, cc = COMBINED[name]
+    ps = 128
+    w, inp = case(cache, qkv, B, Hq, Hkv, D, Lmax, lens, T)
+    table, num_pages, spare = page_layout(w, inp["seq_lens"], ps, spare=2, seed=11, q_len=T)
+    ref = oracle.load().decode_step(w, inp, nthreads=8, window=window)
+    nan = {"i8": np.int8(127), "bf16": np.uint16(0x7FC0), "f16": np.float16(np.nan)}[cache]
+    kp = to_pages(w, inp["k_cache"], table, num_pages, ps, nan)
+    vp = to_pages(w, inp["v_cache"], table, num_pages, ps, nan)
+    sp = None
+    if cache == "i8":
+        sp = np.stack([to_pages(w, inp["scales"][i][..., None], table, num_pages, ps, np.nan)[..., 0]
+                       for i in range(2)])
+    step = make_step(w, force_cuda_core=cc, out_dtype="bf16", window=window, page_size=ps, num_pages=num_pages,
+                     q_len=T)
+    kd, vd = dev(kp), dev(vp)
+    sd = dev(sp) if sp is not None else None
+    out = torch.full((w.B, T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    step.paged(dev(inp["q"]), dev(inp["k_new"]), dev(inp["v_new"]), dev(table), dev(inp["seq_lens"]), out,
+               bias=dev(inp["bias"]), k_pages=kd, v_pages=vd, scales=sd)
+    torch.cuda.synchronize()
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+    got = out.double().cpu().numpy()
+    tol = 1e-2 if cache == "i8" else TOL_MAXABS
+    mant = 7  # bf16 output: fp32 bar plus half an output ulp
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref["out"]) + tol, 2.0 ** -126))) - mant)
+    assert np.all(np.abs(got - ref["out"]) <= tol + 0.5 * ulp), name
+    L = inp["seq_lens"]
+    like = inp["k_cache"].dtype
+    got_k = from_pages(w, kd.cpu().numpy().view(like), table, ps, L, q_len=T)
+    assert_same_bytes(got_k, valid_rows(w, ref["k_cache"], L, q_len=T), f"{name} K pages after append")
+    if cache == "i8":
+        g = from_pages(w, sd.cpu().numpy()[0][..., None], table, ps, L, q_len=T)[..., 0]
+        assert_same_bytes(g, valid_rows(w, ref["scales"][0], L, q_len=T), f"{name} K scales after append")

@@ -83,3 +83,38 @@ def test_noalloc_reports_overflow_and_rejects_oversized_configs():
                                     vc.data_ptr(), sl.data_ptr(), 0, out.data_ptr(), 0, s)
     assert st == ftd.FTD_ERR_INVALID_ARG
     assert "static array" in ftd.ftd_last_error()
+
+
+def test_noalloc_with_window_half_output_and_several_tokens():
+    """The options the no-allocation entry point accepts (all but pages) give the context path's bytes."""
+    import torch
+    T = 3
+    w = Workload("noalloc", B=3, Hq=8, Hkv=8, D=128, Lmax=512, qkv_dtype="f16", cache_dtype="i8", bias_std=0.1,
+                 seed=24, q_len=T)
+    inp = gen_all(w, seed=24, seq_lens=np.array([200, 0, 509], np.int32), fill_beyond="nan")
+    opts = dict(out_dtype="bf16", window=64, q_len=T)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, **opts)
+    cfg = ftd.FtdConfig(w.B, w.Hq, w.Hkv, w.D, w.Lmax, ftd.FTD_F16, ftd.FTD_I8, 0.0, ftd.FTD_BF16, 64, 0, 0, T)
+    s = torch.cuda.current_stream().cuda_stream
+    q, kn, vn, bias, sl = (dev(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens"))
+    outs, caches = [], []
+    for use_noalloc in (False, True):
+        kc, vc, sc = dev(inp["k_cache"]), dev(inp["v_cache"]), dev(inp["scales"])
+        out = torch.full((w.B, T, w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+        if use_noalloc:
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            st = ftd.ftd_decode_mha_noalloc(cfg, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), bias.data_ptr(),
+                                            kc.data_ptr(), vc.data_ptr(), sl.data_ptr(), sc.data_ptr(),
+                                            out.data_ptr(), err.data_ptr(), s)
+            assert st == ftd.FTD_OK, ftd.ftd_last_error()
+        else:
+            step(q, kn, vn, sl, out, bias=bias, k_cache=kc, v_cache=vc, scales=sc)
+        torch.cuda.synchronize()
+        outs.append(out.float().cpu().numpy())
+        caches.append((kc.cpu().numpy(), sc.cpu().numpy()))
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+    assert np.all(np.isfinite(outs[1]))
+    assert np.max(np.abs(outs[0] - outs[1])) <= 1e-2
+    assert np.array_equal(caches[0][0], caches[1][0])
+    assert np.array_equal(caches[0][1].view(np.uint32), caches[1][1].view(np.uint32))  # NaN fill past the lengths
