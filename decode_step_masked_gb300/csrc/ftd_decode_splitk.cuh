@@ -75,7 +75,15 @@ struct Tiling {
     static constexpr int RB = cmax(1, cmin(R, 16 / G));        // rows per reduce-scatter batch
     static constexpr int SCRATCH = 2 * G * T * 4;              // scores + probabilities
     static constexpr int WARP_BYTES = round_up(SPW * STAGE + SCRATCH + SPW * 8, 128);
-    static constexpr int PREFIX_BYTES = round_up((2 * kMaxBatch + 1) * 4, 128);
+    // Static split weights: a segment boundary inside a worker's range costs it a partial,
+    // an arrival, the append and the next segment's q (and often the merge), so each
+    // segment start counts ALPHA extra tiles and a worker that crosses one gets fewer.
+    // The weighted prefix needs one more [B + 1] array; where shared memory has no room
+    // for it, ALPHA is 0 and the plain tile prefix serves.
+    static constexpr bool HAVE_VP =
+        round_up((3 * kMaxBatch + 2) * 4, 128) + WARPS * WARP_BYTES <= 232448;
+    static constexpr int ALPHA = HAVE_VP ? (I8 ? 1 : 4) : 0;  // measured: 7B/13B best at 4, INT8 at 1
+    static constexpr int PREFIX_BYTES = round_up(((HAVE_VP ? 3 : 2) * kMaxBatch + 2) * 4, 128);
     static constexpr int SMEM = PREFIX_BYTES + WARPS * WARP_BYTES;
     static constexpr int OOFF = round_up(2 * G, 4);            // o offset in a partial slot
     static constexpr int SLOT = OOFF + G * D;                  // floats per partial slot
@@ -247,6 +255,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     extern __shared__ __align__(128) unsigned char smem[];
     int* P = reinterpret_cast<int*>(smem);  // [B + 1] tile prefix over slots
     int* Ls = P + (kMaxBatch + 1);          // [B] cached length, -1 when the slot has no work
+    int* VP = TL::HAVE_VP ? Ls + kMaxBatch : P;  // [B + 1] weighted prefix: tiles + ALPHA per segment
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hr = lane >> 4, c = lane & 15;
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
     // Tiles per slot and their prefix; overflowing slots raise the sticky flag.
     if (warp == 0) {
-        int carry = 0;
+        int carry = 0, vcarry = 0;
         bool ovf = false;
         for (int base = 0; base < p.B; base += 32) {
             const int b = base + lane;
@@ -273,18 +282,28 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
             ovf |= (b < p.B) && (L > p.Lmax - p.nq);
             // tiles per segment: from the tile holding the window start to the tile of position L + nq - 1
             int v = valid ? ((L + p.nq - 1) / T + 1 - window_start(L, p.window) / T) * segs : 0;
+            int vw = v + (valid ? TL::ALPHA * segs : 0);
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const int y = __shfl_up_sync(FULL, v, m);
-                if (lane >= m) v += y;
+                const int yw = __shfl_up_sync(FULL, vw, m);
+                if (lane >= m) {
+                    v += y;
+                    vw += yw;
+                }
             }
             if (b < p.B) {
                 P[b + 1] = carry + v;
+                VP[b + 1] = vcarry + vw;
                 Ls[b] = valid ? L : -1;
             }
             carry += __shfl_sync(FULL, v, 31);
+            vcarry += __shfl_sync(FULL, vw, 31);
         }
-        if (lane == 0) P[0] = 0;
+        if (lane == 0) {
+            P[0] = 0;
+            VP[0] = 0;
+        }
         if (__any_sync(FULL, ovf) && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
     }
     fence_mbar_init();
@@ -298,10 +317,37 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     }
 
     const long long U = P[p.B];
+    const long long V = VP[p.B];  // weighted length of the tile space
     const long long W = static_cast<long long>(gridDim.x) * TL::WARPS;
     const int wid = blockIdx.x * TL::WARPS + warp;
-    const int t_begin = static_cast<int>(wid * U / W);
-    const int n_my = static_cast<int>((wid + 1) * U / W) - t_begin;
+    // Worker w takes the tiles whose weighted position v lies in [ceil(w V / W), ceil((w+1) V / W)):
+    // tile i of segment s of slot b sits at VP[b] + s (nt + ALPHA) + i.
+    auto range_begin = [&](long long w) -> int {
+        if (w <= 0) return 0;
+        if (w >= W) return static_cast<int>(U);
+        const long long vt = (w * V + W - 1) / W;
+        int lo = 0, hi = p.B - 1;  // largest b with VP[b] <= vt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (VP[mid] <= vt) lo = mid;
+            else hi = mid - 1;
+        }
+        const int b = lo;
+        if (VP[b + 1] <= vt) return P[b + 1];
+        const int nt = (P[b + 1] - P[b]) / segs;
+        const long long o = vt - VP[b];
+        const long long sg = o / (nt + TL::ALPHA);
+        const long long r = o - sg * (nt + TL::ALPHA);
+        return P[b] + static_cast<int>(sg * nt + (r < nt ? r : nt));
+    };
+    const bool narrow = V * W < (1ll << 32);  // products fit 32 bits: cheaper divisions
+    auto worker_at = [&](int b, int seg, int nt, int i) -> int {
+        const long long v = VP[b] + static_cast<long long>(seg) * (nt + TL::ALPHA) + i;
+        if (narrow) return static_cast<int>(static_cast<uint32_t>(v * W) / static_cast<uint32_t>(V));
+        return static_cast<int>(v * W / V);
+    };
+    const int t_begin = range_begin(wid);
+    const int n_my = range_begin(wid + 1) - t_begin;
     if (n_my <= 0) return;
 
     // ---- bulk copies of one tile (lane 0 only) ----
@@ -430,10 +476,13 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     auto merge_segment = [&](const Cursor& mc) {
         const int segg = mc.b * segs + mc.seg;
         const int kvh = mc.seg / p.nhb, hb = mc.seg % p.nhb;
-        const long long S0 = P[mc.b] + static_cast<long long>(mc.seg) * mc.nt;
-        const int wf = worker_of(S0, U, W);
-        const int wl = worker_of(S0 + mc.nt - 1, U, W);
-        auto has_piece = [&](int w) { return (w * U) / W < ((w + 1) * U) / W; };
+        const int wf = worker_at(mc.b, mc.seg, mc.nt, 0);
+        const int wl = worker_at(mc.b, mc.seg, mc.nt, mc.nt - 1);
+        // wf and wl hold the segment's first and last tiles; a worker between them holds tiles
+        // whenever its weighted range is not empty, which V >= W guarantees
+        auto has_piece = [&](int w) {
+            return V >= W || w == wf || w == wl || range_begin(w) < range_begin(w + 1);
+        };
         // one pass over the pieces with a running log-sum-exp per query row
         constexpr int DL = D / 32;
         float Mx[G], Ls_[G], Ac[G][DL];
