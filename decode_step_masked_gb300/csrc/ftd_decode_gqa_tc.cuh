@@ -51,6 +51,9 @@ constexpr int STAGE = 4 * KB;  // K (2 boxes) + V (2 boxes)
 // groups of four warps split the columns (each thread handles half of them),
 // so a CTA runs 384 threads: warps 0-3 for copies and MMA, warps 4-11 softmax.
 constexpr int softmax_groups(int G) { return G >= 8 ? 2 : 1; }
+
+// Weight of a segment boundary in the static split (in 128-row tiles; see WeightedSplit).
+constexpr int kAlpha = 1;
 constexpr int threads_for(int G) { return 128 + 128 * softmax_groups(G); }
 
 template <int G>
@@ -65,7 +68,10 @@ struct Layout {
     static constexpr int OFF_MISC = OFF_RED + round_up(RED_BYTES, 128);
     static constexpr int MISC_BYTES = 256;           // barriers, TMEM base, flags
     static constexpr int OFF_PREFIX = OFF_MISC + MISC_BYTES;
-    static constexpr int PREFIX_BYTES = (2 * kMaxBatch + 1) * 4;
+    // P, Ls and, where shared memory has room, the weighted prefix VP (else the split is unweighted)
+    static constexpr bool HAVE_VP = OFF_PREFIX + round_up((3 * kMaxBatch + 2) * 4, 128) + 1024 <= 232448;
+    static constexpr int ALPHA = HAVE_VP ? kAlpha : 0;
+    static constexpr int PREFIX_BYTES = ((HAVE_VP ? 3 : 2) * kMaxBatch + 2) * 4;
     static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;  // + alignment slack
     static constexpr int TMEM_COLS = (4 * N <= 32) ? 32 : (4 * N <= 64 ? 64 : 128);
     static constexpr int OOFF = round_up(2 * G, 4);
@@ -263,6 +269,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
     int* bcast = reinterpret_cast<int*>(smem + LY::OFF_MISC + kNumBars * 8 + 8);
     int* P = reinterpret_cast<int*>(smem + LY::OFF_PREFIX);
     int* Ls = P + (kMaxBatch + 1);
+    int* VP = LY::HAVE_VP ? Ls + kMaxBatch : P;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int segs = p.Hkv * p.nhb;
@@ -279,29 +286,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
     }
     grid_dep_wait();    // inputs, caches and lengths may come from the previous launch
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
-    if (warp == 0) {
-        int carry = 0;
-        bool ovf = false;
-        for (int base = 0; base < p.B; base += 32) {
-            const int b = base + lane;
-            const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
-            const bool valid = L >= 0 && L <= p.Lmax - p.nq;
-            ovf |= (b < p.B) && (L > p.Lmax - p.nq);
-            int v = valid ? ((L + p.nq - 1) / TM + 1 - window_start(L, p.window) / TM) * segs : 0;
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                const int y = __shfl_up_sync(FULL, v, m);
-                if (lane >= m) v += y;
-            }
-            if (b < p.B) {
-                P[b + 1] = carry + v;
-                Ls[b] = valid ? L : -1;
-            }
-            carry += __shfl_sync(FULL, v, 31);
-        }
-        if (lane == 0) P[0] = 0;
-        if (__any_sync(FULL, ovf) && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
-    }
+    if (warp == 0) build_prefix(p, TM, segs, LY::ALPHA, P, VP, Ls, lane);
     fence_mbar_init();
     tc::tc_fence_before();
     __syncthreads();
@@ -314,11 +299,11 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
         }
     }
 
-    const long long U = P[p.B];
     const long long W = gridDim.x;
     const int wid = blockIdx.x;
-    const int t_begin = static_cast<int>(wid * U / W);
-    const int n_my = static_cast<int>((wid + 1) * U / W) - t_begin;
+    const WeightedSplit<LY::ALPHA> split{P, VP, p.B, segs, static_cast<int>(W)};
+    const int t_begin = split.begin(wid);
+    const int n_my = split.begin(wid + 1) - t_begin;
 
     if (n_my > 0) {
         if (warp == 0) {
@@ -657,9 +642,8 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         // and the leader's acquire before every thread's merge reads
                         tc::named_bar_sync(1, SMX);
                         if (bcast[0]) {
-                            const long long S0 = P[cu.b] + static_cast<long long>(cu.seg) * cu.nt;
-                            const int wf = worker_of(S0, U, W);
-                            const int wl = worker_of(S0 + cu.nt - 1, U, W);
+                            const int wf = split.worker_at(cu.b, cu.seg, cu.nt, 0);
+                            const int wl = split.worker_at(cu.b, cu.seg, cu.nt, cu.nt - 1);
                             // one pass over the pieces with a running log-sum-exp; all loads
                             // of a piece are independent, so each piece costs one L2 round trip
                             float Mx[GH], Ls_[GH], Ac[GH];
@@ -670,7 +654,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                                 Ac[jj] = 0.f;
                             }
                             for (int w = wf; w <= wl; ++w) {
-                                if (!((w * U) / W < ((w + 1) * U) / W)) continue;
+                                if (!split.has_piece(w, wf, wl)) continue;
                                 const float* sl = p.ws + static_cast<size_t>(segg + w) * LY::SLOT;
                                 float mw[GH], lw[GH], ow[GH];
 #pragma unroll

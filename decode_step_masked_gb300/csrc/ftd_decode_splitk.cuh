@@ -237,11 +237,97 @@ __device__ __forceinline__ void advance(Cursor& cu, const int* P, int segs) {
     cu.nt = (P[cu.b + 1] - P[cu.b]) / segs;
 }
 
-// Worker (global warp index) whose range holds tile t, for ranges
-// [floor(w*U/W), floor((w+1)*U/W)).
-__device__ __forceinline__ int worker_of(long long t, long long U, long long W) {
-    return static_cast<int>(((t + 1) * W - 1) / U);
+// Tiles per slot and their prefixes, computed by one warp: P[b] counts the tiles
+// of the slots before b (segments of T rows, from the tile holding the window start
+// to the tile of position L + nq - 1, times segs), VP[b] the same plus ALPHA per
+// segment, Ls[b] the cached length (-1 for slots without work).  Slots with
+// L + nq > Lmax raise the sticky overflow flag (once, from block 0).
+__device__ __forceinline__ void build_prefix(const DecodeParams& p, int T, int segs, int alpha, int* P, int* VP,
+                                             int* Ls, int lane) {
+    constexpr unsigned FULL = 0xffffffffu;
+    int carry = 0, vcarry = 0;
+    bool ovf = false;
+    for (int base = 0; base < p.B; base += 32) {
+        const int b = base + lane;
+        const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
+        const bool valid = L >= 0 && L <= p.Lmax - p.nq;
+        ovf |= (b < p.B) && (L > p.Lmax - p.nq);
+        int v = valid ? ((L + p.nq - 1) / T + 1 - window_start(L, p.window) / T) * segs : 0;
+        int vw = v + (valid ? alpha * segs : 0);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int y = __shfl_up_sync(FULL, v, m);
+            const int yw = __shfl_up_sync(FULL, vw, m);
+            if (lane >= m) {
+                v += y;
+                vw += yw;
+            }
+        }
+        if (b < p.B) {
+            P[b + 1] = carry + v;
+            VP[b + 1] = vcarry + vw;
+            Ls[b] = valid ? L : -1;
+        }
+        carry += __shfl_sync(FULL, v, 31);
+        vcarry += __shfl_sync(FULL, vw, 31);
+    }
+    if (lane == 0) {
+        P[0] = 0;
+        VP[0] = 0;
+    }
+    if (__any_sync(FULL, ovf) && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
 }
+
+// Static split of the tile space over W workers, weighted: a segment boundary inside
+// a worker's range costs it a partial, an arrival, the append and the next segment's
+// q (and often the merge), so tile i of segment s of slot b sits at weighted position
+// VP[b] + s (nt + ALPHA) + i, and worker w takes the tiles whose position lies in
+// [ceil(w V / W), ceil((w+1) V / W)), V the weighted length.  A worker that crosses a
+// boundary therefore gets about ALPHA fewer tiles.  ALPHA = 0 is the plain equal split.
+// P and VP live in shared memory; their totals are read from there when needed.
+template <int ALPHA>
+struct WeightedSplit {
+    const int* P;
+    const int* VP;
+    int B, segs, W;
+
+    __device__ long long U() const { return P[B]; }
+    __device__ long long V() const { return VP[B]; }
+
+    // first tile of worker w (U for w >= W)
+    __device__ int begin(long long w) const {
+        if (w <= 0) return 0;
+        if (w >= W) return P[B];
+        const long long vt = (w * V() + W - 1) / W;
+        int lo = 0, hi = B - 1;  // largest b with VP[b] <= vt
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (VP[mid] <= vt) lo = mid;
+            else hi = mid - 1;
+        }
+        if (VP[lo + 1] <= vt) return P[lo + 1];
+        const int nt = (P[lo + 1] - P[lo]) / segs;
+        const long long o = vt - VP[lo];
+        const long long sg = o / (nt + ALPHA);
+        const long long r = o - sg * (nt + ALPHA);
+        return P[lo] + static_cast<int>(sg * nt + (r < nt ? r : nt));
+    }
+
+    // worker holding tile i of segment seg (nt tiles) of slot b
+    __device__ int worker_at(int b, int seg, int nt, int i) const {
+        const long long v = VP[b] + static_cast<long long>(seg) * (nt + ALPHA) + i;
+        const long long vv = V();
+        if (vv * W < (1ll << 32))  // the product fits 32 bits: a cheaper division
+            return static_cast<int>(static_cast<uint32_t>(v * W) / static_cast<uint32_t>(vv));
+        return static_cast<int>(v * W / vv);
+    }
+
+    // whether worker w, between the holders wf and wl of a segment's first and last
+    // tiles, holds tiles of it: always when V >= W (every weighted range is non-empty)
+    __device__ bool has_piece(int w, int wf, int wl) const {
+        return V() >= W || w == wf || w == wl || begin(w) < begin(w + 1);
+    }
+};
 
 // ================================================================ kernel
 template <typename CT, int D, int G>
@@ -271,41 +357,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     }
     grid_dep_wait();    // inputs, caches and lengths may come from the previous launch
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
-    // Tiles per slot and their prefix; overflowing slots raise the sticky flag.
-    if (warp == 0) {
-        int carry = 0, vcarry = 0;
-        bool ovf = false;
-        for (int base = 0; base < p.B; base += 32) {
-            const int b = base + lane;
-            const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
-            const bool valid = L >= 0 && L <= p.Lmax - p.nq;
-            ovf |= (b < p.B) && (L > p.Lmax - p.nq);
-            // tiles per segment: from the tile holding the window start to the tile of position L + nq - 1
-            int v = valid ? ((L + p.nq - 1) / T + 1 - window_start(L, p.window) / T) * segs : 0;
-            int vw = v + (valid ? TL::ALPHA * segs : 0);
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                const int y = __shfl_up_sync(FULL, v, m);
-                const int yw = __shfl_up_sync(FULL, vw, m);
-                if (lane >= m) {
-                    v += y;
-                    vw += yw;
-                }
-            }
-            if (b < p.B) {
-                P[b + 1] = carry + v;
-                VP[b + 1] = vcarry + vw;
-                Ls[b] = valid ? L : -1;
-            }
-            carry += __shfl_sync(FULL, v, 31);
-            vcarry += __shfl_sync(FULL, vw, 31);
-        }
-        if (lane == 0) {
-            P[0] = 0;
-            VP[0] = 0;
-        }
-        if (__any_sync(FULL, ovf) && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
-    }
+    if (warp == 0) build_prefix(p, T, segs, TL::ALPHA, P, VP, Ls, lane);
     fence_mbar_init();
     __syncthreads();
 
@@ -316,38 +368,11 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
         }
     }
 
-    const long long U = P[p.B];
-    const long long V = VP[p.B];  // weighted length of the tile space
     const long long W = static_cast<long long>(gridDim.x) * TL::WARPS;
     const int wid = blockIdx.x * TL::WARPS + warp;
-    // Worker w takes the tiles whose weighted position v lies in [ceil(w V / W), ceil((w+1) V / W)):
-    // tile i of segment s of slot b sits at VP[b] + s (nt + ALPHA) + i.
-    auto range_begin = [&](long long w) -> int {
-        if (w <= 0) return 0;
-        if (w >= W) return static_cast<int>(U);
-        const long long vt = (w * V + W - 1) / W;
-        int lo = 0, hi = p.B - 1;  // largest b with VP[b] <= vt
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (VP[mid] <= vt) lo = mid;
-            else hi = mid - 1;
-        }
-        const int b = lo;
-        if (VP[b + 1] <= vt) return P[b + 1];
-        const int nt = (P[b + 1] - P[b]) / segs;
-        const long long o = vt - VP[b];
-        const long long sg = o / (nt + TL::ALPHA);
-        const long long r = o - sg * (nt + TL::ALPHA);
-        return P[b] + static_cast<int>(sg * nt + (r < nt ? r : nt));
-    };
-    const bool narrow = V * W < (1ll << 32);  // products fit 32 bits: cheaper divisions
-    auto worker_at = [&](int b, int seg, int nt, int i) -> int {
-        const long long v = VP[b] + static_cast<long long>(seg) * (nt + TL::ALPHA) + i;
-        if (narrow) return static_cast<int>(static_cast<uint32_t>(v * W) / static_cast<uint32_t>(V));
-        return static_cast<int>(v * W / V);
-    };
-    const int t_begin = range_begin(wid);
-    const int n_my = range_begin(wid + 1) - t_begin;
+    const WeightedSplit<TL::ALPHA> split{P, VP, p.B, segs, static_cast<int>(W)};
+    const int t_begin = split.begin(wid);
+    const int n_my = split.begin(wid + 1) - t_begin;
     if (n_my <= 0) return;
 
     // ---- bulk copies of one tile (lane 0 only) ----
@@ -476,13 +501,9 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     auto merge_segment = [&](const Cursor& mc) {
         const int segg = mc.b * segs + mc.seg;
         const int kvh = mc.seg / p.nhb, hb = mc.seg % p.nhb;
-        const int wf = worker_at(mc.b, mc.seg, mc.nt, 0);
-        const int wl = worker_at(mc.b, mc.seg, mc.nt, mc.nt - 1);
-        // wf and wl hold the segment's first and last tiles; a worker between them holds tiles
-        // whenever its weighted range is not empty, which V >= W guarantees
-        auto has_piece = [&](int w) {
-            return V >= W || w == wf || w == wl || range_begin(w) < range_begin(w + 1);
-        };
+        const int wf = split.worker_at(mc.b, mc.seg, mc.nt, 0);
+        const int wl = split.worker_at(mc.b, mc.seg, mc.nt, mc.nt - 1);
+        auto has_piece = [&](int w) { return split.has_piece(w, wf, wl); };
         // one pass over the pieces with a running log-sum-exp per query row
         constexpr int DL = D / 32;
         float Mx[G], Ls_[G], Ac[G][DL];
