@@ -336,6 +336,8 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     constexpr int T = TL::T, R = TL::R, EPL = TL::EPL, ROW = TL::ROW, SPW = TL::SPW, RB = TL::RB;
     constexpr int TILE = TL::TILE, SCL = TL::SCL, STAGE = TL::STAGE, EB = TL::EB;
     constexpr bool I8 = TL::I8;
+    // INT8 blocks of <= 2 query rows on 32-row tiles: P.V on dp4a with integer weights
+    constexpr bool IPV = I8 && G <= 2 && T == 32;
     constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ __align__(128) unsigned char smem[];
@@ -742,6 +744,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
 
         // ---- online softmax over the tile (log2 domain) ----
         float alpha[G];
+        float wsc[G];  // dp4a P.V: the tile's weight scale per query row
         const int r = lane % T;
         // query row j sees rows [lo_j, hi_j) of the tile: positions up to L + tk[j], and from
         // its own window start on
@@ -767,7 +770,29 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
             for (int mm = T / 2; mm >= 1; mm >>= 1) tsum += __shfl_xor_sync(FULL, tsum, mm);
             l[j] = l[j] * alpha[j] + tsum;
             m[j] = mnew;
-            if (lane < T) {
+            if constexpr (IPV) {
+                // weights w = p * vscale as three int8 levels of the tile's largest weight,
+                // w ~ s1 (h + m / 254 + q / 254^2), byte-packed per group of 4 rows of a half-warp
+                const float wgt =
+                    (r >= r_lo && r < n_total) ? pv * reinterpret_cast<const float*>(st + 2 * TILE + SCL)[r] : 0.f;
+                float wmax = wgt;
+#pragma unroll
+                for (int mm = 16; mm >= 1; mm >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(FULL, wmax, mm));
+                const float s1 = wmax > 0.f ? wmax / 127.f : 1.f;
+                const float inv1 = 1.f / s1;
+                const int h = __float2int_rn(wgt * inv1);
+                const float r1 = wgt - static_cast<float>(h) * s1;
+                const int mq = max(-127, min(127, __float2int_rn(r1 * (254.f * inv1))));
+                const float r2 = r1 - static_cast<float>(mq) * (s1 * (1.f / 254.f));
+                const int lq = max(-127, min(127, __float2int_rn(r2 * (64516.f * inv1))));
+                const int rh = r & 1, gi = (r >> 1) >> 2, kk = (r >> 1) & 3;  // half-warp, group, position
+                signed char* pq = reinterpret_cast<signed char*>(pb);
+#pragma unroll
+                for (int lv = 0; lv < 3; ++lv)
+                    pq[((((lv * G + j) * 2 + rh) * 4 + gi) * 4) + kk] =
+                        static_cast<signed char>(lv == 0 ? h : (lv == 1 ? mq : lq));
+                wsc[j] = s1;
+            } else if (lane < T) {
                 float wgt = pv;
                 if constexpr (I8)
                     wgt = (r >= r_lo && r < n_total) ? pv * reinterpret_cast<const float*>(st + 2 * TILE + SCL)[r] : 0.f;
@@ -791,7 +816,53 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
                 for (int e = 0; e < EPL; ++e) o[j][e] = fmaf(pj, vf[e], o[j][e]);
             }
         };
-        if (r_lo == 0 && n_total == T) {  // whole tile visible: no per-row test
+        if constexpr (IPV) {
+            // dp4a P.V: four rows of codes, transposed so each word holds one column's four
+            // bytes, times the four rows' packed weights, for each weight level.  Rows with
+            // weight 0 (masked or stale) contribute nothing; codes are plain integers.
+            int acc[G][EPL][3];
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e)
+#pragma unroll
+                    for (int lv = 0; lv < 3; ++lv) acc[j][e][lv] = 0;
+            const int* pw = reinterpret_cast<const int*>(pb);
+#pragma unroll
+            for (int g = 0; g < R / 4; ++g) {
+                uint32_t col[EPL];
+#pragma unroll
+                for (int half = 0; half < EPL / 4; ++half) {
+                    uint32_t a[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        a[k] = *reinterpret_cast<const uint32_t*>(Vt + (2 * (4 * g + k) + hr) * ROW + c * EPL + 4 * half);
+                    const uint32_t t0 = __byte_perm(a[0], a[1], 0x5140), t1 = __byte_perm(a[0], a[1], 0x7362);
+                    const uint32_t t2 = __byte_perm(a[2], a[3], 0x5140), t3 = __byte_perm(a[2], a[3], 0x7362);
+                    col[4 * half + 0] = __byte_perm(t0, t2, 0x5410);
+                    col[4 * half + 1] = __byte_perm(t0, t2, 0x7632);
+                    col[4 * half + 2] = __byte_perm(t1, t3, 0x5410);
+                    col[4 * half + 3] = __byte_perm(t1, t3, 0x7632);
+                }
+#pragma unroll
+                for (int j = 0; j < G; ++j)
+#pragma unroll
+                    for (int lv = 0; lv < 3; ++lv) {
+                        const int wq = pw[((lv * G + j) * 2 + hr) * 4 + g];
+#pragma unroll
+                        for (int e = 0; e < EPL; ++e) acc[j][e][lv] = __dp4a(static_cast<int>(col[e]), wq, acc[j][e][lv]);
+                    }
+            }
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float s2 = wsc[j] * (1.f / 254.f);
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) {
+                    const float hm = static_cast<float>(acc[j][e][0] * 254 + acc[j][e][1]);
+                    o[j][e] = fmaf(s2, hm + static_cast<float>(acc[j][e][2]) * (1.f / 254.f), o[j][e]);
+                }
+            }
+        } else if (r_lo == 0 && n_total == T) {  // whole tile visible: no per-row test
 #pragma unroll
             for (int i = 0; i < R; ++i) pv_row(2 * i + hr);
         } else {  // rows outside [r_lo, n_total) hold stale stage data and are skipped

@@ -198,6 +198,18 @@ def test_pool_pointers_and_host_entry_point():
     step.close()
 
 
+@pytest.mark.parametrize("cache,Hq,Hkv", [("bf16", 2, 2), ("i8", 2, 2), ("f16", 8, 1)])
+def test_maximum_batch(cache, Hq, Hkv):
+    """1024 slots (the largest batch), ragged short contexts with inactive and overflowing slots:
+    the prefix over slots and the weighted split search over the whole batch."""
+    rng = np.random.default_rng(5)
+    lens = rng.integers(-3, 64, size=1024).astype(np.int32)  # negative: inactive; 63: at Lmax - 1
+    lens[17] = 64  # overflow
+    w, inp = small(cache, "f16" if cache != "bf16" else "bf16", B=1024, Hq=Hq, Hkv=Hkv, D=64, Lmax=64,
+                   lens=lens)
+    check_step(w, inp, what=f"1024 slots {cache} Hq{Hq} Hkv{Hkv}")
+
+
 def test_host_entry_point_with_pinned_buffers():
     """Pinned host buffers take the direct path (one gather launch, output written to the host
     by the kernel); the result matches the oracle and the caches get the appended rows."""
