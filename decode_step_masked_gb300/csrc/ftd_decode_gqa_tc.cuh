@@ -47,13 +47,18 @@ constexpr int NS = 3;     // K/V stages
 constexpr int KB = 16384; // one 64-column box of 128 rows (bytes)
 constexpr int STAGE = 4 * KB;  // K (2 boxes) + V (2 boxes)
 
-// The softmax is the per-tile critical path.  With 8 or more query columns two
-// groups of four warps split the columns (each thread handles half of them),
-// so a CTA runs 384 threads: warps 0-3 for copies and MMA, warps 4-11 softmax.
-constexpr int softmax_groups(int G) { return G >= 8 ? 2 : 1; }
+// The softmax is the per-tile critical path.  Groups of four warps split the
+// query columns so that each thread handles at most four: two groups for 8
+// columns, four for 16.  Warps 0-3 copy and issue MMAs, warps 4.. run the softmax.
+constexpr int softmax_groups(int G) { return G >= 16 ? 4 : (G >= 8 ? 2 : 1); }
 
 // Weight of a segment boundary in the static split (in 128-row tiles; see WeightedSplit).
 constexpr int kAlpha = 1;
+
+// Margin (log2 units) by which a score may pass a column's running reference
+// before the softmax moves the reference: weights then stay below 2^8, well
+// inside the range of the hi / lo operand pair and of the fp32 accumulators.
+constexpr float kRescaleLog2 = 8.f;
 constexpr int threads_for(int G) { return 128 + 128 * softmax_groups(G); }
 
 template <int G>
@@ -236,6 +241,107 @@ __device__ __forceinline__ float from_ct<__half>(__half x) { return __half2float
 
 }  // namespace tc
 
+// ------------------------------------------------- tile space in passes
+// The tensor-core kernel can order its tile space as np passes of spp segments per
+// slot: a pass runs over the slots b, then the segments, then the tiles.  With one
+// pass per block of query rows of a kv head (spp = Hkv), the passes are alike:
+// with W workers and np dividing W, worker w and worker w + W / np stream the same
+// K/V tiles at the same time and the later passes find them in L2.  P and VP hold
+// the prefixes of one pass; Cursor::seg = s * np + h for segment s of pass h, which
+// is the kernel's kvh * nhb + hb in both orders.
+__device__ __forceinline__ Cursor locate_pass(int t, const int* P, int B, int spp, int np) {
+    const int h = np > 1 ? t / P[B] : 0;  // called only for t < np * P[B]
+    t -= h * P[B];
+    int lo = 0, hi = B - 1;  // largest b with P[b] <= t; then P[b] <= t < P[b + 1]
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (P[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    Cursor cu;
+    cu.b = lo;
+    cu.nt = (P[lo + 1] - P[lo]) / spp;
+    const int rem = t - P[lo];
+    const int sg = rem / cu.nt;
+    cu.seg = sg * np + h;
+    cu.tile = rem - sg * cu.nt;
+    return cu;
+}
+
+// next tile; called only while one is left
+__device__ __forceinline__ void advance_pass(Cursor& cu, const int* P, int B, int spp, int np) {
+    if (++cu.tile < cu.nt) return;
+    cu.tile = 0;
+    cu.seg += np;
+    if (cu.seg < spp * np) return;
+    cu.seg -= spp * np;  // segment 0 of the same pass ...
+    do {
+        if (++cu.b == B) {  // ... or of the next pass
+            cu.b = 0;
+            ++cu.seg;
+        }
+    } while (P[cu.b + 1] == P[cu.b]);
+    cu.nt = (P[cu.b + 1] - P[cu.b]) / spp;
+}
+
+// Ordinal of segment s of slot b in pass h, in tile order.  A piece (segment
+// ordinal o, worker w) keeps its partial in slot o + w: along the tile order each
+// step to the next piece raises o or w or both, so no two pieces share a slot.
+__device__ __forceinline__ int seg_ordinal(int B, int spp, int b, int s, int h) {
+    return (h * B + b) * spp + s;
+}
+
+// Static split of the tile space in passes over W workers, weighted as in
+// WeightedSplit: tile i of segment s of slot b in pass h sits at weighted position
+// h V1 + VP[b] + s (nt + ALPHA) + i, V1 = VP[B] the weighted length of a pass, and
+// worker w takes the tiles whose position lies in [ceil(w V / W), ceil((w+1) V / W)),
+// V = np V1.
+template <int ALPHA>
+struct PassSplit {
+    const int* P;
+    const int* VP;
+    int B, spp, np, W;
+
+    __device__ long long V() const { return static_cast<long long>(np) * VP[B]; }
+
+    // first tile of worker w (the whole space for w >= W)
+    __device__ int begin(long long w) const {
+        const int V1 = VP[B];
+        if (w <= 0 || V1 == 0) return 0;
+        if (w >= W) return np * P[B];
+        const long long vt = (w * V() + W - 1) / W;
+        const int h = np > 1 ? static_cast<int>(vt / V1) : 0;  // np when vt = V: the end of the space
+        const long long v1 = vt - static_cast<long long>(h) * V1;
+        int lo = 0, hi = B - 1;  // largest b with VP[b] <= v1
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (VP[mid] <= v1) lo = mid;
+            else hi = mid - 1;
+        }
+        if (VP[lo + 1] <= v1) return h * P[B] + P[lo + 1];
+        const int nt = (P[lo + 1] - P[lo]) / spp;
+        const long long o = v1 - VP[lo];
+        const long long sg = o / (nt + ALPHA);
+        const long long r = o - sg * (nt + ALPHA);
+        return h * P[B] + P[lo] + static_cast<int>(sg * nt + (r < nt ? r : nt));
+    }
+
+    // worker holding tile i of segment s of slot b in pass h (nt tiles)
+    __device__ int worker_at(int b, int s, int h, int nt, int i) const {
+        const long long v = static_cast<long long>(h) * VP[B] + VP[b] + static_cast<long long>(s) * (nt + ALPHA) + i;
+        const long long vv = V();
+        if (vv * W < (1ll << 32))  // the product fits 32 bits: a cheaper division
+            return static_cast<int>(static_cast<uint32_t>(v * W) / static_cast<uint32_t>(vv));
+        return static_cast<int>(v * W / vv);
+    }
+
+    // whether worker w, between the holders wf and wl of a segment's first and last
+    // tiles, holds tiles of it: always when V >= W (every weighted range is non-empty)
+    __device__ bool has_piece(int w, int wf, int wl) const {
+        return V() >= W || w == wf || w == wl || begin(w) < begin(w + 1);
+    }
+};
+
 // Barrier slots in the misc area.
 enum : int { kBarFull = 0, kBarEmpty = 3, kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarQReady = 12,
              kNumBars = 13 };
@@ -272,7 +378,6 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
     int* VP = LY::HAVE_VP ? Ls + kMaxBatch : P;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int segs = p.Hkv * p.nhb;
     auto bar = [&](int i) { return smem_addr(&bars[i]); };
 
     if (tid == 0) {
@@ -286,7 +391,15 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
     }
     grid_dep_wait();    // inputs, caches and lengths may come from the previous launch
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
-    if (warp == 0) build_prefix(p, TM, segs, LY::ALPHA, P, VP, Ls, lane);
+    // Single-token steps with blocks of 16 query rows (a kv head shared by 32 or more
+    // query heads) run the head blocks of a kv head as passes (np = nhb).  Elsewhere
+    // they stay side by side in one pass: with several new tokens per step that keeps
+    // the kernel's register budget, and blocks of 8 rows rarely come more than one
+    // to a kv head.
+    constexpr bool kPasses = !MQ && G >= 16;
+    const int np = kPasses ? p.nhb : 1;
+    const int spp = kPasses ? p.Hkv : p.Hkv * p.nhb;
+    if (warp == 0) build_prefix(p, TM, spp, LY::ALPHA, P, VP, Ls, lane);
     fence_mbar_init();
     tc::tc_fence_before();
     __syncthreads();
@@ -301,7 +414,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
 
     const long long W = gridDim.x;
     const int wid = blockIdx.x;
-    const WeightedSplit<LY::ALPHA> split{P, VP, p.B, segs, static_cast<int>(W)};
+    const PassSplit<LY::ALPHA> split{P, VP, p.B, spp, np, static_cast<int>(W)};
     const int t_begin = split.begin(wid);
     const int n_my = split.begin(wid + 1) - t_begin;
 
@@ -309,7 +422,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
         if (warp == 0) {
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
-                Cursor cu = locate(t_begin, P, p.B, segs);
+                Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
                 PageCursor pages;
                 const uint64_t l2pol = l2_stream_policy();
                 int k = 0;
@@ -331,7 +444,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                     tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
                     tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
                     tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
-                    if (k + 1 < n_my) advance(cu, P, segs);
+                    if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
                 }
                 if (k < n_my) {
                     // aborted: let the copies already issued land before the block exits
@@ -344,22 +457,30 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
             // All 32 lanes walk every stage phase in order (a waiter that skipped
             // phases could be fooled by the parity of an older one); the lanes
             // patch the last tile of a segment together, lane 0 issues the MMAs.
-            Cursor cu = locate(t_begin, P, p.B, segs);
+            Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
             const uint32_t id_s = tc::instr_desc(BF, TM, N, false);
             const uint32_t id_o = tc::instr_desc(BF, D, N, true);
             int qcount = 0;
             bool ok = true;
+            // Operand descriptors of stage 0 and of the first Q / P buffers.  An offset
+            // of x bytes is x / 16 added to the 14-bit start-address field (shared
+            // addresses stay below 256 KB, so the field never carries), which keeps
+            // the issuing thread's chain per MMA to an add and the MMA itself.
+            const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(stages), 16, 1024);
+            const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(stages) + 2 * KB, tc::kVLbo, tc::kVSbo);
+            const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(Qs), 16, 1024);
+            const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(Ps), 16, 1024);
             auto issue_pv = [&](int kk) -> bool {
                 const bool w = tc::wait_or_abort(bar(kBarPFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
                 if (__any_sync(FULL, !w)) return false;
                 if (lane == 0) {
                     tc::tc_fence_after();
-                    const uint32_t vbase = smem_addr(stages + (kk % NS) * tc::STAGE + 2 * KB);
-                    const uint32_t pbase = smem_addr(Ps + (kk & 1) * PSZ);
+                    const uint64_t va = dv0 + static_cast<uint32_t>((kk % NS) * (tc::STAGE >> 4));
+                    const uint64_t pa = dp0 + static_cast<uint32_t>((kk & 1) * (PSZ >> 4));
 #pragma unroll
                     for (int ks = 0; ks < TM / 16; ++ks) {
-                        const uint64_t a = tc::smem_desc_sw128(vbase + ks * 2048, tc::kVLbo, tc::kVSbo);
-                        const uint64_t bd = tc::smem_desc_sw128(pbase + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+                        const uint64_t a = va + (ks * 2048 >> 4);
+                        const uint64_t bd = pa + (((ks >> 2) * (N * 128) + (ks & 3) * 32) >> 4);
                         tc::mma_f16(tmem + 2 * N + (kk & 1) * N, a, bd, id_o, ks > 0);
                     }
                     tc::mma_commit(bar(kBarOFull + (kk & 1)));
@@ -447,19 +568,18 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 }
                 if (lane == 0) {
                     tc::tc_fence_after();
-                    const uint32_t kbase = smem_addr(stages + s * tc::STAGE);
-                    const uint32_t qbase = smem_addr(Qs);
+                    const uint64_t ka = dk0 + static_cast<uint32_t>(s * (tc::STAGE >> 4));
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t a = tc::smem_desc_sw128(kbase + (ks >> 2) * KB + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(qbase + (ks >> 2) * (N * 128) + (ks & 3) * 32, 16, 1024);
+                        const uint64_t a = ka + (((ks >> 2) * KB + (ks & 3) * 32) >> 4);
+                        const uint64_t bd = dq0 + (((ks >> 2) * (N * 128) + (ks & 3) * 32) >> 4);
                         tc::mma_f16(tmem + (k & 1) * N, a, bd, id_s, ks > 0);
                     }
                     tc::mma_commit(bar(kBarSFull + (k & 1)));
                 }
                 __syncwarp();
                 if (k > 0 && !new_piece && !issue_pv(k - 1)) { ok = false; break; }
-                if (k + 1 < n_my) advance(cu, P, segs);
+                if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
             }
             if (ok) issue_pv(n_my - 1);
         } else if (warp >= 4) {
@@ -473,7 +593,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
             const bool leader = ch == 0 && r == 0;  // the thread that arrives on the count-1 barriers
             const int QB = p.qblk;  // real query rows of a block; columns QB .. G-1 carry a zero query
             const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
-            Cursor cu = locate(t_begin, P, p.B, segs);
+            Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
             float m[GH], l[GH], o[GH], al[GH];
             int tk[GH];  // token of each owned query column (0 unless several new tokens per step)
             // output row of query row qi of a kv head
@@ -499,6 +619,50 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 for (int j = 0; j < GH; ++j) o[j] = al[j] * o[j] + (oh[j] + ol[j]);
                 return true;
             };
+            // The scaled query of the owned columns of piece c (dimension r), with the
+            // token of each column; columns QB .. G-1 of a padded block get zero.
+            float qn[GH];
+            int tkn[GH];
+            auto load_q = [&](const Cursor& c) {
+                const int kvh = c.seg / p.nhb, hb = c.seg % p.nhb;
+#pragma unroll
+                for (int jj = 0; jj < GH; ++jj) {
+                    const int j = c0 + jj;
+                    // q row of column j; several tokens per step interleave tokens and heads
+                    size_t qrow;
+                    int h;
+                    if constexpr (MQ) {
+                        tkn[jj] = j < QB ? q_token(p, hb * QB + j) : 0;
+                        h = kvh * p.group + (hb * QB + j - tkn[jj] * p.group);
+                        qrow = (static_cast<size_t>(c.b) * p.nq + tkn[jj]) * p.Hq + h;
+                    } else {
+                        tkn[jj] = 0;
+                        h = kvh * p.group + hb * QB + j;
+                        qrow = static_cast<size_t>(c.b) * p.Hq + h;
+                    }
+                    float x = 0.f;
+                    if (j < QB) {
+                        x = ld_qkv(p.q, p.qkv_dtype, qrow * D + r);
+                        if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + r);
+                        x *= p.qscale;
+                    }
+                    qn[jj] = x;
+                }
+            };
+            // Q operand (hi / lo) into shared memory, published to the MMA issuer
+            auto store_q = [&]() {
+#pragma unroll
+                for (int jj = 0; jj < GH; ++jj) {
+                    const CT hi = tc::to_ct<CT>(qn[jj]);
+                    const CT lo = tc::to_ct<CT>(qn[jj] - tc::from_ct<CT>(hi));
+                    *reinterpret_cast<CT*>(Qs + tc::sw128_offset(c0 + jj, r, N)) = hi;
+                    *reinterpret_cast<CT*>(Qs + tc::sw128_offset(G + c0 + jj, r, N)) = lo;
+                }
+                fence_proxy_async_smem();
+                tc::named_bar_sync(1, SMX);
+                if (leader) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarQReady)) : "memory");
+            };
+            bool q_staged = false;  // the next piece's Q is already in shared memory
             for (int k = 0; k < n_my; ++k) {
                 const bool new_piece = (k == 0) || (cu.tile == 0);
                 const bool last = cu.tile == cu.nt - 1;
@@ -508,38 +672,28 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
                 if (new_piece) {
                     piece_first = cu.tile;
+                    if (!q_staged) {
+                        load_q(cu);
+                        store_q();
+                    }
+                    q_staged = false;
 #pragma unroll
                     for (int jj = 0; jj < GH; ++jj) {
-                        const int j = c0 + jj;
-                        // q row of column j; several tokens per step interleave tokens and heads
-                        size_t qrow;
-                        int h;
-                        if constexpr (MQ) {
-                            tk[jj] = j < QB ? q_token(p, hb * QB + j) : 0;
-                            h = kvh * p.group + (hb * QB + j - tk[jj] * p.group);
-                            qrow = (static_cast<size_t>(cu.b) * p.nq + tk[jj]) * p.Hq + h;
-                        } else {
-                            tk[jj] = 0;
-                            h = kvh * p.group + hb * QB + j;
-                            qrow = static_cast<size_t>(cu.b) * p.Hq + h;
-                        }
-                        float x = 0.f;
-                        if (j < QB) {
-                            x = ld_qkv(p.q, p.qkv_dtype, qrow * D + r);
-                            if (p.bias) x += ld_qkv(p.bias, p.qkv_dtype, static_cast<size_t>(h) * D + r);
-                            x *= p.qscale;
-                        }
-                        const CT hi = tc::to_ct<CT>(x);
-                        const CT lo = tc::to_ct<CT>(x - tc::from_ct<CT>(hi));
-                        *reinterpret_cast<CT*>(Qs + tc::sw128_offset(j, r, N)) = hi;
-                        *reinterpret_cast<CT*>(Qs + tc::sw128_offset(G + j, r, N)) = lo;
+                        tk[jj] = tkn[jj];
                         m[jj] = -INFINITY;
                         l[jj] = 0.f;
                         o[jj] = 0.f;
                     }
-                    fence_proxy_async_smem();
-                    tc::named_bar_sync(1, SMX);
-                    if (leader) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarQReady)) : "memory");
+                }
+                // On a piece's last tile the next piece's query is loaded now and staged
+                // as soon as this tile's scores are consumed (the issuer waits for it
+                // before the next score MMA, so the single Q buffer is free), ahead of the
+                // output or merge of this piece.
+                const bool stage_next = last && k + 1 < n_my;
+                if (stage_next) {
+                    Cursor nx = cu;
+                    advance_pass(nx, P, p.B, spp, np);
+                    load_q(nx);
                 }
                 // ---- scores of this tile ----
                 const bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag);
@@ -553,44 +707,78 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 const int hi0 = L + 1 - t0, lo0 = p.window > 0 ? L + 1 - p.window - t0 : -(1 << 30);
                 const bool valid0 = r >= lo0 && r < hi0;  // the rows every column sees (single token)
                 float sc[GH];
+                bool need = false;  // a visible score above the column's reference by more than the margin
 #pragma unroll
                 for (int jj = 0; jj < GH; ++jj) {
                     const bool valid = MQ ? (r >= lo0 + tk[jj] && r < hi0 + tk[jj]) : valid0;
                     sc[jj] = valid ? sh[jj] + sl_[jj] : -INFINITY;
-                    float v = sc[jj];
-#pragma unroll
-                    for (int mm = 16; mm >= 1; mm >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, mm));
-                    if (lane == 0) red_max[q4 * G + c0 + jj] = v;
+                    need |= sc[jj] > m[jj] + tc::kRescaleLog2;  // always when m = -inf and the score is visible
                 }
-                tc::named_bar_sync(1, SMX);
                 float alpha[GH];
                 unsigned char* pb = Ps + (k & 1) * PSZ;
-#pragma unroll
-                for (int jj = 0; jj < GH; ++jj) {
-                    const int j = c0 + jj;
-                    const float tmax = fmaxf(fmaxf(red_max[j], red_max[G + j]), fmaxf(red_max[2 * G + j], red_max[3 * G + j]));
-                    const float mnew = fmaxf(m[jj], tmax);
-                    float pj;
-                    if constexpr (MQ) {
-                        // a column with no visible row yet keeps m = -inf; 0 stands in as the reference
-                        const float mref = mnew == -INFINITY ? 0.f : mnew;
-                        alpha[jj] = exp2f(m[jj] - mref);
-                        pj = exp2f(sc[jj] - mref);
-                    } else {
-                        alpha[jj] = exp2f(m[jj] - mnew);
-                        pj = valid0 ? exp2f(sc[jj] - mnew) : 0.f;
-                    }
-                    l[jj] = l[jj] * alpha[jj] + pj;
-                    m[jj] = mnew;
+                auto put_p = [&](int jj, float pj) {
                     const CT hi = tc::to_ct<CT>(pj);
                     const CT lo = tc::to_ct<CT>(pj - tc::from_ct<CT>(hi));
-                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(j, r, N)) = hi;
-                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(G + j, r, N)) = lo;
+                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(c0 + jj, r, N)) = hi;
+                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(G + c0 + jj, r, N)) = lo;
+                };
+                // Optimistic pass: the weights are taken against the running reference m,
+                // which is valid (any reference is) as long as they stay below 2^margin.
+                // One barrier then both publishes P and takes the vote; only when some
+                // thread saw a larger score do the columns move to the tile's maximum.
+                float pq[GH];
+                if (!need) {
+#pragma unroll
+                    for (int jj = 0; jj < GH; ++jj) {
+                        // a column with no visible row yet keeps m = -inf; 0 stands in as the reference
+                        pq[jj] = exp2f(sc[jj] - (m[jj] == -INFINITY ? 0.f : m[jj]));
+                        put_p(jj, pq[jj]);
+                    }
                 }
                 fence_proxy_async_smem();
                 tc::tc_fence_before();
-                tc::named_bar_sync(1, SMX);
+                if (!tc::bar_any(1, SMX, need)) {
+#pragma unroll
+                    for (int jj = 0; jj < GH; ++jj) {
+                        alpha[jj] = 1.f;
+                        l[jj] += pq[jj];
+                    }
+                } else {
+#pragma unroll
+                    for (int jj = 0; jj < GH; ++jj) {
+                        float v = sc[jj];
+#pragma unroll
+                        for (int mm = 16; mm >= 1; mm >>= 1) v = fmaxf(v, __shfl_xor_sync(FULL, v, mm));
+                        if (lane == 0) red_max[q4 * G + c0 + jj] = v;
+                    }
+                    tc::named_bar_sync(1, SMX);
+#pragma unroll
+                    for (int jj = 0; jj < GH; ++jj) {
+                        const int j = c0 + jj;
+                        const float tmax = fmaxf(fmaxf(red_max[j], red_max[G + j]), fmaxf(red_max[2 * G + j], red_max[3 * G + j]));
+                        const float mnew = fmaxf(m[jj], tmax);
+                        float pj;
+                        if constexpr (MQ) {
+                            const float mref = mnew == -INFINITY ? 0.f : mnew;
+                            alpha[jj] = exp2f(m[jj] - mref);
+                            pj = exp2f(sc[jj] - mref);
+                        } else {
+                            alpha[jj] = exp2f(m[jj] - mnew);
+                            pj = valid0 ? exp2f(sc[jj] - mnew) : 0.f;
+                        }
+                        l[jj] = l[jj] * alpha[jj] + pj;
+                        m[jj] = mnew;
+                        put_p(jj, pj);
+                    }
+                    fence_proxy_async_smem();
+                    tc::tc_fence_before();
+                    tc::named_bar_sync(1, SMX);
+                }
                 if (leader) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarPFull + (k & 1))) : "memory");
+                if (stage_next) {
+                    store_q();
+                    q_staged = true;
+                }
                 if (pending && !acc_o(k - 1)) break;
 #pragma unroll
                 for (int jj = 0; jj < GH; ++jj) al[jj] = alpha[jj];
@@ -614,7 +802,9 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         const int j = c0 + jj;
                         lt[jj] = red_sum[j] + red_sum[G + j] + red_sum[2 * G + j] + red_sum[3 * G + j];
                     }
-                    const int segg = cu.b * segs + cu.seg;
+                    // segment s of pass h in the tile order: (kvh, hb) in passes, (seg, 0) in one pass
+                    const int ss = kPasses ? kvh : cu.seg, sh_ = kPasses ? hb : 0;
+                    const int segg = seg_ordinal(p.B, spp, cu.b, ss, sh_);
                     if (piece_first == 0 && last) {
 #pragma unroll
                         for (int jj = 0; jj < GH; ++jj)
@@ -642,8 +832,8 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         // and the leader's acquire before every thread's merge reads
                         tc::named_bar_sync(1, SMX);
                         if (bcast[0]) {
-                            const int wf = split.worker_at(cu.b, cu.seg, cu.nt, 0);
-                            const int wl = split.worker_at(cu.b, cu.seg, cu.nt, cu.nt - 1);
+                            const int wf = split.worker_at(cu.b, ss, sh_, cu.nt, 0);
+                            const int wl = split.worker_at(cu.b, ss, sh_, cu.nt, cu.nt - 1);
                             // one pass over the pieces with a running log-sum-exp; all loads
                             // of a piece are independent, so each piece costs one L2 round trip
                             float Mx[GH], Ls_[GH], Ac[GH];
@@ -683,7 +873,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         tc::named_bar_sync(1, SMX);
                     }
                 }
-                if (k + 1 < n_my) advance(cu, P, segs);
+                if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
             }
         }
     }

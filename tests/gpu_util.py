@@ -5,7 +5,7 @@ from __future__ import annotations
 import numpy as np
 
 import decode_step_masked_gb300 as ftd
-from synthetic import gen_cache_slot, gen_scales_slot
+from synthetic import gen_cache_slot, gen_scales_slot, to_storage
 
 # Parity bars: fp32/fp16/bf16 caches with fp32 accumulation, and INT8 caches
 # against the oracle run on the dequantised values.
@@ -177,3 +177,33 @@ def valid_rows(w, arr, lens, q_len=1):
         if 0 <= L <= w.Lmax - q_len:
             out[b, :, :L + q_len] = arr[b, :, :L + q_len]
     return out
+
+
+def _from_storage(a, dt):
+    a = np.asarray(a)
+    if dt == "bf16":
+        return (a.astype(np.uint32) << 16).view(np.float32)
+    return a.astype(np.float32)
+
+
+def rising_scores(w, inp, rise_log2=40.0, seed=5):
+    """Inputs whose scores climb by about ``rise_log2`` (base-2 units) from the first
+    cached position to the last: each kv head gets a unit direction u, its queries
+    point along u and its cached keys carry a component growing linearly along u.
+    The running maximum of every query row then moves again and again inside a
+    context.  fp16 / bf16 caches only; positions past the lengths keep their fill."""
+    rng = np.random.default_rng(seed)
+    D, g = w.D, w.Hq // w.Hkv
+    u = rng.standard_normal((w.Hkv, D))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    A = 12.0  # key component at the end of the cache
+    sq = rise_log2 * np.sqrt(D) / (A * np.log2(np.e))
+    q = _from_storage(inp["q"], w.qkv_dtype).astype(np.float64)
+    lead = q.shape[:-2]  # [B] or [B, T]
+    heads = np.repeat(u, g, axis=0)  # [Hq, D]
+    q = sq * np.broadcast_to(heads, lead + heads.shape) + 0.1 * q
+    k = _from_storage(inp["k_cache"], w.cache_dtype).astype(np.float64)  # [B, Hkv, Lmax, D]
+    ramp = A * np.arange(w.Lmax, dtype=np.float64) / w.Lmax
+    k = 0.3 * k + ramp[None, None, :, None] * u[None, :, None, :]
+    return dict(inp, q=to_storage(q.astype(np.float32), w.qkv_dtype),
+                k_cache=to_storage(k.astype(np.float32), w.cache_dtype))

@@ -15,7 +15,7 @@ import pytest
 import decode_step_masked_gb300 as ftd
 import oracle
 from synthetic import Workload, gen_all
-from tests.gpu_util import (TOL_MAXABS, assert_close, assert_same_bytes, dev, from_pages, make_step,
+from tests.gpu_util import (TOL_MAXABS, assert_close, assert_same_bytes, dev, from_pages, make_step, rising_scores,
                             page_layout, run_step, to_pages, valid_rows)
 
 pytestmark = pytest.mark.gpu
@@ -64,6 +64,16 @@ def check(w, inp, cc, window=0, out_dtype="f32", what=""):
     if w.cache_dtype == "i8":
         assert_same_bytes(got["scales"], ref["scales"], f"{what} INT8 scales after append")
     return got, ref
+
+
+@pytest.mark.parametrize("name", ["gqa_bf16_T2_tc", "gqa_bf16_T3_tc", "mqa_f16_T5_tc", "mqa_f16_T5_cc"])
+def test_multi_token_rising_scores(name):
+    """Scores climbing along the context: the per-column running maxima move inside a
+    piece while each new token's column still has its own causal limit."""
+    *args, cc = CASES[name]
+    w, inp = case(*args)
+    got, ref = check(w, rising_scores(w, inp), cc, what=f"{name} rising")
+    assert_close(got["out"], ref["out"], what=f"{name} rising")
 
 
 @pytest.mark.parametrize("name", list(CASES))

@@ -11,7 +11,7 @@ import decode_step_masked_gb300 as ftd
 import oracle
 from synthetic import WORKLOADS, Workload, gen_all, gen_qkv, gen_seq_lens
 from tests.gpu_util import (assert_close, assert_same_bytes, dev, device_view, fill_device_cache,
-                            fill_device_scales, run_step)
+                            fill_device_scales, rising_scores, run_step)
 
 pytestmark = pytest.mark.gpu
 
@@ -144,6 +144,20 @@ def test_large_scores_stay_finite():
     w, inp = small("f32", "f32", B=2, Hq=4, Hkv=4, D=64, Lmax=512, lens=[400, 77], bias=None)
     inp = dict(inp, q=(inp["q"] * np.float32(40.0)).astype(np.float32))
     check_step(w, inp, what="large scores")
+
+
+@pytest.mark.parametrize("cache,Hq,Hkv,cc", [
+    ("bf16", 16, 2, False),  # tensor cores, 8 query columns
+    ("f16", 32, 2, False),   # tensor cores, 16 query columns
+    ("bf16", 16, 2, True),   # CUDA cores, grouped
+    ("f16", 4, 4, False),    # CUDA cores, one query row per kv head
+])
+def test_scores_rising_along_the_context(cache, Hq, Hkv, cc):
+    """Scores that climb by ~40 (base 2) along each context move every row's running
+    maximum many times, tiles after the first included, so the softmax's rescaling
+    of earlier weights and partial outputs is exercised, not just its first tile."""
+    w, inp = small(cache, cache, B=4, Hq=Hq, Hkv=Hkv, D=128, Lmax=2048, lens=[1500, 700, 130, 2047])
+    check_step(w, rising_scores(w, inp), what=f"rising scores {cache} {Hq}/{Hkv}", force_cuda_core=cc)
 
 
 def test_consecutive_steps_continue_the_sequence():
