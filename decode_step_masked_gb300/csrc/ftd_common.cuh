@@ -204,6 +204,13 @@ __device__ __forceinline__ uint64_t l2_stream_policy() {
 }
 
 // bulk_g2s with an L2 cache policy (l2_stream_policy) for the streamed cache rows.
+// L2 prefetch of `bytes` contiguous global bytes (16-byte aligned start, size a
+// multiple of 16).  A hint: L2 is the coherence point, so lines another kernel is
+// still writing are never served stale.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
                                               uint64_t pol) {
     asm volatile(

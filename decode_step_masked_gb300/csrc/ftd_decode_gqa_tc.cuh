@@ -389,8 +389,6 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                      "r"(LY::TMEM_COLS));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
-    grid_dep_wait();    // inputs, caches and lengths may come from the previous launch
-    grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
     // Single-token steps with blocks of 16 query rows (a kv head shared by 32 or more
     // query heads) run the head blocks of a kv head as passes (np = nhb).  Elsewhere
     // they stay side by side in one pass: with several new tokens per step that keeps
@@ -406,17 +404,37 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-        if (P[b + 1] == P[b]) {
-            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
-        }
-    }
-
+    // The split depends only on the lengths, which no launch of this library writes,
+    // so it runs before the wait on the previous launch, and a block that starts
+    // while the previous step drains warms L2 with its first tiles (contiguous
+    // caches).  Reads of the caches and writes of shared outputs come after the wait.
     const long long W = gridDim.x;
     const int wid = blockIdx.x;
     const PassSplit<LY::ALPHA> split{P, VP, p.B, spp, np, static_cast<int>(W)};
     const int t_begin = split.begin(wid);
     const int n_my = split.begin(wid + 1) - t_begin;
+    if (n_my > 0 && tid == 0 && !p.block_table) {
+        Cursor c = locate_pass(t_begin, P, p.B, spp, np);
+        for (int k = 0; k < min(NS, n_my); ++k) {
+            const int L = Ls[c.b];
+            const int t0 = (window_start(L, p.window) / TM + c.tile) * TM;
+            const int n_cache = min(TM, max(0, L - t0));
+            if (n_cache > 0) {
+                const size_t rb = static_cast<size_t>(cache_row(p, c.b, c.seg / p.nhb, t0, 0));
+                bulk_prefetch_l2(p.k_cache + rb * D * 2, static_cast<uint32_t>(n_cache) * D * 2);
+                bulk_prefetch_l2(p.v_cache + rb * D * 2, static_cast<uint32_t>(n_cache) * D * 2);
+            }
+            if (k + 1 < min(NS, n_my)) advance_pass(c, P, p.B, spp, np);
+        }
+    }
+    grid_dep_wait();    // inputs, caches and outputs may be in use by the previous launch
+    grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
+
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        if (P[b + 1] == P[b]) {
+            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
+        }
+    }
 
     if (n_my > 0) {
         if (warp == 0) {

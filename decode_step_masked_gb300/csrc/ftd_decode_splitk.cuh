@@ -249,7 +249,7 @@ __device__ __forceinline__ void build_prefix(const DecodeParams& p, int T, int s
     bool ovf = false;
     for (int base = 0; base < p.B; base += 32) {
         const int b = base + lane;
-        const int L = b < p.B ? __ldg(p.seq_lens + b) : -1;
+        const int L = b < p.B ? __ldcg(p.seq_lens + b) : -1;  // L2: may run before the wait on the previous launch
         const bool valid = L >= 0 && L <= p.Lmax - p.nq;
         ovf |= (b < p.B) && (L > p.Lmax - p.nq);
         int v = valid ? ((L + p.nq - 1) / T + 1 - window_start(L, p.window) / T) * segs : 0;
@@ -357,11 +357,37 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
 #pragma unroll
         for (int s = 0; s < SPW; ++s) mbar_init(smem_addr(&bars[s]), 1);
     }
-    grid_dep_wait();    // inputs, caches and lengths may come from the previous launch
-    grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
+    // The split depends only on the lengths, which no launch of this library
+    // writes, so it is computed before waiting on the previous launch: a block
+    // that starts while the previous step drains then warms L2 with its first
+    // tiles (contiguous caches) instead of idling.  Everything that reads the
+    // caches' contents or writes memory the previous launch uses comes after
+    // the wait.
     if (warp == 0) build_prefix(p, T, segs, TL::ALPHA, P, VP, Ls, lane);
     fence_mbar_init();
     __syncthreads();
+
+    const long long W = static_cast<long long>(gridDim.x) * TL::WARPS;
+    const int wid = blockIdx.x * TL::WARPS + warp;
+    const WeightedSplit<TL::ALPHA> split{P, VP, p.B, segs, static_cast<int>(W)};
+    const int t_begin = split.begin(wid);
+    const int n_my = split.begin(wid + 1) - t_begin;
+    if (n_my > 0 && lane == 0 && !p.block_table) {
+        Cursor c = locate(t_begin, P, p.B, segs);
+        for (int k = 0; k < min(SPW, n_my); ++k) {
+            const int L = Ls[c.b];
+            const int t0 = (window_start(L, p.window) / T + c.tile) * T;
+            const int n_cache = min(T, max(0, L - t0));
+            if (n_cache > 0) {
+                const size_t rb = static_cast<size_t>(cache_row(p, c.b, c.seg / p.nhb, t0, 0));
+                bulk_prefetch_l2(p.k_cache + rb * ROW, static_cast<uint32_t>(n_cache) * ROW);
+                bulk_prefetch_l2(p.v_cache + rb * ROW, static_cast<uint32_t>(n_cache) * ROW);
+            }
+            if (k + 1 < min(SPW, n_my)) advance(c, P, segs);
+        }
+    }
+    grid_dep_wait();    // inputs, caches and outputs may be in use by the previous launch
+    grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
 
     // Slots without work (inactive or overflowing) get a zero output.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
@@ -369,12 +395,6 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
             zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
         }
     }
-
-    const long long W = static_cast<long long>(gridDim.x) * TL::WARPS;
-    const int wid = blockIdx.x * TL::WARPS + warp;
-    const WeightedSplit<TL::ALPHA> split{P, VP, p.B, segs, static_cast<int>(W)};
-    const int t_begin = split.begin(wid);
-    const int n_my = split.begin(wid + 1) - t_begin;
     if (n_my <= 0) return;
 
     // ---- bulk copies of one tile (lane 0 only) ----

@@ -156,6 +156,12 @@ ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** 
  * Launches one kernel; no host synchronisation and no allocation.  Two calls
  * on the same context must not overlap in time (they share the workspace):
  * issue them on one stream, or order their streams with events.
+ * The kernel is launched with programmatic dependent launch: it may start
+ * while the preceding kernel on the stream finishes, if that kernel allows
+ * it (this library's decode kernels do, right after their own start).  Before
+ * it waits for that kernel it reads only seq_lens (and prefetches cache lines
+ * into L2, which is always safe), so a preceding kernel that allows an early
+ * start must not write seq_lens after allowing it.
  * A paged context (page_size > 0) is refused with INVALID_ARG.
  */
 ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
