@@ -46,7 +46,7 @@ KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
 OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("13b", dict(page_size=256)),
                 ("70b", dict(out_dtype="bf16")), ("70b", dict(window=1024)), ("70b", dict(page_size=256)),
                 ("int8", dict(page_size=256)), ("7b", dict(q_len=4)), ("7b", dict(q_len=8)),
-                ("70b", dict(q_len=4))]
+                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)), ("mqa", {})]
 
 
 def kernel_name(w, q_len=1) -> str:
@@ -518,7 +518,7 @@ def main():
         opts = {}
         for name, kw in OPTION_CASES:
             w2, _, by2, pools2, _, r2, us2 = measure_config(name, 1000, 50, 99, device, stream, **kw)
-            key = name + ":" + ",".join(f"{k}={v}" for k, v in kw.items())
+            key = name + (":" + ",".join(f"{k}={v}" for k, v in kw.items()) if kw else "")
             opts[key] = dict(us=us2, gbs=by2["kv"] / us2 / 1e3, frac=by2["kv"] / us2 / 1e3 / peaks["hbm_gbs"],
                              kv_mb=by2["kv"] / 1e6, kernel=kernel_name(w2, kw.get("q_len", 1)))
             del pools2

@@ -452,15 +452,13 @@ ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, 
 
 // Copies the step's inputs from GPU-addressable (pinned) host memory into the
 // context's staging buffers in one launch, in place of one copy call per
-// buffer: 16-byte words for q, k_new, v_new and the bias, 4-byte words for the
-// lengths.  On Grace systems the reads cross NVLink-C2C.
+// buffer: 16-byte words for q, k_new, v_new and the bias.  On Grace systems the
+// reads cross NVLink-C2C.  The lengths are not copied: the decode kernel reads
+// them in place, before it waits for this grid (see ftd_decode_mha_host).
 struct GatherArgs {
     const uint4* src[4];
     uint4* dst[4];
     uint32_t n16[4];
-    const int32_t* lens_src;
-    int32_t* lens_dst;
-    uint32_t n_lens;
 };
 
 __global__ void __launch_bounds__(256) gather_step_inputs(GatherArgs a) {
@@ -472,7 +470,6 @@ __global__ void __launch_bounds__(256) gather_step_inputs(GatherArgs a) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
         for (uint32_t i = t; i < a.n16[k]; i += stride) a.dst[k][i] = a.src[k][i];
-    for (uint32_t i = t; i < a.n_lens; i += stride) a.lens_dst[i] = a.lens_src[i];
 }
 
 // Device address of host pointer p when the GPU can address it (pinned and mapped), else null.
@@ -525,14 +522,15 @@ ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, c
             ga.dst[i] = static_cast<uint4*>(dsts[i]);
             ga.n16[i] = static_cast<uint32_t>(bytes[i] / 16);
         }
-        ga.lens_src = static_cast<const int32_t*>(ctx->hd[4]);
-        ga.lens_dst = ctx->st_lens;
-        ga.n_lens = static_cast<uint32_t>(B);
         gather_step_inputs<<<ctx->grid, 256, 0, s>>>(ga);
         if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "input gather launch");
         g_launches.fetch_add(1);
+        // The decode kernel reads the lengths before it waits for the gather grid
+        // (which lets it start early), so it reads them from the caller's pinned
+        // buffer, which nothing on the device writes, not from a staging copy.
         ftd_status st = launch_decode(ctx, ctx->st_q, ctx->st_k, ctx->st_v, qkv_bias ? ctx->st_bias : nullptr,
-                                      k_cache, v_cache, nullptr, ctx->st_lens, scales, ctx->hd[5], s);
+                                      k_cache, v_cache, nullptr, static_cast<const int32_t*>(ctx->hd[4]), scales,
+                                      ctx->hd[5], s);
         if (st != FTD_OK) return st;
         e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");

@@ -81,6 +81,10 @@ WORKLOADS = {
         "70b", B=16, Hq=64, Hkv=8, D=128, Lmax=8192, qkv_dtype="bf16", cache_dtype="bf16",
         lens=("fixed", 8191), seed=3,
         description="70B-shaped GQA decode: B16 Hq64 Hkv8 D128, context 8192, bf16"),
+    "mqa": Workload(
+        "mqa", B=64, Hq=64, Hkv=1, D=128, Lmax=4096, qkv_dtype="bf16", cache_dtype="bf16",
+        lens=("fixed", 4095), seed=5,
+        description="MQA-shaped decode: B64, 64 query heads on one kv head, D128, context 4096, bf16"),
     "int8": Workload(
         "int8", B=64, Hq=32, Hkv=32, D=128, Lmax=2048, qkv_dtype="f16", cache_dtype="i8",
         lens=("ctx_uniform", 512, 2048), scale_range=(0.01, 0.05), seed=4,

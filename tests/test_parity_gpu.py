@@ -254,12 +254,43 @@ def test_host_entry_point_with_pinned_buffers():
     step.close()
 
 
+def test_host_entry_point_lengths_change_between_calls():
+    """The direct host path reads the lengths in place: calls that rewrite the pinned
+    lengths between them each see their own lengths (the decode kernel computes its
+    split before it waits for the input gather)."""
+    import torch
+    w, inp = small("bf16", "bf16", B=3, Hq=16, Hkv=2, D=128, Lmax=256, lens=[255, 255, 255])
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    kc, vc = dev(inp["k_cache"]), dev(inp["v_cache"])
+
+    def pinned(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).pin_memory()
+
+    hq, hk, hv, hb, hl = (pinned(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens"))
+    out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32).pin_memory()
+    s = torch.cuda.current_stream().cuda_stream
+    for lens in ([0, 130, 255], [200, 7, 129], [128, 255, 1], [0, 130, 255]):
+        hl.copy_(torch.tensor(lens, dtype=torch.int32))
+        ref = oracle.load().decode_step(w, dict(inp, seq_lens=np.array(lens, np.int32)))
+        kcur, vcur = kc.clone(), vc.clone()
+        ftd.check(ftd.ftd_decode_mha_host(step.ctx, hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), hb.data_ptr(),
+                                          kcur.data_ptr(), vcur.data_ptr(), hl.data_ptr(), 0, out.data_ptr(), s))
+        assert_close(out.numpy().astype(np.float64), ref["out"], what=f"host entry point, lengths {lens}")
+        assert_same_bytes(kcur.cpu().numpy().view(np.uint16), ref["k_cache"], f"K after append, lengths {lens}")
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+
+
 # ------------------------------------------------------------- full size
 SAMPLED = {"7b": [(0, 0), (3, 17), (7, 31)], "13b": [(0, 5), (11, 39), (31, 0), (17, 22)],
-           "70b": [(0, 0), (5, 37), (15, 63)], "int8": [(0, 1), (33, 30), (63, 31)]}
+           "70b": [(0, 0), (5, 37), (15, 63)], "int8": [(0, 1), (33, 30), (63, 31)],
+           "mqa": [(0, 0), (21, 17), (63, 63)]}
 
 
-@pytest.mark.parametrize("name", ["7b", "13b", "70b", "int8"])
+@pytest.mark.parametrize("name", ["7b", "13b", "70b", "int8", "mqa"])
 def test_full_size_workload_sampled(name):
     """Full-size workloads in the launch configuration the bench times; the oracle checks
     sampled (slot, head) outputs one slot at a time, and every appended row bit for bit."""
