@@ -450,28 +450,6 @@ ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, 
                          static_cast<cudaStream_t>(stream));
 }
 
-// Copies the step's inputs from GPU-addressable (pinned) host memory into the
-// context's staging buffers in one launch, in place of one copy call per
-// buffer: 16-byte words for q, k_new, v_new and the bias.  On Grace systems the
-// reads cross NVLink-C2C.  The lengths are not copied: the decode kernel reads
-// them in place, before it waits for this grid (see ftd_decode_mha_host).
-struct GatherArgs {
-    const uint4* src[4];
-    uint4* dst[4];
-    uint32_t n16[4];
-};
-
-__global__ void __launch_bounds__(256) gather_step_inputs(GatherArgs a) {
-    // the decode launch that follows may place its blocks now (they hold no shared
-    // memory of ours); they wait in griddepcontrol.wait until this grid has finished
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const uint32_t stride = gridDim.x * blockDim.x;
-    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        for (uint32_t i = t; i < a.n16[k]; i += stride) a.dst[k][i] = a.src[k][i];
-}
-
 // Device address of host pointer p when the GPU can address it (pinned and mapped), else null.
 static void* device_alias(const void* p) {
     if (!p) return nullptr;
@@ -495,8 +473,10 @@ ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, c
     const size_t B = ctx->cfg.max_batch;
     cudaError_t e;
 
-    // Pinned, GPU-addressable host buffers (looked up once per set of pointers): one
-    // gather launch brings the inputs in, and the kernel writes out straight to the host.
+    // Pinned, GPU-addressable host buffers (looked up once per set of pointers): the
+    // decode kernel reads the inputs in place (on Grace systems across NVLink-C2C;
+    // each q, k_new and v_new row is read by the few workers of its segment) and
+    // writes out straight to the host, so a step is one launch and no copy call.
     const void* hp[6] = {q, k_new, v_new, qkv_bias, seq_lens, out};
     bool same = true;
     for (int i = 0; i < 6; ++i) same = same && hp[i] == ctx->hp[i];
@@ -513,22 +493,7 @@ ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, c
         direct = direct && a != 0 && (a & (i == 4 ? 3u : 15u)) == 0;
     }
     if (direct) {
-        GatherArgs ga{};
-        const void* srcs[4] = {ctx->hd[0], ctx->hd[1], ctx->hd[2], ctx->hd[3]};
-        void* dsts[4] = {ctx->st_q, ctx->st_k, ctx->st_v, ctx->st_bias};
-        const size_t bytes[4] = {ctx->q_bytes, ctx->kv_new_bytes, ctx->kv_new_bytes, qkv_bias ? ctx->bias_bytes : 0};
-        for (int i = 0; i < 4; ++i) {
-            ga.src[i] = static_cast<const uint4*>(srcs[i]);
-            ga.dst[i] = static_cast<uint4*>(dsts[i]);
-            ga.n16[i] = static_cast<uint32_t>(bytes[i] / 16);
-        }
-        gather_step_inputs<<<ctx->grid, 256, 0, s>>>(ga);
-        if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "input gather launch");
-        g_launches.fetch_add(1);
-        // The decode kernel reads the lengths before it waits for the gather grid
-        // (which lets it start early), so it reads them from the caller's pinned
-        // buffer, which nothing on the device writes, not from a staging copy.
-        ftd_status st = launch_decode(ctx, ctx->st_q, ctx->st_k, ctx->st_v, qkv_bias ? ctx->st_bias : nullptr,
+        ftd_status st = launch_decode(ctx, ctx->hd[0], ctx->hd[1], ctx->hd[2], qkv_bias ? ctx->hd[3] : nullptr,
                                       k_cache, v_cache, nullptr, static_cast<const int32_t*>(ctx->hd[4]), scales,
                                       ctx->hd[5], s);
         if (st != FTD_OK) return st;

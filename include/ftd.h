@@ -199,13 +199,13 @@ ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, 
  * in host memory.  q, k_new, v_new, qkv_bias (nullable), seq_lens and out are
  * HOST pointers; the caches stay on the device as in ftd_decode_mha (NULL =
  * the pool).  When every one of them is pinned, GPU-addressable memory
- * (cudaHostAlloc / cudaHostRegister; 16-byte aligned, seq_lens 4-byte) one
- * gather kernel copies the inputs into the pool's staging buffers and the
- * decode kernel writes out straight into the host buffer (two launches, no
- * copy calls; on Grace systems both cross NVLink-C2C).  Otherwise the inputs
- * are copied in and out is copied back with cudaMemcpyAsync.  Either way the
- * call synchronises `stream` before it returns, so out is valid on return.
- * Contiguous contexts only.
+ * (cudaHostAlloc / cudaHostRegister; 16-byte aligned, seq_lens 4-byte) the
+ * decode kernel reads the inputs in place and writes out straight into the
+ * host buffer (one launch, no copy calls; on Grace systems both cross
+ * NVLink-C2C).  The buffers must not change until the call returns.
+ * Otherwise the inputs are copied in and out is copied back with
+ * cudaMemcpyAsync.  Either way the call synchronises `stream` before it
+ * returns, so out is valid on return.  Contiguous contexts only.
  */
 ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                const void* qkv_bias, void* k_cache, void* v_cache,

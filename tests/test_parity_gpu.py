@@ -225,8 +225,9 @@ def test_maximum_batch(cache, Hq, Hkv):
 
 
 def test_host_entry_point_with_pinned_buffers():
-    """Pinned host buffers take the direct path (one gather launch, output written to the host
-    by the kernel); the result matches the oracle and the caches get the appended rows."""
+    """Pinned host buffers take the direct path (one launch that reads the inputs in place and
+    writes the output to the host); the result matches the oracle and the caches get the
+    appended rows."""
     import torch
     w, inp = small("bf16", "bf16", B=3, Hq=16, Hkv=2, D=128, Lmax=256, lens=[0, 130, 255])
     ref = oracle.load().decode_step(w, inp)
@@ -247,7 +248,7 @@ def test_host_entry_point_with_pinned_buffers():
         n0 = ftd.ftd_kernel_launches()
         ftd.check(ftd.ftd_decode_mha_host(step.ctx, hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), hb.data_ptr(),
                                           kcur.data_ptr(), vcur.data_ptr(), hl.data_ptr(), 0, out.data_ptr(), s))
-        assert ftd.ftd_kernel_launches() - n0 == 2, "pinned buffers should take the gather + decode path"
+        assert ftd.ftd_kernel_launches() - n0 == 1, "pinned buffers should take the one-launch direct path"
         assert_close(out.numpy().astype(np.float64), ref["out"], what=f"pinned host entry point, call {rep}")
         assert_same_bytes(kcur.cpu().numpy().view(np.uint16), ref["k_cache"], "K after append")
     assert step.get_error() == ftd.FTD_OK
@@ -256,8 +257,7 @@ def test_host_entry_point_with_pinned_buffers():
 
 def test_host_entry_point_lengths_change_between_calls():
     """The direct host path reads the lengths in place: calls that rewrite the pinned
-    lengths between them each see their own lengths (the decode kernel computes its
-    split before it waits for the input gather)."""
+    lengths between them each see their own lengths."""
     import torch
     w, inp = small("bf16", "bf16", B=3, Hq=16, Hkv=2, D=128, Lmax=256, lens=[255, 255, 255])
     step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
