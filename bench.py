@@ -51,8 +51,9 @@ OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("1
 
 def kernel_name(w, q_len=1) -> str:
     """The kernel one step of workload ``w`` runs (the library's own selection rule)."""
-    tc = (w.cache_dtype in ("f16", "bf16") and w.D == 128 and (max(1, q_len) * w.Hq // w.Hkv) % 4 == 0
-          and os.environ.get("FTD_FORCE_CUDA_CORE", "0") != "1")
+    rows = max(1, q_len) * w.Hq // w.Hkv
+    tc = (w.D == 128 and os.environ.get("FTD_FORCE_CUDA_CORE", "0") != "1"
+          and ((w.cache_dtype in ("f16", "bf16") and rows % 4 == 0) or (w.cache_dtype == "i8" and rows % 8 == 0)))
     return "decode_gqa_tc_kernel" if tc else "decode_splitk_kernel"
 
 

@@ -73,18 +73,23 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// 2-D view of a [B][Hkv][Lmax][128] fp16/bf16 cache as rows of 128 elements,
-// read in boxes of 64 columns x 128 rows with the 128-byte swizzle the
-// tensor-core operands expect.
-bool encode_cache_map(CUtensorMap* map, void* base, bool bf16, size_t rows) {
+// 2-D view of a [B][Hkv][Lmax][128] cache as rows of 128 elements.  fp16/bf16:
+// boxes of 64 columns x 128 rows with the 128-byte swizzle the tensor-core
+// operands expect.  INT8: whole 128-byte rows in boxes of 128 rows, unswizzled
+// (the kernel converts them to the operand layout itself).
+bool encode_cache_map(CUtensorMap* map, void* base, ftd_dtype dt, size_t rows) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
+    const bool i8 = dt == FTD_I8;
     const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {128 * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(i8 ? 128 : 128 * 2)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(i8 ? 128 : 64), 128};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, base, dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const CUtensorMapDataType ty = i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : (dt == FTD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                        : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    return fn(map, ty, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -232,17 +237,21 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     // fp16/bf16 caches with head_dim 128 whose kv heads carry a multiple of 4
     // query rows (group x new tokens) use the tensor-core kernel, in blocks of
     // 16 or 8 rows (blocks of 4 fill half of an 8-column block, since the MMA
-    // needs N >= 16 with the hi/lo split); FTD_FORCE_CUDA_CORE=1 in the
-    // environment at ftd_init selects the CUDA-core kernel instead.
+    // needs N >= 16 with the hi/lo split).  INT8 caches with head_dim 128 and a
+    // multiple of 8 query rows per kv head use its INT8 variant, in blocks of 8.
+    // FTD_FORCE_CUDA_CORE=1 in the environment at ftd_init selects the CUDA-core
+    // kernel instead.
     const char* force = getenv("FTD_FORCE_CUDA_CORE");
+    const bool forced = force && force[0] == '1';
     const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
-                         rows_q % 4 == 0 && !(force && force[0] == '1');
+                         rows_q % 4 == 0 && !forced;
+    const bool want_tc_i8 = c.cache_dtype == FTD_I8 && c.head_dim == 128 && rows_q % 8 == 0 && !forced;
     ftd::TcKernelInfo tki{};
     int tc_nhb = 1, tc_qblk = 8;
-    if (want_tc && encode_tiled()) {
-        const int Gt = rows_q % 16 == 0 ? 16 : 8;
+    if ((want_tc || want_tc_i8) && encode_tiled()) {
+        const int Gt = (rows_q % 16 == 0 && !want_tc_i8) ? 16 : 8;
         tc_qblk = rows_q % 8 == 0 ? Gt : 4;
-        tki = ftd::select_tc(c.cache_dtype == FTD_BF16, Gt, nq > 1);
+        tki = want_tc_i8 ? ftd::select_tc_i8(nq > 1) : ftd::select_tc(c.cache_dtype == FTD_BF16, Gt, nq > 1);
         tc_nhb = rows_q / tc_qblk;
         e = cudaFuncSetAttribute(tki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tki.smem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (tensor-core kernel)");
@@ -405,14 +414,13 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     cudaError_t e;
     if (ctx->use_tc) {
         const size_t rows = ctx->rows;
-        const bool bf16 = c.cache_dtype == FTD_BF16;
         if (ctx->tm_k_base != k_cache) {
-            if (!encode_cache_map(&ctx->tmk, k_cache, bf16, rows))
+            if (!encode_cache_map(&ctx->tmk, k_cache, c.cache_dtype, rows))
                 return fail(FTD_ERR_CUDA, "cuTensorMapEncodeTiled failed for k_cache");
             ctx->tm_k_base = k_cache;
         }
         if (ctx->tm_v_base != v_cache) {
-            if (!encode_cache_map(&ctx->tmv, v_cache, bf16, rows))
+            if (!encode_cache_map(&ctx->tmv, v_cache, c.cache_dtype, rows))
                 return fail(FTD_ERR_CUDA, "cuTensorMapEncodeTiled failed for v_cache");
             ctx->tm_v_base = v_cache;
         }

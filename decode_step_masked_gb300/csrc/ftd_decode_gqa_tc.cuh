@@ -61,12 +61,21 @@ constexpr int kAlpha = 1;
 constexpr float kRescaleLog2 = 8.f;
 constexpr int threads_for(int G) { return 128 + 128 * softmax_groups(G); }
 
-template <int G>
+// INT8 caches: a raw stage holds a tile's codes (128 rows x 128 B for K, then for
+// V, unswizzled) and its 128 K and 128 V scales.
+constexpr int STAGE8 = 2 * TM * D + 2 * TM * 4;
+
+template <int G, bool I8 = false>
 struct Layout {
     static constexpr int N = 2 * G;                // hi and lo parts
     static constexpr int QS = 2 * N * 128;         // Qs / Ps: 2 k-blocks of N rows x 128 B
+    // operand stages the MMAs read: the TMA ring itself (fp16 / bf16), or two
+    // stages of fp16 codes that warps 2-3 convert from two raw INT8 stages
+    static constexpr int NB = I8 ? 2 : NS;
     static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_QS = NS * STAGE;
+    static constexpr int OFF_S8 = NB * STAGE;                                // raw INT8 stages
+    static constexpr int OFF_SC = OFF_S8 + (I8 ? 2 * round_up(STAGE8, 1024) : 0);  // [NB][2][TM] scales
+    static constexpr int OFF_QS = OFF_SC + (I8 ? NB * 2 * TM * 4 : 0);
     static constexpr int OFF_P = OFF_QS + round_up(QS, 1024);
     static constexpr int OFF_RED = OFF_P + 2 * round_up(QS, 1024);
     static constexpr int RED_BYTES = 4 * G * 4 * 2;  // per warp, per head: max and sum
@@ -239,6 +248,19 @@ __device__ __forceinline__ float from_ct<__nv_bfloat16>(__nv_bfloat16 x) { retur
 template <>
 __device__ __forceinline__ float from_ct<__half>(__half x) { return __half2float(x); }
 
+// Two int8 codes (bytes sel of w, each already offset by 128 through w ^ 0x80808080)
+// as an fp16 pair: the offset byte becomes the low mantissa bits under the exponent
+// of 1024, so the half is 1024 + 128 + code exactly, and 1152 is subtracted exactly.
+__device__ __forceinline__ uint32_t codes_to_h2(uint32_t wo, uint32_t sel) {
+    const uint32_t h = __byte_perm(wo, 0x64646464u, sel);
+    __half2 v;
+    memcpy(&v, &h, 4);
+    v = __hsub2(v, __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+    uint32_t r;
+    memcpy(&r, &v, 4);
+    return r;
+}
+
 }  // namespace tc
 
 // ------------------------------------------------- tile space in passes
@@ -343,8 +365,10 @@ struct PassSplit {
 };
 
 // Barrier slots in the misc area.
+// For INT8 caches kBarFull / kBarEmpty guard the converted operand stages and
+// kBarFull8 / kBarEmpty8 the raw stages.
 enum : int { kBarFull = 0, kBarEmpty = 3, kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarQReady = 12,
-             kNumBars = 13 };
+             kBarFull8 = 13, kBarEmpty8 = 15, kNumBars = 17 };
 
 // MQ: several new tokens per slot (q_len > 1), so the columns of S carry
 // their own causal limits; without it every column shares one row range.
@@ -352,19 +376,26 @@ template <typename CT, int G, bool MQ>
 __global__ void __launch_bounds__(tc::threads_for(G), 1)
     decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
-    using LY = tc::Layout<G>;
-    constexpr int N = LY::N, TM = tc::TM, D = tc::D, NS = tc::NS, KB = tc::KB;
+    // INT8 caches: the MMAs run on fp16 copies of the codes (exact), and the
+    // per-row scales multiply the scores and are folded into the weights.
+    constexpr bool I8 = std::is_same_v<CT, int8_t>;
+    using MT = std::conditional_t<I8, __half, CT>;  // operand type of the MMAs
+    using LY = tc::Layout<G, I8>;
+    constexpr int N = LY::N, TM = tc::TM, D = tc::D, NS = tc::NS, KB = tc::KB, NB = LY::NB;
+    constexpr int EBC = I8 ? 1 : 2;  // bytes per cache element
     constexpr int SH = tc::softmax_groups(G);  // softmax warp groups, splitting the query columns
     constexpr int GH = G / SH;                  // query columns per softmax thread
     constexpr int SMX = 128 * SH;               // softmax threads
     constexpr int PSZ = round_up(LY::QS, 1024);
-    constexpr bool BF = std::is_same_v<CT, __nv_bfloat16>;
+    constexpr bool BF = std::is_same_v<MT, __nv_bfloat16>;
     constexpr unsigned FULL = 0xffffffffu;
 
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~static_cast<uintptr_t>(1023));
     unsigned char* stages = smem + LY::OFF_STAGE;
+    unsigned char* stages8 = smem + LY::OFF_S8;                  // INT8: raw stages
+    float* scl = reinterpret_cast<float*>(smem + LY::OFF_SC);   // INT8: [NB][K | V][TM] scales
     unsigned char* Qs = smem + LY::OFF_QS;
     unsigned char* Ps = smem + LY::OFF_P;
     float* red_max = reinterpret_cast<float*>(smem + LY::OFF_RED);
@@ -421,8 +452,8 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
             const int n_cache = min(TM, max(0, L - t0));
             if (n_cache > 0) {
                 const size_t rb = static_cast<size_t>(cache_row(p, c.b, c.seg / p.nhb, t0, 0));
-                bulk_prefetch_l2(p.k_cache + rb * D * 2, static_cast<uint32_t>(n_cache) * D * 2);
-                bulk_prefetch_l2(p.v_cache + rb * D * 2, static_cast<uint32_t>(n_cache) * D * 2);
+                bulk_prefetch_l2(p.k_cache + rb * D * EBC, static_cast<uint32_t>(n_cache) * D * EBC);
+                bulk_prefetch_l2(p.v_cache + rb * D * EBC, static_cast<uint32_t>(n_cache) * D * EBC);
             }
             if (k + 1 < min(NS, n_my)) advance_pass(c, P, p.B, spp, np);
         }
@@ -455,19 +486,44 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         rb = 0;
                     }
                     const int row0 = static_cast<int>(rb);
-                    if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag)) break;
-                    const uint32_t st = smem_addr(stages + s * tc::STAGE);
-                    mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
-                    tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s), l2pol);
-                    tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
-                    tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
-                    tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
+                    if constexpr (I8) {
+                        // raw stage: K and V codes (one 128 x 128 B box each) and the scales
+                        // of the rows before the new tokens
+                        const int s8 = k & 1;
+                        if (k >= 2 && !tc::wait_or_abort(bar(kBarEmpty8 + s8), ((k >> 1) - 1) & 1, p.err, abort_flag))
+                            break;
+                        const int n_cache = min(TM, max(0, Ls[cu.b] - t0));
+                        const uint32_t sb = static_cast<uint32_t>((n_cache * 4 + 15) & ~15);
+                        unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
+                        const uint32_t fb = bar(kBarFull8 + s8);
+                        mbar_arrive_expect_tx(fb, 2 * TM * D + 2 * sb);
+                        tc::tma_load_2d(smem_addr(st8), &tmk, 0, row0, fb, l2pol);
+                        tc::tma_load_2d(smem_addr(st8 + TM * D), &tmv, 0, row0, fb, l2pol);
+                        if (sb) {
+                            bulk_g2s_hint(smem_addr(st8 + 2 * TM * D), p.k_scales + rb, sb, fb, l2pol);
+                            bulk_g2s_hint(smem_addr(st8 + 2 * TM * D + TM * 4), p.v_scales + rb, sb, fb, l2pol);
+                        }
+                    } else {
+                        if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag))
+                            break;
+                        const uint32_t st = smem_addr(stages + s * tc::STAGE);
+                        mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
+                        tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s), l2pol);
+                        tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
+                        tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
+                        tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
+                    }
                     if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
                 }
                 if (k < n_my) {
                     // aborted: let the copies already issued land before the block exits
-                    for (int kk = max(0, k - NS); kk < k; ++kk)
-                        mbar_wait_bounded(bar(kBarFull + kk % NS), (kk / NS) & 1, p.err);
+                    if constexpr (I8) {
+                        for (int kk = max(0, k - 2); kk < k; ++kk)
+                            mbar_wait_bounded(bar(kBarFull8 + (kk & 1)), (kk >> 1) & 1, p.err);
+                    } else {
+                        for (int kk = max(0, k - NS); kk < k; ++kk)
+                            mbar_wait_bounded(bar(kBarFull + kk % NS), (kk / NS) & 1, p.err);
+                    }
                 }
             }
         } else if (warp == 1) {
@@ -493,7 +549,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 if (__any_sync(FULL, !w)) return false;
                 if (lane == 0) {
                     tc::tc_fence_after();
-                    const uint64_t va = dv0 + static_cast<uint32_t>((kk % NS) * (tc::STAGE >> 4));
+                    const uint64_t va = dv0 + static_cast<uint32_t>((kk % NB) * (tc::STAGE >> 4));
                     const uint64_t pa = dp0 + static_cast<uint32_t>((kk & 1) * (PSZ >> 4));
 #pragma unroll
                     for (int ks = 0; ks < TM / 16; ++ks) {
@@ -502,18 +558,20 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         tc::mma_f16(tmem + 2 * N + (kk & 1) * N, a, bd, id_o, ks > 0);
                     }
                     tc::mma_commit(bar(kBarOFull + (kk & 1)));
-                    tc::mma_commit(bar(kBarEmpty + kk % NS));
+                    tc::mma_commit(bar(kBarEmpty + kk % NB));
                 }
                 __syncwarp();
                 return true;
             };
             for (int k = 0; k < n_my; ++k) {
-                const int s = k % NS;
+                const int s = k % NB;
                 const bool new_piece = (k == 0) || (cu.tile == 0);
                 if (k > 0 && new_piece && !issue_pv(k - 1)) { ok = false; break; }
-                const bool wf = tc::wait_or_abort(bar(kBarFull + s), (k / NS) & 1, p.err, abort_flag);
+                const bool wf = tc::wait_or_abort(bar(kBarFull + s), (k / NB) & 1, p.err, abort_flag);
                 if (__any_sync(FULL, !wf)) { ok = false; break; }
-                if (cu.tile == 0 && p.window > 0) {
+                // (INT8: the converting warps append, and the weights of rows outside
+                // the window or past the end are zero, so no staged row needs zeroing)
+                if (!I8 && cu.tile == 0 && p.window > 0) {
                     // rows of the first tile before the window start get weight 0; zero
                     // their staged V so stale or non-finite history cannot reach O
                     const int nlo = window_start(Ls[cu.b], p.window) % TM;
@@ -530,7 +588,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 bool has_new = cu.tile == cu.nt - 1;
                 if constexpr (MQ)
                     has_new = Ls[cu.b] < (window_start(Ls[cu.b], p.window) / TM + cu.tile + 1) * TM;
-                if (has_new) {
+                if (!I8 && has_new) {
                     // ---- append the new tokens (rows L - t0 ..) and zero staged V rows past the end ----
                     const int L = Ls[cu.b];
                     const int t0 = (window_start(L, p.window) / TM + cu.tile) * TM;
@@ -560,7 +618,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                                 x0 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e);
                                 x1 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e + 1);
                             }
-                            const CT y0 = tc::to_ct<CT>(x0), y1 = tc::to_ct<CT>(x1);
+                            const MT y0 = tc::to_ct<MT>(x0), y1 = tc::to_ct<MT>(x1);
                             uint16_t u0, u1;
                             memcpy(&u0, &y0, 2);
                             memcpy(&u1, &y1, 2);
@@ -600,6 +658,91 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
             }
             if (ok) issue_pv(n_my - 1);
+        } else if (I8 && warp >= 2 && warp < 4) {
+            // ------------------------------------- INT8: append and fp16 conversion
+            // Warps 2-3 take the raw stages in order.  In a tile holding new tokens
+            // warp 2 quantises the K rows and warp 3 the V rows (cache codes and
+            // scales, and the staged copies).  Then all 64 threads convert the codes
+            // into the fp16 operand layout of the MMAs (128-byte swizzle, as TMA
+            // writes it for fp16 caches), copy the scales beside it, publish the
+            // operand stage and free the raw stage.
+            const int ct = tid - 64;
+            const bool isv = warp == 3;
+            Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
+            for (int k = 0; k < n_my; ++k) {
+                const int s8 = k & 1, sb = k % NB;
+                const bool okf = tc::wait_or_abort(bar(kBarFull8 + s8), (k >> 1) & 1, p.err, abort_flag);
+                if (tc::bar_any(3, 64, !okf)) break;
+                unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
+                float* ssc = reinterpret_cast<float*>(st8 + 2 * TM * D);  // [K | V][TM]
+                const int L = Ls[cu.b];
+                const int t0 = (window_start(L, p.window) / TM + cu.tile) * TM;
+                bool has_new = cu.tile == cu.nt - 1;
+                if constexpr (MQ) has_new = L < t0 + TM;
+                if (has_new) {
+                    const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
+                    const int n_total = min(TM, L + p.nq - t0);
+                    for (int nr = max(0, L - t0); nr < n_total; ++nr) {
+                        const int tok = t0 + nr - L, pos = t0 + nr;
+                        const void* src = isv ? p.v_new : p.k_new;
+                        const size_t si = ((static_cast<size_t>(cu.b) * p.nq + tok) * p.Hkv + kvh) * D + lane * 4;
+                        const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + lane * 4;
+                        float x[4];
+                        float amax = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            x[e] = ld_qkv(src, p.qkv_dtype, si + e);
+                            if (p.bias) x[e] += ld_qkv(p.bias, p.qkv_dtype, bi + e);  // one binary32 add
+                            amax = fmaxf(amax, fabsf(x[e]));
+                        }
+                        amax = warp_max(amax);
+                        const float qs = amax == 0.f ? 1.f : __fdiv_rn(amax, 127.f);
+                        uint32_t w = 0u;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            int code = 0;
+                            if (amax != 0.f) code = max(-127, min(127, __float2int_rn(__fdiv_rn(x[e], qs))));
+                            w |= (static_cast<uint32_t>(code) & 0xffu) << (8 * e);
+                        }
+                        *reinterpret_cast<uint32_t*>(st8 + (isv ? TM * D : 0) + nr * D + lane * 4) = w;
+                        if (lane == 0) ssc[(isv ? TM : 0) + nr] = qs;
+                        const long long rowL = cache_row(p, cu.b, kvh, pos, page_of(p, cu.b, pos));
+                        if (rowL >= 0 && hb == 0) {  // the first head block writes the cache
+                            *reinterpret_cast<uint32_t*>((isv ? p.v_cache : p.k_cache) + rowL * D + lane * 4) = w;
+                            if (lane == 0) (isv ? p.v_scales : p.k_scales)[rowL] = qs;
+                        }
+                    }
+                }
+                // the operand stage is free once the MMAs of tile k - NB have completed;
+                // the barrier also makes the appended rows visible to both warps
+                bool oke = true;
+                if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmpty + sb), ((k / NB) - 1) & 1, p.err, abort_flag);
+                if (tc::bar_any(3, 64, !oke)) break;
+                unsigned char* dst = stages + sb * tc::STAGE;
+                for (int i = ct; i < 2 * TM * (D / 16); i += 64) {  // 16-code chunks: [K | V][row][8]
+                    const int v = i / (TM * (D / 16)), r = (i / (D / 16)) % TM, j = i % (D / 16);
+                    const uint4 u = *reinterpret_cast<const uint4*>(st8 + v * TM * D + r * D + j * 16);
+                    const uint32_t a[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u,
+                                           u.w ^ 0x80808080u};
+                    const uint4 h0 = make_uint4(tc::codes_to_h2(a[0], 0x4140), tc::codes_to_h2(a[0], 0x4342),
+                                                tc::codes_to_h2(a[1], 0x4140), tc::codes_to_h2(a[1], 0x4342));
+                    const uint4 h1 = make_uint4(tc::codes_to_h2(a[2], 0x4140), tc::codes_to_h2(a[2], 0x4342),
+                                                tc::codes_to_h2(a[3], 0x4140), tc::codes_to_h2(a[3], 0x4342));
+                    // fp16 columns 16 j .. 16 j + 15: box j / 4, 16-byte chunks 2 (j % 4) and 2 (j % 4) + 1
+                    unsigned char* row = dst + v * 2 * KB + (j >> 2) * KB + r * 128;
+                    const int c16 = 2 * (j & 3);
+                    *reinterpret_cast<uint4*>(row + ((c16 ^ (r & 7)) << 4)) = h0;
+                    *reinterpret_cast<uint4*>(row + (((c16 + 1) ^ (r & 7)) << 4)) = h1;
+                }
+                for (int i = ct; i < 2 * TM; i += 64) scl[sb * 2 * TM + i] = ssc[i];
+                fence_proxy_async_smem();  // the MMAs read the stage through the async proxy
+                tc::named_bar_sync(3, 64);
+                if (ct == 0) {
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarFull + sb)) : "memory");
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarEmpty8 + s8)) : "memory");
+                }
+                if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
+            }
         } else if (warp >= 4) {
             // ------------------------------------------------ softmax and output
             // SH groups of four warps; group ch owns query columns [ch * GH, (ch + 1) * GH)
@@ -671,10 +814,10 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
             auto store_q = [&]() {
 #pragma unroll
                 for (int jj = 0; jj < GH; ++jj) {
-                    const CT hi = tc::to_ct<CT>(qn[jj]);
-                    const CT lo = tc::to_ct<CT>(qn[jj] - tc::from_ct<CT>(hi));
-                    *reinterpret_cast<CT*>(Qs + tc::sw128_offset(c0 + jj, r, N)) = hi;
-                    *reinterpret_cast<CT*>(Qs + tc::sw128_offset(G + c0 + jj, r, N)) = lo;
+                    const MT hi = tc::to_ct<MT>(qn[jj]);
+                    const MT lo = tc::to_ct<MT>(qn[jj] - tc::from_ct<MT>(hi));
+                    *reinterpret_cast<MT*>(Qs + tc::sw128_offset(c0 + jj, r, N)) = hi;
+                    *reinterpret_cast<MT*>(Qs + tc::sw128_offset(G + c0 + jj, r, N)) = lo;
                 }
                 fence_proxy_async_smem();
                 tc::named_bar_sync(1, SMX);
@@ -714,7 +857,10 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                     load_q(nx);
                 }
                 // ---- scores of this tile ----
-                const bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag);
+                bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag);
+                // INT8: the scales of the tile come from the converting warps; waiting on
+                // their publication (complete by now) orders those writes before the reads
+                if constexpr (I8) oks = oks && tc::wait_or_abort(bar(kBarFull + k % NB), (k / NB) & 1, p.err, abort_flag);
                 if (tc::bar_any(2, SMX, !oks)) break;
                 tc::tc_fence_after();
                 __syncwarp();
@@ -725,20 +871,27 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 const int hi0 = L + 1 - t0, lo0 = p.window > 0 ? L + 1 - p.window - t0 : -(1 << 30);
                 const bool valid0 = r >= lo0 && r < hi0;  // the rows every column sees (single token)
                 float sc[GH];
+                float vf[GH];  // INT8: the row's V scale, folded into the weight (0 for rows not seen)
                 bool need = false;  // a visible score above the column's reference by more than the margin
+                float ksr = 1.f, vsr = 1.f;
+                if constexpr (I8) {
+                    ksr = scl[(k % NB) * 2 * TM + r];
+                    vsr = scl[(k % NB) * 2 * TM + TM + r];
+                }
 #pragma unroll
                 for (int jj = 0; jj < GH; ++jj) {
                     const bool valid = MQ ? (r >= lo0 + tk[jj] && r < hi0 + tk[jj]) : valid0;
-                    sc[jj] = valid ? sh[jj] + sl_[jj] : -INFINITY;
+                    sc[jj] = valid ? (I8 ? (sh[jj] + sl_[jj]) * ksr : sh[jj] + sl_[jj]) : -INFINITY;
+                    vf[jj] = valid ? vsr : 0.f;
                     need |= sc[jj] > m[jj] + tc::kRescaleLog2;  // always when m = -inf and the score is visible
                 }
                 float alpha[GH];
                 unsigned char* pb = Ps + (k & 1) * PSZ;
                 auto put_p = [&](int jj, float pj) {
-                    const CT hi = tc::to_ct<CT>(pj);
-                    const CT lo = tc::to_ct<CT>(pj - tc::from_ct<CT>(hi));
-                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(c0 + jj, r, N)) = hi;
-                    *reinterpret_cast<CT*>(pb + tc::sw128_offset(G + c0 + jj, r, N)) = lo;
+                    const MT hi = tc::to_ct<MT>(pj);
+                    const MT lo = tc::to_ct<MT>(pj - tc::from_ct<MT>(hi));
+                    *reinterpret_cast<MT*>(pb + tc::sw128_offset(c0 + jj, r, N)) = hi;
+                    *reinterpret_cast<MT*>(pb + tc::sw128_offset(G + c0 + jj, r, N)) = lo;
                 };
                 // Optimistic pass: the weights are taken against the running reference m,
                 // which is valid (any reference is) as long as they stay below 2^margin.
@@ -750,7 +903,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                     for (int jj = 0; jj < GH; ++jj) {
                         // a column with no visible row yet keeps m = -inf; 0 stands in as the reference
                         pq[jj] = exp2f(sc[jj] - (m[jj] == -INFINITY ? 0.f : m[jj]));
-                        put_p(jj, pq[jj]);
+                        put_p(jj, I8 ? pq[jj] * vf[jj] : pq[jj]);
                     }
                 }
                 fence_proxy_async_smem();
@@ -786,7 +939,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         }
                         l[jj] = l[jj] * alpha[jj] + pj;
                         m[jj] = mnew;
-                        put_p(jj, pj);
+                        put_p(jj, I8 ? pj * vf[jj] : pj);
                     }
                     fence_proxy_async_smem();
                     tc::tc_fence_before();
@@ -917,11 +1070,12 @@ struct TcKernelInfo {
 
 template <typename CT, int G, bool MQ>
 TcKernelInfo tc_kernel_info() {
-    using LY = tc::Layout<G>;
+    using LY = tc::Layout<G, std::is_same_v<CT, int8_t>>;
     return TcKernelInfo{reinterpret_cast<const void*>(&decode_gqa_tc_kernel<CT, G, MQ>), LY::SMEM, LY::SLOT, G,
                         tc::threads_for(G)};
 }
 
 TcKernelInfo select_tc(bool bf16, int G, bool multi_token);
+TcKernelInfo select_tc_i8(bool multi_token);
 
 }  // namespace ftd

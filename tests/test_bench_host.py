@@ -60,6 +60,10 @@ def test_step_bytes_several_new_tokens():
     assert by_w["ctx"] == 13  # rows some token sees: positions 91 .. 103
     assert bench.kernel_name(w, 8) == "decode_gqa_tc_kernel" and bench.kernel_name(w, 4) == "decode_gqa_tc_kernel"
     assert bench.kernel_name(w, 2) == "decode_splitk_kernel"
+    i8 = WORKLOADS["int8"]  # INT8: the tensor-core variant takes blocks of 8 query rows
+    assert bench.kernel_name(i8) == "decode_splitk_kernel" and bench.kernel_name(i8, 4) == "decode_splitk_kernel"
+    assert bench.kernel_name(i8, 8) == "decode_gqa_tc_kernel"
+    assert bench.kernel_name(i8.with_(Hq=64, Hkv=8)) == "decode_gqa_tc_kernel"
 
 
 def test_page_table_is_a_permutation():

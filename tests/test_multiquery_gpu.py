@@ -50,6 +50,8 @@ CASES = {
     "gqa_bf16_T3_cc": ("bf16", "bf16", 3, 16, 2, 128, 1024, [125, 500, 1021], 3, True),
     "mqa_f16_T5_tc": ("f16", "f16", 2, 8, 1, 128, 512, [124, 300], 5, False),
     "mqa_f16_T5_cc": ("f16", "f16", 2, 8, 1, 128, 512, [124, 300], 5, True),
+    "gqa_i8_T2_tc": ("i8", "f16", 4, 16, 4, 128, 1024, [0, 127, 126, 1022], 2, False),  # 8 rows per kv head
+    "mqa_i8_T3_tc": ("i8", "bf16", 3, 8, 1, 128, 512, [125, 0, 509], 3, False),         # 24 rows: 3 blocks
 }
 
 

@@ -51,6 +51,8 @@ SHAPES = {
     "gqa_tc_bf16": ("bf16", "bf16", 4, 32, 4, 128, 1024, [0, 127, 700, 1023], False),
     "gqa_tc_f16": ("f16", "f16", 3, 16, 2, 128, 1024, [129, 512, 1000], False),
     "gqa_cc_bf16": ("bf16", "bf16", 4, 32, 4, 128, 1024, [0, 127, 700, 1023], True),
+    "gqa_tc_i8": ("i8", "f16", 4, 32, 4, 128, 1024, [0, 127, 700, 1023], False),
+    "gqa_cc_i8": ("i8", "f16", 4, 32, 4, 128, 1024, [0, 127, 700, 1023], True),
 }
 
 
@@ -175,6 +177,7 @@ PAGED = {
     "gqa_tc_bf16_p256": ("bf16", "bf16", 4, 32, 4, 128, 1024, [0, 255, 700, 1023], 256, False),
     "gqa_tc_f16_p128": ("f16", "f16", 3, 16, 2, 128, 1024, [129, 512, 1000], 128, False),
     "gqa_cc_bf16_p256": ("bf16", "bf16", 4, 32, 4, 128, 1024, [0, 255, 700, 1023], 256, True),
+    "gqa_tc_i8_p128": ("i8", "f16", 3, 16, 2, 128, 1024, [129, 512, 1000], 128, False),
 }
 
 
@@ -227,7 +230,7 @@ def test_paged_cache(shape):
 
 
 @pytest.mark.parametrize("window", [100, 256, 300])
-@pytest.mark.parametrize("shape", ["mha_bf16_p128", "gqa_tc_bf16_p256", "mha_i8_p128"])
+@pytest.mark.parametrize("shape", ["mha_bf16_p128", "gqa_tc_bf16_p256", "mha_i8_p128", "gqa_tc_i8_p128"])
 def test_paged_with_window_reads_only_window_pages(shape, window):
     """Entries of pages wholly before the window start are never read: they hold the sentinel."""
     cache, qkv, B, Hq, Hkv, D, Lmax, lens, ps, cc = PAGED[shape]

@@ -96,6 +96,18 @@ def test_tensor_core_many_tiles_per_cta(cache, B, Hq, Hkv, Lmax, lens):
     check_step(w, inp, what=f"tc many tiles {B}x{Hq}/{Hkv} {cache}")
 
 
+@pytest.mark.parametrize("B,Hq,Hkv,Lmax,lens", [
+    (16, 64, 8, 8192, [8191] * 16),                                      # 70B-shaped, ~54 tiles per CTA
+    (8, 16, 1, 8192, [8191, 4000, 7000, 129, 8000, 6143, 5000, 7777]),  # 16 rows: 2 blocks of 8, ragged
+    (6, 16, 2, 1024, [16000 % 1024, 127, 128, 0, 129, 1023]),           # tile edges, one token
+])
+def test_tensor_core_int8(B, Hq, Hkv, Lmax, lens):
+    """INT8 caches with blocks of 8 query rows: codes converted to fp16 on chip, scales on the
+    scores and in the weights; appended codes and scales bit for bit."""
+    w, inp = small("i8", "f16", B=B, Hq=Hq, Hkv=Hkv, D=128, Lmax=Lmax, lens=lens, bias=0.1)
+    check_step(w, inp, what=f"tc int8 {B}x{Hq}/{Hkv}")
+
+
 def test_inactive_and_overflow_slots():
     w, inp = small("bf16", "bf16", B=6, Hq=4, Hkv=2, D=128, Lmax=128, lens=[-1, 127, 128, 5, 1000, -7])
     got, ref = check_step(w, inp, what="inactive/overflow")
