@@ -73,10 +73,10 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-// 2-D view of a [B][Hkv][Lmax][128] cache as rows of 128 elements.  fp16/bf16:
-// boxes of 64 columns x 128 rows with the 128-byte swizzle the tensor-core
-// operands expect.  INT8: whole 128-byte rows in boxes of 128 rows, unswizzled
-// (the kernel converts them to the operand layout itself).
+// 2-D view of a [B][Hkv][Lmax][128] cache as rows of 128 elements, read in
+// boxes of 128 rows with the 128-byte swizzle: 64 columns per box for fp16/bf16
+// (the tensor-core operand layout), whole 128-byte rows for INT8 (the kernel
+// converts those to the operand layout itself).
 bool encode_cache_map(CUtensorMap* map, void* base, ftd_dtype dt, size_t rows) {
     EncodeTiledFn fn = encode_tiled();
     if (!fn) return false;
@@ -89,7 +89,7 @@ bool encode_cache_map(CUtensorMap* map, void* base, ftd_dtype dt, size_t rows) {
                                       : (dt == FTD_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
     return fn(map, ty, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

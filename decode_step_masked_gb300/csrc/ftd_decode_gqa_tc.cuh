@@ -59,10 +59,13 @@ constexpr int kAlpha = 1;
 // before the softmax moves the reference: weights then stay below 2^8, well
 // inside the range of the hi / lo operand pair and of the fp32 accumulators.
 constexpr float kRescaleLog2 = 8.f;
-constexpr int threads_for(int G) { return 128 + 128 * softmax_groups(G); }
+// INT8 caches add four warps (12-15) to the two (2-3) that convert codes to fp16.
+constexpr int converter_threads(bool i8) { return i8 ? 192 : 0; }
+constexpr int threads_for(int G, bool i8 = false) { return 128 + 128 * softmax_groups(G) + (i8 ? 128 : 0); }
 
 // INT8 caches: a raw stage holds a tile's codes (128 rows x 128 B for K, then for
-// V, unswizzled) and its 128 K and 128 V scales.
+// V, with the 128-byte swizzle: 16-byte chunk c of row r at chunk c ^ (r % 8)) and
+// its 128 K and 128 V scales.
 constexpr int STAGE8 = 2 * TM * D + 2 * TM * 4;
 
 template <int G, bool I8 = false>
@@ -74,8 +77,11 @@ struct Layout {
     static constexpr int NB = I8 ? 2 : NS;
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_S8 = NB * STAGE;                                // raw INT8 stages
-    static constexpr int OFF_SC = OFF_S8 + (I8 ? 2 * round_up(STAGE8, 1024) : 0);  // [NB][2][TM] scales
-    static constexpr int OFF_QS = OFF_SC + (I8 ? NB * 2 * TM * 4 : 0);
+    // [4][K | V][TM] scales, slot k % 4: the softmax of tile k reads its slot until
+    // it publishes P, and the slot is rewritten for tile k + 4 only after the score
+    // MMAs of tile k + 2, which follow the P.V issue of tile k
+    static constexpr int OFF_SC = OFF_S8 + (I8 ? 2 * round_up(STAGE8, 1024) : 0);
+    static constexpr int OFF_QS = OFF_SC + (I8 ? 4 * 2 * TM * 4 : 0);
     static constexpr int OFF_P = OFF_QS + round_up(QS, 1024);
     static constexpr int OFF_RED = OFF_P + 2 * round_up(QS, 1024);
     static constexpr int RED_BYTES = 4 * G * 4 * 2;  // per warp, per head: max and sum
@@ -365,15 +371,16 @@ struct PassSplit {
 };
 
 // Barrier slots in the misc area.
-// For INT8 caches kBarFull / kBarEmpty guard the converted operand stages and
-// kBarFull8 / kBarEmpty8 the raw stages.
+// For INT8 caches kBarFull / kBarEmpty guard the K halves of the converted
+// operand stages, kBarFullV / kBarEmptyV their V halves, kBarFull8 / kBarEmpty8
+// the raw stages, and kBarScale the four scale slots.
 enum : int { kBarFull = 0, kBarEmpty = 3, kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarQReady = 12,
-             kBarFull8 = 13, kBarEmpty8 = 15, kNumBars = 17 };
+             kBarFull8 = 13, kBarEmpty8 = 15, kBarFullV = 17, kBarEmptyV = 19, kBarScale = 21, kNumBars = 25 };
 
 // MQ: several new tokens per slot (q_len > 1), so the columns of S carry
 // their own causal limits; without it every column shares one row range.
 template <typename CT, int G, bool MQ>
-__global__ void __launch_bounds__(tc::threads_for(G), 1)
+__global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>), 1)
     decode_gqa_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                          const DecodeParams p) {
     // INT8 caches: the MMAs run on fp16 copies of the codes (exact), and the
@@ -395,7 +402,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                                                            ~static_cast<uintptr_t>(1023));
     unsigned char* stages = smem + LY::OFF_STAGE;
     unsigned char* stages8 = smem + LY::OFF_S8;                  // INT8: raw stages
-    float* scl = reinterpret_cast<float*>(smem + LY::OFF_SC);   // INT8: [NB][K | V][TM] scales
+    float* scl = reinterpret_cast<float*>(smem + LY::OFF_SC);   // INT8: [4][K | V][TM] scales
     unsigned char* Qs = smem + LY::OFF_QS;
     unsigned char* Ps = smem + LY::OFF_P;
     float* red_max = reinterpret_cast<float*>(smem + LY::OFF_RED);
@@ -545,7 +552,8 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
             const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(Qs), 16, 1024);
             const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(Ps), 16, 1024);
             auto issue_pv = [&](int kk) -> bool {
-                const bool w = tc::wait_or_abort(bar(kBarPFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
+                bool w = tc::wait_or_abort(bar(kBarPFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
+                if constexpr (I8) w = w && tc::wait_or_abort(bar(kBarFullV + kk % NB), (kk / NB) & 1, p.err, abort_flag);
                 if (__any_sync(FULL, !w)) return false;
                 if (lane == 0) {
                     tc::tc_fence_after();
@@ -558,7 +566,7 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         tc::mma_f16(tmem + 2 * N + (kk & 1) * N, a, bd, id_o, ks > 0);
                     }
                     tc::mma_commit(bar(kBarOFull + (kk & 1)));
-                    tc::mma_commit(bar(kBarEmpty + kk % NB));
+                    tc::mma_commit(bar((I8 ? kBarEmptyV : kBarEmpty) + kk % NB));
                 }
                 __syncwarp();
                 return true;
@@ -652,34 +660,36 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         tc::mma_f16(tmem + (k & 1) * N, a, bd, id_s, ks > 0);
                     }
                     tc::mma_commit(bar(kBarSFull + (k & 1)));
+                    if constexpr (I8) tc::mma_commit(bar(kBarEmpty + s));  // the K half is read
                 }
                 __syncwarp();
                 if (k > 0 && !new_piece && !issue_pv(k - 1)) { ok = false; break; }
                 if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
             }
             if (ok) issue_pv(n_my - 1);
-        } else if (I8 && warp >= 2 && warp < 4) {
+        } else if (I8 && ((warp >= 2 && warp < 4) || warp >= 4 + 4 * SH)) {
             // ------------------------------------- INT8: append and fp16 conversion
-            // Warps 2-3 take the raw stages in order.  In a tile holding new tokens
-            // warp 2 quantises the K rows and warp 3 the V rows (cache codes and
-            // scales, and the staged copies).  Then all 64 threads convert the codes
-            // into the fp16 operand layout of the MMAs (128-byte swizzle, as TMA
-            // writes it for fp16 caches), copy the scales beside it, publish the
+            // Warps 2-3 and 12-15 take the raw stages in order.  In a tile holding
+            // new tokens warp 2 quantises the K rows and warp 3 the V rows (cache
+            // codes and scales, and the staged copies).  Then all 192 threads convert
+            // the codes into the fp16 operand layout of the MMAs (128-byte swizzle, as
+            // TMA writes it for fp16 caches), copy the scales beside it, publish the
             // operand stage and free the raw stage.
-            const int ct = tid - 64;
+            constexpr int NCV = tc::converter_threads(I8);
+            const int ct = warp < 4 ? tid - 64 : tid - (128 + SMX) + 64;  // 0 .. NCV - 1
             const bool isv = warp == 3;
             Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
             for (int k = 0; k < n_my; ++k) {
                 const int s8 = k & 1, sb = k % NB;
                 const bool okf = tc::wait_or_abort(bar(kBarFull8 + s8), (k >> 1) & 1, p.err, abort_flag);
-                if (tc::bar_any(3, 64, !okf)) break;
+                if (tc::bar_any(3, NCV, !okf)) break;
                 unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
                 float* ssc = reinterpret_cast<float*>(st8 + 2 * TM * D);  // [K | V][TM]
                 const int L = Ls[cu.b];
                 const int t0 = (window_start(L, p.window) / TM + cu.tile) * TM;
                 bool has_new = cu.tile == cu.nt - 1;
                 if constexpr (MQ) has_new = L < t0 + TM;
-                if (has_new) {
+                if (has_new && warp < 4) {  // warp 2 appends K rows, warp 3 V rows
                     const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
                     const int n_total = min(TM, L + p.nq - t0);
                     for (int nr = max(0, L - t0); nr < n_total; ++nr) {
@@ -704,7 +714,8 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                             if (amax != 0.f) code = max(-127, min(127, __float2int_rn(__fdiv_rn(x[e], qs))));
                             w |= (static_cast<uint32_t>(code) & 0xffu) << (8 * e);
                         }
-                        *reinterpret_cast<uint32_t*>(st8 + (isv ? TM * D : 0) + nr * D + lane * 4) = w;
+                        *reinterpret_cast<uint32_t*>(st8 + (isv ? TM * D : 0) + nr * D +
+                                                     ((((lane >> 2) ^ (nr & 7)) << 4) | ((lane & 3) << 2))) = w;
                         if (lane == 0) ssc[(isv ? TM : 0) + nr] = qs;
                         const long long rowL = cache_row(p, cu.b, kvh, pos, page_of(p, cu.b, pos));
                         if (rowL >= 0 && hb == 0) {  // the first head block writes the cache
@@ -713,37 +724,55 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                         }
                     }
                 }
-                // the operand stage is free once the MMAs of tile k - NB have completed;
-                // the barrier also makes the appended rows visible to both warps
+                // Codes to fp16, one half of the operand stage: half 0 (K) once the score
+                // MMAs of tile k - NB have read it, half 1 (V) once its P.V MMAs have.
+                // Each thread converts 16-code chunks (row r, chunk j) of the half, rows
+                // fastest across the threads: with both layouts swizzled, the eight
+                // rows a quarter-warp touches fall in distinct banks.
+                unsigned char* dst = stages + sb * tc::STAGE;
+                auto convert = [&](int v) {
+#pragma unroll 4
+                    for (int i = ct; i < TM * (D / 16); i += NCV) {
+                        const int r = i % TM, j = i / TM;
+                        const uint4 u =
+                            *reinterpret_cast<const uint4*>(st8 + v * TM * D + r * D + ((j ^ (r & 7)) << 4));
+                        const uint32_t a0 = u.x ^ 0x80808080u, a1 = u.y ^ 0x80808080u;
+                        const uint32_t a2 = u.z ^ 0x80808080u, a3 = u.w ^ 0x80808080u;
+                        const uint4 h0 = make_uint4(tc::codes_to_h2(a0, 0x4140), tc::codes_to_h2(a0, 0x4342),
+                                                    tc::codes_to_h2(a1, 0x4140), tc::codes_to_h2(a1, 0x4342));
+                        const uint4 h1 = make_uint4(tc::codes_to_h2(a2, 0x4140), tc::codes_to_h2(a2, 0x4342),
+                                                    tc::codes_to_h2(a3, 0x4140), tc::codes_to_h2(a3, 0x4342));
+                        // fp16 columns 16 j .. 16 j + 15: box j / 4, 16-byte chunks 2 (j % 4) and +1
+                        unsigned char* row = dst + v * 2 * KB + (j >> 2) * KB + r * 128;
+                        const int c16 = 2 * (j & 3);
+                        *reinterpret_cast<uint4*>(row + ((c16 ^ (r & 7)) << 4)) = h0;
+                        *reinterpret_cast<uint4*>(row + (((c16 + 1) ^ (r & 7)) << 4)) = h1;
+                    }
+                };
                 bool oke = true;
                 if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmpty + sb), ((k / NB) - 1) & 1, p.err, abort_flag);
-                if (tc::bar_any(3, 64, !oke)) break;
-                unsigned char* dst = stages + sb * tc::STAGE;
-                for (int i = ct; i < 2 * TM * (D / 16); i += 64) {  // 16-code chunks: [K | V][row][8]
-                    const int v = i / (TM * (D / 16)), r = (i / (D / 16)) % TM, j = i % (D / 16);
-                    const uint4 u = *reinterpret_cast<const uint4*>(st8 + v * TM * D + r * D + j * 16);
-                    const uint32_t a[4] = {u.x ^ 0x80808080u, u.y ^ 0x80808080u, u.z ^ 0x80808080u,
-                                           u.w ^ 0x80808080u};
-                    const uint4 h0 = make_uint4(tc::codes_to_h2(a[0], 0x4140), tc::codes_to_h2(a[0], 0x4342),
-                                                tc::codes_to_h2(a[1], 0x4140), tc::codes_to_h2(a[1], 0x4342));
-                    const uint4 h1 = make_uint4(tc::codes_to_h2(a[2], 0x4140), tc::codes_to_h2(a[2], 0x4342),
-                                                tc::codes_to_h2(a[3], 0x4140), tc::codes_to_h2(a[3], 0x4342));
-                    // fp16 columns 16 j .. 16 j + 15: box j / 4, 16-byte chunks 2 (j % 4) and 2 (j % 4) + 1
-                    unsigned char* row = dst + v * 2 * KB + (j >> 2) * KB + r * 128;
-                    const int c16 = 2 * (j & 3);
-                    *reinterpret_cast<uint4*>(row + ((c16 ^ (r & 7)) << 4)) = h0;
-                    *reinterpret_cast<uint4*>(row + (((c16 + 1) ^ (r & 7)) << 4)) = h1;
-                }
-                for (int i = ct; i < 2 * TM; i += 64) scl[sb * 2 * TM + i] = ssc[i];
+                // (the barrier also makes the appended rows visible to both warps)
+                if (tc::bar_any(3, NCV, !oke)) break;
+                convert(0);
+                for (int i = ct; i < 2 * TM; i += NCV) scl[(k & 3) * 2 * TM + i] = ssc[i];  // K and V scales
                 fence_proxy_async_smem();  // the MMAs read the stage through the async proxy
-                tc::named_bar_sync(3, 64);
+                tc::named_bar_sync(3, NCV);
                 if (ct == 0) {
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarFull + sb)) : "memory");
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarScale + (k & 3))) : "memory");
+                }
+                if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmptyV + sb), ((k / NB) - 1) & 1, p.err, abort_flag);
+                if (tc::bar_any(3, NCV, !oke)) break;
+                convert(1);
+                fence_proxy_async_smem();
+                tc::named_bar_sync(3, NCV);
+                if (ct == 0) {
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarFullV + sb)) : "memory");
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarEmpty8 + s8)) : "memory");
                 }
                 if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
             }
-        } else if (warp >= 4) {
+        } else if (warp >= 4 && warp < 4 + 4 * SH) {
             // ------------------------------------------------ softmax and output
             // SH groups of four warps; group ch owns query columns [ch * GH, (ch + 1) * GH)
             // and thread r of a group owns row r of S (TMEM lane r) and dimension r of O.
@@ -859,8 +888,9 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 // ---- scores of this tile ----
                 bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag);
                 // INT8: the scales of the tile come from the converting warps; waiting on
-                // their publication (complete by now) orders those writes before the reads
-                if constexpr (I8) oks = oks && tc::wait_or_abort(bar(kBarFull + k % NB), (k / NB) & 1, p.err, abort_flag);
+                // their publication orders those writes before the reads.  (Slot k % 4 is
+                // published again for tile k + 4 only after this softmax has issued P(k).)
+                if constexpr (I8) oks = oks && tc::wait_or_abort(bar(kBarScale + (k & 3)), (k >> 2) & 1, p.err, abort_flag);
                 if (tc::bar_any(2, SMX, !oks)) break;
                 tc::tc_fence_after();
                 __syncwarp();
@@ -875,8 +905,8 @@ __global__ void __launch_bounds__(tc::threads_for(G), 1)
                 bool need = false;  // a visible score above the column's reference by more than the margin
                 float ksr = 1.f, vsr = 1.f;
                 if constexpr (I8) {
-                    ksr = scl[(k % NB) * 2 * TM + r];
-                    vsr = scl[(k % NB) * 2 * TM + TM + r];
+                    ksr = scl[(k & 3) * 2 * TM + r];
+                    vsr = scl[(k & 3) * 2 * TM + TM + r];
                 }
 #pragma unroll
                 for (int jj = 0; jj < GH; ++jj) {
@@ -1065,14 +1095,14 @@ struct TcKernelInfo {
     int smem;
     int slot_floats;
     int G;
-    int threads;  // threads per CTA (tc::threads_for(G))
+    int threads;  // threads per CTA (tc::threads_for)
 };
 
 template <typename CT, int G, bool MQ>
 TcKernelInfo tc_kernel_info() {
     using LY = tc::Layout<G, std::is_same_v<CT, int8_t>>;
     return TcKernelInfo{reinterpret_cast<const void*>(&decode_gqa_tc_kernel<CT, G, MQ>), LY::SMEM, LY::SLOT, G,
-                        tc::threads_for(G)};
+                        tc::threads_for(G, std::is_same_v<CT, int8_t>)};
 }
 
 TcKernelInfo select_tc(bool bf16, int G, bool multi_token);
