@@ -46,7 +46,7 @@ KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
 OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("13b", dict(page_size=256)),
                 ("70b", dict(out_dtype="bf16")), ("70b", dict(window=1024)), ("70b", dict(page_size=256)),
                 ("int8", dict(page_size=256)), ("7b", dict(q_len=4)), ("7b", dict(q_len=8)),
-                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)), ("mqa", {})]
+                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)), ("mqa", {}), ("70b_i8", {})]
 
 
 def kernel_name(w, q_len=1) -> str:

@@ -16,20 +16,24 @@
 // so each product keeps about 16 mantissa bits of the fp32 operand; the
 // accumulators are fp32 in TMEM and hi + lo are summed when read back.
 //
-// Roles (256 threads, one CTA per SM, persistent):
+// Roles (one persistent CTA per SM; 256, 384 or 640 threads for blocks of
+// 4, 8 or 16 query columns, 512 for INT8 caches):
 //   warp 0  bulk tensor copies (TMA, 128B swizzle) of K and V tiles into a
-//           3-stage ring;
+//           3-stage ring (INT8: raw codes and scales into a 2-stage ring);
 //   warp 1  TMEM allocation, the append and the tcgen05.mma issue: its lanes
 //           wait for every staged tile in order; in the last tile of a segment
 //           they write k' = k_new + b_k (and v') rounded to the cache type into
 //           the cache and into the staged tile and zero the staged V rows past
 //           the sequence end (so 0 * garbage never reaches the product), then
 //           lane 0 issues the MMAs;
-//   warps 4-7 (128 threads) the online softmax: thread i owns row i of S and
-//           dimension i of O; they build Qs, read S from TMEM, keep the
-//           running max / sum per head, write Ps, rescale-and-add O, and at
-//           the end of a piece write the output or a split-K partial, merged
-//           by the last piece exactly as in the CUDA-core kernel.
+//   warps 2-3 and 12-15 (INT8 only) the append of quantised rows and the
+//           conversion of the codes into fp16 operand stages;
+//   warps 4.. the online softmax in groups of four warps that split the query
+//           columns: thread i of a group owns row i of S and dimension i of O;
+//           they build Qs, read S from TMEM, keep the running max / sum per
+//           head, write Ps, rescale-and-add O, and at the end of a piece write
+//           the output or a split-K partial, merged by the last piece exactly as
+//           in the CUDA-core kernel.
 // Work split: the same balanced contiguous ranges of a global tile space as
 // ftd_decode_splitk.cuh, with 128-row tiles and one CTA per worker.
 #pragma once

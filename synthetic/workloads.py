@@ -81,6 +81,10 @@ WORKLOADS = {
         "70b", B=16, Hq=64, Hkv=8, D=128, Lmax=8192, qkv_dtype="bf16", cache_dtype="bf16",
         lens=("fixed", 8191), seed=3,
         description="70B-shaped GQA decode: B16 Hq64 Hkv8 D128, context 8192, bf16"),
+    "70b_i8": Workload(
+        "70b_i8", B=16, Hq=64, Hkv=8, D=128, Lmax=8192, qkv_dtype="f16", cache_dtype="i8",
+        lens=("fixed", 8191), scale_range=(0.01, 0.05), seed=6,
+        description="70B-shaped GQA decode with an INT8 cache: B16 Hq64 Hkv8 D128, context 8192, fp16 q"),
     "mqa": Workload(
         "mqa", B=64, Hq=64, Hkv=1, D=128, Lmax=4096, qkv_dtype="bf16", cache_dtype="bf16",
         lens=("fixed", 4095), seed=5,

@@ -299,10 +299,10 @@ def test_host_entry_point_lengths_change_between_calls():
 # ------------------------------------------------------------- full size
 SAMPLED = {"7b": [(0, 0), (3, 17), (7, 31)], "13b": [(0, 5), (11, 39), (31, 0), (17, 22)],
            "70b": [(0, 0), (5, 37), (15, 63)], "int8": [(0, 1), (33, 30), (63, 31)],
-           "mqa": [(0, 0), (21, 17), (63, 63)]}
+           "mqa": [(0, 0), (21, 17), (63, 63)], "70b_i8": [(0, 0), (7, 40), (15, 63)]}
 
 
-@pytest.mark.parametrize("name", ["7b", "13b", "70b", "int8", "mqa"])
+@pytest.mark.parametrize("name", ["7b", "13b", "70b", "int8", "mqa", "70b_i8"])
 def test_full_size_workload_sampled(name):
     """Full-size workloads in the launch configuration the bench times; the oracle checks
     sampled (slot, head) outputs one slot at a time, and every appended row bit for bit."""
