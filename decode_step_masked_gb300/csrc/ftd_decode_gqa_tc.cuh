@@ -734,8 +734,11 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                 // fastest across the threads: with both layouts swizzled, the eight
                 // rows a quarter-warp touches fall in distinct banks.
                 unsigned char* dst = stages + sb * tc::STAGE;
+                // (Not unrolled: with four roles' loops sharing each SM sub-partition's
+                // instruction cache, the unrolled copy stalled on instruction fetch and
+                // cost 30 % of the step.)
                 auto convert = [&](int v) {
-#pragma unroll 4
+#pragma unroll 1
                     for (int i = ct; i < TM * (D / 16); i += NCV) {
                         const int r = i % TM, j = i / TM;
                         const uint4 u =
