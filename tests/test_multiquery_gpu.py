@@ -164,6 +164,7 @@ def test_multi_token_paged_across_pages(cc):
 # every option at once: paged cache, sliding window, several tokens per step, half output
 COMBINED = {
     "i8_cc": ("i8", "f16", 3, 8, 8, 128, 512, [126, 0, 380], 3, False),
+    "i8_tc": ("i8", "f16", 3, 16, 4, 128, 1024, [126, 700, 1000], 2, False),  # 8 rows: INT8 tensor cores
     "bf16_tc": ("bf16", "bf16", 3, 32, 4, 128, 1024, [126, 700, 1000], 2, False),
     "bf16_cc": ("bf16", "bf16", 3, 32, 4, 128, 1024, [126, 700, 1000], 2, True),
     "f16_mha_tc": ("f16", "f16", 2, 4, 4, 128, 512, [250, 100], 4, False),
