@@ -339,6 +339,38 @@ def oracle_timing(w, seconds: float, nthreads: int, seed: int = 0):
     return dict(gbs=done_bytes / elapsed / 1e9, slots=slots, seconds=elapsed, bytes=done_bytes)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    import platform
+    import subprocess
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for line in r.stdout.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
+def brute_tiny_ms() -> float:
+    """Milliseconds of one tiny-workload step of the pure-Python brute force (oracle/brute.py)."""
+    from oracle import brute
+    from synthetic import gen_all
+    w = WORKLOADS["tiny"]
+    inp = gen_all(w)
+    t0 = time.perf_counter()
+    brute.decode_step(w, inp)
+    return (time.perf_counter() - t0) * 1e3
+
+
 def oracle_one_head_seconds(w, nthreads=1) -> float:
     import oracle
     from synthetic import gen_all
@@ -528,10 +560,16 @@ def main():
         # ---- the float64 oracle on the host cores ----
         cores = os.cpu_count() or 1
         cb = oracle_timing(w, 10.0, cores)
+        c1 = oracle_timing(w, 3.0, 1)  # the same oracle on one core
         line["cpu_baseline"] = dict(value=cb["gbs"], unit="GB/s", cores=cores, kind="oracle",
                                     sample=f"{cb['slots']} whole slot(s) of the {w.name} workload "
                                            f"({cb['bytes'] / 1e6:.0f} MB of KV) in {cb['seconds']:.1f} s, "
-                                           f"OpenMP over (slot, head)")
+                                           f"OpenMP over (slot, head)",
+                                    cpu_model=cpu_model(),
+                                    single_thread=dict(value=c1["gbs"], unit="GB/s", cores=1,
+                                                       sample=f"{c1['slots']} whole slot(s) in "
+                                                              f"{c1['seconds']:.1f} s"),
+                                    brute_tiny_ms=brute_tiny_ms())
     elif rank == 0:
         line["e2e"] = None
     if rank == 0:

@@ -118,3 +118,9 @@ def test_reduce_over_two_gloo_ranks():
 
 def test_reduce_single_rank_is_identity():
     assert bench.reduce_over_ranks(3.0, 7.0, 1) == (3.0, 7.0)
+
+
+def test_cpu_baseline_helpers():
+    """The CPU baseline records the host CPU's model and times the brute force on the tiny step."""
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+    assert bench.brute_tiny_ms() > 0.0
