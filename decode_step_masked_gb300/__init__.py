@@ -30,9 +30,9 @@ FTD_F32, FTD_F16, FTD_BF16, FTD_I8 = 0, 1, 2, 3
 DTYPES = {"f32": FTD_F32, "f16": FTD_F16, "bf16": FTD_BF16, "i8": FTD_I8}
 
 # Symbols include/ftd.h declares; the loader checks each one is exported.
-EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_paged", "ftd_decode_mha_host",
-           "ftd_get_error", "ftd_destroy", "ftd_status_str", "ftd_last_error", "ftd_kernel_launches",
-           "ftd_decode_mha_noalloc")
+EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_current", "ftd_decode_mha_paged",
+           "ftd_decode_mha_host", "ftd_get_error", "ftd_destroy", "ftd_status_str", "ftd_last_error",
+           "ftd_kernel_launches", "ftd_decode_mha_noalloc")
 
 
 class FtdConfig(ctypes.Structure):
@@ -73,6 +73,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     for fn in (lib.ftd_decode_mha, lib.ftd_decode_mha_host):
         fn.argtypes = [P] * 11
         fn.restype = I
+    lib.ftd_decode_mha_current.argtypes = [P] * 10
+    lib.ftd_decode_mha_current.restype = I
     lib.ftd_decode_mha_paged.argtypes = [P] * 12
     lib.ftd_decode_mha_paged.restype = I
     lib.ftd_get_error.argtypes = [P]
@@ -125,6 +127,11 @@ def _ptrs(*xs):
 def ftd_decode_mha(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out, stream) -> int:
     return load_library().ftd_decode_mha(*_ptrs(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens,
                                                 scales, out, stream))
+
+
+def ftd_decode_mha_current(q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out, stream) -> int:
+    return load_library().ftd_decode_mha_current(*_ptrs(q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens,
+                                                        scales, out, stream))
 
 
 def ftd_decode_mha_paged(ctx, q, k_new, v_new, qkv_bias, k_pages, v_pages, block_table, seq_lens, scales, out,

@@ -24,6 +24,7 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
+std::atomic<ftd_ctx*> g_current{nullptr};  // the most recently initialised live context
 
 ftd_status fail(ftd_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ftd_status fail(ftd_status s, const char* fmt, ...) {
@@ -328,6 +329,7 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
         return cuda_fail(e, "cudaMemsetAsync of the cache pool");
     }
     *out = ctx;
+    g_current.store(ctx);
     return FTD_OK;
 }
 
@@ -448,6 +450,14 @@ ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const 
                          static_cast<cudaStream_t>(stream));
 }
 
+ftd_status ftd_decode_mha_current(const void* q, const void* k_new, const void* v_new, const void* qkv_bias,
+                                  void* k_cache, void* v_cache, const int32_t* seq_lens, float* scales, void* out,
+                                  void* stream) {
+    ftd_ctx* ctx = g_current.load();
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_current: no context (ftd_init first)");
+    return ftd_decode_mha(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out, stream);
+}
+
 ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                 const void* qkv_bias, void* k_pages, void* v_pages, const int32_t* block_table,
                                 const int32_t* seq_lens, float* scales, void* out, void* stream) {
@@ -555,6 +565,8 @@ ftd_status ftd_get_error(ftd_ctx* ctx) {
 
 void ftd_destroy(ftd_ctx* ctx) {
     if (!ctx) return;
+    ftd_ctx* expected = ctx;
+    g_current.compare_exchange_strong(expected, nullptr);
     cudaDeviceSynchronize();
     cudaFree(ctx->pool);
     delete ctx;

@@ -169,6 +169,17 @@ ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const 
                           const int32_t* seq_lens, float* scales, void* out, void* stream);
 
 /*
+ * ftd_decode_mha_current -- ftd_decode_mha with the specified ten-argument
+ * signature (no context handle): it runs on the most recently initialised
+ * context that has not been destroyed, and returns FTD_ERR_INVALID_ARG when
+ * there is none.  For a process that holds one context; with several, pass
+ * the handle to ftd_decode_mha instead.
+ */
+ftd_status ftd_decode_mha_current(const void* q, const void* k_new, const void* v_new, const void* qkv_bias,
+                                  void* k_cache, void* v_cache, const int32_t* seq_lens, float* scales,
+                                  void* out, void* stream);
+
+/*
  * ftd_decode_mha_paged -- ftd_decode_mha over a paged cache (intelliparadigm.com
  * section 5.1, framerc.cn section 3.2: the cache is cut into fixed-size pages
  * and a block table maps each slot's positions to pages, so the pool holds

@@ -91,6 +91,9 @@ def test_null_arguments(lib):
     assert ftd.ftd_get_error(0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_cache_ptrs(0)[0] == ftd.FTD_ERR_INVALID_ARG
     ftd.ftd_destroy(0)  # no-op
+    # without a live context the handle-free entry point refuses (no context exists on a CPU host)
+    assert ftd.ftd_decode_mha_current(16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
+    assert "no context" in ftd.ftd_last_error()
 
 
 def test_no_launches_from_host_failures(lib):

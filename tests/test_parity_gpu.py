@@ -236,6 +236,33 @@ def test_maximum_batch(cache, Hq, Hkv):
     check_step(w, inp, what=f"1024 slots {cache} Hq{Hq} Hkv{Hkv}")
 
 
+def test_current_context_entry_point():
+    """ftd_decode_mha_current (the specified ten-argument call) runs on the most recently
+    initialised context and gives the same bytes as ftd_decode_mha on it; after that context
+    is destroyed it refuses."""
+    import torch
+    w, inp = small("bf16", "bf16", B=3, Hq=16, Hkv=2, D=128, Lmax=256, lens=[0, 130, 255])
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    q, kn, vn, bias, sl = (dev(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens"))
+    outs, caches = [], []
+    for current in (False, True):
+        kc, vc = dev(inp["k_cache"]), dev(inp["v_cache"])
+        out = torch.full((w.B, w.Hq, w.D), float("nan"), dtype=torch.float32, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        args = (q.data_ptr(), kn.data_ptr(), vn.data_ptr(), bias.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+                sl.data_ptr(), 0, out.data_ptr(), s)
+        st = ftd.ftd_decode_mha_current(*args) if current else ftd.ftd_decode_mha(step.ctx, *args)
+        ftd.check(st)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+        caches.append(kc.cpu().numpy())
+    assert step.get_error() == ftd.FTD_OK
+    assert_same_bytes(outs[1], outs[0], "ftd_decode_mha_current output")
+    assert_same_bytes(caches[1], caches[0], "ftd_decode_mha_current append")
+    step.close()
+    assert ftd.ftd_decode_mha_current(0, 0, 0, 0, 0, 0, 0, 0, 0, 0) == ftd.FTD_ERR_INVALID_ARG
+
+
 def test_host_entry_point_with_pinned_buffers():
     """Pinned host buffers take the direct path (one launch that reads the inputs in place and
     writes the output to the host); the result matches the oracle and the caches get the
