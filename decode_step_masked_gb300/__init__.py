@@ -121,7 +121,10 @@ def ftd_cache_ptrs(ctx: int):
 
 
 def _ptrs(*xs):
-    return [ctypes.c_void_p(x or None) for x in xs]
+    # Addresses go through as Python ints (or None): the argtypes declare them
+    # c_void_p, and ctypes converts ints itself, without a wrapper object per
+    # argument on the per-step path.
+    return xs
 
 
 def ftd_decode_mha(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out, stream) -> int:
