@@ -30,7 +30,7 @@
  * reads kv head h / (Hq / Hkv)) and an INT8 cache with an fp32 scale per
  * (slot, kv head, position) (pptc.cn section 3.1).
  *
- * Three options the pages name next to the step:
+ * Four options the pages name next to the step:
  *  - out_dtype F16 / BF16: the output is rounded once, to nearest even, from
  *    the fp32 result, in the precision the following projection reads
  *    (lpnh.cn section 2.1: the fused kernels run in half precision).
