@@ -19,6 +19,7 @@
 #include "../../include/ftd.h"
 #include "ftd_decode_splitk.cuh"
 #include "ftd_decode_gqa_tc.cuh"
+#include "ftd_internal.cuh"
 
 namespace {
 
@@ -97,6 +98,38 @@ bool encode_cache_map(CUtensorMap* map, void* base, ftd_dtype dt, size_t rows) {
 }  // namespace
 
 namespace ftd {
+// fp16/bf16 caches with head_dim 128 whose kv heads carry a multiple of 4 query
+// rows (group x new tokens) use the tensor-core kernel, in blocks of 16 or 8
+// rows (blocks of 4 fill half of an 8-column block, since the MMA needs N >= 16
+// with the hi/lo split).  INT8 caches with head_dim 128 and a multiple of 8
+// query rows per kv head use its INT8 variant, in blocks of 8.
+// FTD_FORCE_CUDA_CORE=1 in the environment selects the CUDA-core kernel instead.
+// Internal to the library (hidden), shared by ftd_init and the no-allocation
+// entry point; tki.fn is null when the CUDA-core kernel runs.
+__attribute__((visibility("hidden"))) TcChoice choose_tc(const ftd_config& c) {
+    TcChoice r{};
+    r.nhb = 1;
+    r.qblk = 8;
+    const int rows_q = (c.q_len > 1 ? c.q_len : 1) * (c.n_q_heads / c.n_kv_heads);
+    const char* force = getenv("FTD_FORCE_CUDA_CORE");
+    const bool forced = force && force[0] == '1';
+    const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
+                         rows_q % 4 == 0 && !forced;
+    const bool want_tc_i8 = c.cache_dtype == FTD_I8 && c.head_dim == 128 && rows_q % 8 == 0 && !forced;
+    if ((want_tc || want_tc_i8) && encode_tiled()) {
+        const int Gt = (rows_q % 16 == 0 && !want_tc_i8) ? 16 : 8;
+        r.qblk = rows_q % 8 == 0 ? Gt : 4;
+        r.tki = want_tc_i8 ? select_tc_i8(c.q_len > 1) : select_tc(c.cache_dtype == FTD_BF16, Gt, c.q_len > 1);
+        r.nhb = rows_q / r.qblk;
+    }
+    return r;
+}
+
+__attribute__((visibility("hidden"))) bool encode_tc_cache_map(CUtensorMap* map, void* base, ftd_dtype dt,
+                                                               size_t rows) {
+    return encode_cache_map(map, base, dt, rows);
+}
+
 // Internal to the library (hidden): used by the no-allocation entry point so its
 // failures show in ftd_last_error() and its launches in ftd_kernel_launches().
 __attribute__((visibility("hidden"))) void set_last_error(const char* msg) { g_last_error = msg; }
@@ -235,25 +268,10 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     const size_t cache_bytes = rows * D * elem_bytes(c.cache_dtype);
     const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * rows * sizeof(float) : 0;
 
-    // fp16/bf16 caches with head_dim 128 whose kv heads carry a multiple of 4
-    // query rows (group x new tokens) use the tensor-core kernel, in blocks of
-    // 16 or 8 rows (blocks of 4 fill half of an 8-column block, since the MMA
-    // needs N >= 16 with the hi/lo split).  INT8 caches with head_dim 128 and a
-    // multiple of 8 query rows per kv head use its INT8 variant, in blocks of 8.
-    // FTD_FORCE_CUDA_CORE=1 in the environment at ftd_init selects the CUDA-core
-    // kernel instead.
-    const char* force = getenv("FTD_FORCE_CUDA_CORE");
-    const bool forced = force && force[0] == '1';
-    const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
-                         rows_q % 4 == 0 && !forced;
-    const bool want_tc_i8 = c.cache_dtype == FTD_I8 && c.head_dim == 128 && rows_q % 8 == 0 && !forced;
-    ftd::TcKernelInfo tki{};
-    int tc_nhb = 1, tc_qblk = 8;
-    if ((want_tc || want_tc_i8) && encode_tiled()) {
-        const int Gt = (rows_q % 16 == 0 && !want_tc_i8) ? 16 : 8;
-        tc_qblk = rows_q % 8 == 0 ? Gt : 4;
-        tki = want_tc_i8 ? ftd::select_tc_i8(nq > 1) : ftd::select_tc(c.cache_dtype == FTD_BF16, Gt, nq > 1);
-        tc_nhb = rows_q / tc_qblk;
+    const ftd::TcChoice tcc = ftd::choose_tc(c);
+    const ftd::TcKernelInfo tki = tcc.tki;
+    const int tc_nhb = tcc.nhb, tc_qblk = tcc.qblk;
+    if (tki.fn) {
         e = cudaFuncSetAttribute(tki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tki.smem);
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute (tensor-core kernel)");
     }

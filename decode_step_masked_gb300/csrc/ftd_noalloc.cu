@@ -26,6 +26,7 @@
 
 #include "../../include/ftd.h"
 #include "ftd_decode_splitk.cuh"
+#include "ftd_internal.cuh"
 
 namespace {
 
@@ -100,6 +101,13 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
         default: return reject(FTD_ERR_UNSUPPORTED, "cache_dtype");
     }
     if (!ki.fn) return reject(FTD_ERR_UNSUPPORTED, "no kernel for this configuration");
+    if (static_cast<size_t>(c.max_batch) * c.n_kv_heads * c.max_len >= (static_cast<size_t>(1) << 31))
+        return reject(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit row indices");
+    // the same kernel choice as ftd_init: the tensor-core kernel where it applies
+    const ftd::TcChoice tcc = ftd::choose_tc(c);
+    const bool use_tc = tcc.tki.fn != nullptr;
+    const void* fn = use_tc ? tcc.tki.fn : ki.fn;
+    const int smem = use_tc ? tcc.tki.smem : ki.smem;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
@@ -118,19 +126,20 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
             ds->sms = sms;
             ds->ready = true;
         }
-        if (!ds->configured.count(ki.fn)) {
-            if (cudaFuncSetAttribute(ki.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, ki.smem) != cudaSuccess)
+        if (!ds->configured.count(fn)) {
+            if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
                 return reject(FTD_ERR_CUDA, "cudaFuncSetAttribute failed");
-            ds->configured.insert(ki.fn);
+            ds->configured.insert(fn);
         }
     }
 
     // Scratch layout: [error word | counters | split-K partial slots], 256-byte aligned parts.
-    const size_t n_seg = static_cast<size_t>(c.max_batch) * c.n_kv_heads * nhb;
-    const size_t n_slots = n_seg + static_cast<size_t>(ds->sms) * ki.warps;
+    const size_t n_seg = static_cast<size_t>(c.max_batch) * c.n_kv_heads * (use_tc ? tcc.nhb : nhb);
+    const size_t n_slots = n_seg + static_cast<size_t>(ds->sms) * (use_tc ? 1 : ki.warps);
     const size_t cnt_off = 256;
     const size_t ws_off = cnt_off + (n_seg * sizeof(uint32_t) + 255) / 256 * 256;
-    const size_t need = ws_off + n_slots * static_cast<size_t>(ki.slot_floats) * sizeof(float);
+    const size_t need =
+        ws_off + n_slots * static_cast<size_t>(use_tc ? tcc.tki.slot_floats : ki.slot_floats) * sizeof(float);
     if (need > FTD_NOALLOC_SCRATCH_BYTES) {
         char buf[256];
         snprintf(buf, sizeof buf,
@@ -172,9 +181,22 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
     p.window = c.window;
     p.nq = nq;
 
-    void* args[] = {&p};
-    cudaError_t e = cudaLaunchKernel(ki.fn, dim3(ds->sms), dim3(ki.warps * 32), args,
-                                     static_cast<size_t>(ki.smem), s);
+    cudaError_t e;
+    if (use_tc) {
+        // tensor maps of the caller's caches, encoded per call on the host (no allocation)
+        CUtensorMap tmk, tmv;
+        const size_t rows = static_cast<size_t>(c.max_batch) * c.n_kv_heads * c.max_len;
+        if (!ftd::encode_tc_cache_map(&tmk, k_cache, c.cache_dtype, rows) ||
+            !ftd::encode_tc_cache_map(&tmv, v_cache, c.cache_dtype, rows))
+            return reject(FTD_ERR_CUDA, "cuTensorMapEncodeTiled failed for the caches");
+        p.nhb = tcc.nhb;
+        p.qblk = tcc.qblk;
+        void* args[] = {&tmk, &tmv, &p};
+        e = cudaLaunchKernel(fn, dim3(ds->sms), dim3(tcc.tki.threads), args, static_cast<size_t>(smem), s);
+    } else {
+        void* args[] = {&p};
+        e = cudaLaunchKernel(fn, dim3(ds->sms), dim3(ki.warps * 32), args, static_cast<size_t>(smem), s);
+    }
     if (e != cudaSuccess) return reject(FTD_ERR_CUDA, cudaGetErrorString(e));
     ftd::note_launch();
     return FTD_OK;

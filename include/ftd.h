@@ -267,9 +267,9 @@ uint64_t ftd_kernel_launches(void);
  *   stream           : cudaStream_t as void*.
  *
  * It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- * It always runs the CUDA-core split-K kernel (the tensor-core kernel needs
- * tensor maps of the cache, which a context caches).  Its results match
- * ftd_decode_mha's within the same bounds; grouped caches are slower here.
+ * It runs the kernel ftd_decode_mha would run for the same config; for the
+ * tensor-core kernel it encodes the caches' tensor maps on the host at every
+ * call (a context caches them), so its results are ftd_decode_mha's bytes.
  * Its split-K partials, counters and error word live in one static device
  * array of FTD_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the
  * library holds until the process exits.  A configuration that needs more

@@ -118,3 +118,37 @@ def test_noalloc_with_window_half_output_and_several_tokens():
     assert np.max(np.abs(outs[0] - outs[1])) <= 1e-2
     assert np.array_equal(caches[0][0], caches[1][0])
     assert np.array_equal(caches[0][1].view(np.uint32), caches[1][1].view(np.uint32))  # NaN fill past the lengths
+
+
+def test_noalloc_int8_grouped_runs_the_tensor_core_kernel():
+    """A grouped INT8 cache (8 query rows per kv head) runs the same tensor-core kernel as the
+    context path: identical output, appended codes and scales."""
+    import torch
+    w = Workload("noalloc", B=4, Hq=16, Hkv=2, D=128, Lmax=1024, qkv_dtype="f16", cache_dtype="i8", bias_std=0.1,
+                 seed=25)
+    inp = gen_all(w, seed=25, seq_lens=np.array([1000, 0, 129, 511], np.int32), fill_beyond="nan")
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    cfg = ftd.FtdConfig(w.B, w.Hq, w.Hkv, w.D, w.Lmax, ftd.FTD_F16, ftd.FTD_I8, 0.0)
+    s = torch.cuda.current_stream().cuda_stream
+    q, kn, vn, bias, sl = (dev(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens"))
+    outs, caches = [], []
+    for use_noalloc in (False, True):
+        kc, vc, sc = dev(inp["k_cache"]), dev(inp["v_cache"]), dev(inp["scales"])
+        out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+        if use_noalloc:
+            err = torch.zeros(1, dtype=torch.int32, device="cuda")
+            st = ftd.ftd_decode_mha_noalloc(cfg, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), bias.data_ptr(),
+                                            kc.data_ptr(), vc.data_ptr(), sl.data_ptr(), sc.data_ptr(),
+                                            out.data_ptr(), err.data_ptr(), s)
+            assert st == ftd.FTD_OK, ftd.ftd_last_error()
+        else:
+            step(q, kn, vn, sl, out, bias=bias, k_cache=kc, v_cache=vc, scales=sc)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy())
+        caches.append((kc.cpu().numpy(), vc.cpu().numpy(), sc.cpu().numpy()))
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+    assert np.all(np.isfinite(outs[1]))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert np.array_equal(caches[0][0], caches[1][0]) and np.array_equal(caches[0][1], caches[1][1])
+    assert np.array_equal(caches[0][2].view(np.uint32), caches[1][2].view(np.uint32))
