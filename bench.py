@@ -1,6 +1,6 @@
 """Benchmark of the decode step: KV-read GB/s (fraction of HBM peak) and µs per step.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 7b|13b|70b|int8|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 13b|7b|70b|int8|tiny|...]
     python bench.py --impl reference ...   # the float64 CPU oracle as the reference arm
 
 One step is one ``ftd_decode_mha`` call: bias add, KV append, scores, softmax,
@@ -8,7 +8,13 @@ P.V and the split-K merge for every slot of the batch.  Inputs are synthetic
 (seeded, the workload shapes of the decode step's pages) and resident in HBM
 before timing starts.  Consecutive steps rotate between cache pools whose
 combined size is several times the 129 MB L2, so each step streams its KV
-cache from HBM.  Rank 0 prints one JSON line.
+cache from HBM.  The default workload is the largest one, the 13B-shaped
+ragged continuous batch.  Rank 0 prints one JSON line.
+
+Every workload is timed two ways: back to back (graph-replayed steps; each
+step may start while the previous one drains), and isolated (each step follows
+a 320 MB device copy on the same stream, as a decode step follows the
+projection kernels in a model, so it starts cold, with nothing of it in L2).
 
 With ``--gpus N`` under torchrun every rank runs an independent replica (its
 own batch; the decode step needs no collective), ``value`` is the aggregate of
@@ -52,7 +58,7 @@ OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("1
 def kernel_name(w, q_len=1) -> str:
     """The kernel one step of workload ``w`` runs (the library's own selection rule)."""
     rows = max(1, q_len) * w.Hq // w.Hkv
-    tc = (w.D == 128 and os.environ.get("FTD_FORCE_CUDA_CORE", "0") != "1"
+    tc = (w.D == 128
           and ((w.cache_dtype in ("f16", "bf16") and rows % 4 == 0) or (w.cache_dtype == "i8" and rows % 8 == 0)))
     return "decode_gqa_tc_kernel" if tc else "decode_splitk_kernel"
 
@@ -171,14 +177,11 @@ def n_pools_for(w, kv_bytes):
     return int(max(2, min(4, np.ceil(300e6 / kv_bytes) + 1)))
 
 
-def run_timed(step, w, pools, inp, steps, warmup, stream, chunk=100):
-    """W untimed steps, then exactly K steps timed with CUDA events on the launching stream.
+FLUSH_BYTES = 160 << 20  # each isolated step follows a copy of this many bytes (320 MB of traffic)
 
-    The K steps are replayed from CUDA graphs of ``chunk`` captured steps (plus
-    one graph for the remainder), the pattern the pages recommend for the
-    fixed-shape decode loop, so host launch latency does not starve the GPU.
-    """
-    import torch
+
+def decode_call(step, pools, inp, stream):
+    """A function that issues step i on ``stream`` (cache pool i mod the pool count)."""
     import decode_step_masked_gb300 as ftd
     n = len(pools)
 
@@ -192,6 +195,44 @@ def run_timed(step, w, pools, inp, steps, warmup, stream, chunk=100):
             ftd.check(ftd.ftd_decode_mha_paged(step.ctx, *common, inp["block_table"].data_ptr(), *tail))
         else:
             ftd.check(ftd.ftd_decode_mha(step.ctx, *common, *tail))
+    return one
+
+
+def run_isolated(step, pools, inp, n, stream, flush):
+    """n steps, each preceded on the same stream by a device copy larger than 2x L2
+    (flush = (src, dst) byte tensors).  The copy is not a decode launch, so the step
+    cannot overlap a previous step, and it evicts the step's inputs from L2.  Each
+    step is timed alone with CUDA events recorded right before and after it.
+    Returns the per-step times in µs."""
+    import torch
+    import decode_step_masked_gb300 as ftd
+    one = decode_call(step, pools, inp, stream)
+    src, dst = flush
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for i in range(3):  # warm-up
+            dst.copy_(src)
+            one(i)
+        for i, (e0, e1) in enumerate(evs):
+            dst.copy_(src)
+            e0.record(stream)
+            one(i)
+            e1.record(stream)
+    torch.cuda.synchronize()
+    ftd.check(step.get_error())
+    return np.array([e0.elapsed_time(e1) * 1e3 for e0, e1 in evs])
+
+
+def run_timed(step, w, pools, inp, steps, warmup, stream, chunk=100):
+    """W untimed steps, then exactly K steps timed with CUDA events on the launching stream.
+
+    The K steps are replayed from CUDA graphs of ``chunk`` captured steps (plus
+    one graph for the remainder), the pattern the pages recommend for the
+    fixed-shape decode loop, so host launch latency does not starve the GPU.
+    """
+    import torch
+    import decode_step_masked_gb300 as ftd
+    one = decode_call(step, pools, inp, stream)
 
     def capture(nsteps):
         g = torch.cuda.CUDAGraph()
@@ -443,11 +484,13 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", window=0, page_size=0, q_len=1):
+def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", window=0, page_size=0, q_len=1,
+                   flush=None, isolated=0):
     """Time one workload; the options select a half-precision output, a sliding
     window, a paged cache (one shuffled block table shared by the rotated pools)
     or several new tokens per slot (the cached lengths drop by q_len - 1 so the
-    step's last position stays where the plain workload's is)."""
+    step's last position stays where the plain workload's is).  With flush and
+    isolated > 0, also time that many isolated steps (run_isolated)."""
     import torch
     import decode_step_masked_gb300 as ftd
     w = WORKLOADS[name]
@@ -463,9 +506,29 @@ def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", w
     step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, out_dtype=out_dtype,
                           window=window, page_size=page_size, num_pages=num_pages, q_len=q_len)
     r = run_timed(step, w, pools, inp, steps, warmup, stream)
+    if isolated and flush is not None:
+        r["isolated_us"] = run_isolated(step, pools, inp, isolated, stream, flush)
     step.close()
     us = r["total_ms"] * 1e3 / steps
     return w, lens, by, pools, inp, r, us
+
+
+def roofline(w, by, r, us, peaks, q_len=1):
+    """The roofline record of one workload: algorithmic bytes of one launch over its
+    measured time, back to back and isolated, against the measured copy peak, with
+    the DRAM traffic of a committed ncu capture of the same kernel source."""
+    per = r["per_us"]
+    d = dict(bound="hbm", achieved=by["total"] / (us * 1e-6) / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
+             frac=by["total"] / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], traffic=load_traffic(w.name),
+             peak_source=f"{peaks['source']} (STREAM-style copy)", kernel=kernel_name(w, q_len),
+             bytes_per_launch=by["total"], launch_us=us, p50_us=float(np.median(per)),
+             p99_us=float(np.percentile(per, 99)), p_note="per-step means of 100-step graph replays")
+    iso = r.get("isolated_us")
+    if iso is not None and len(iso):
+        med = float(np.median(iso))
+        d.update(isolated_us=med, isolated_p99_us=float(np.percentile(iso, 99)), isolated_steps=len(iso),
+                 isolated_frac=by["total"] / (med * 1e-6) / 1e9 / peaks["hbm_gbs"])
+    return d
 
 
 def main():
@@ -473,14 +536,18 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=100)
-    ap.add_argument("--config", default="7b", choices=sorted(WORKLOADS))
+    ap.add_argument("--config", default="13b", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ftd", choices=["ftd", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip per-config, e2e and CPU-baseline legs")
+    ap.add_argument("--isolated", type=int, default=200, help="isolated steps timed per workload")
     ap.add_argument("--ncu-launches", type=int, default=0,
                     help="profiling mode: launch N untimed steps of --config on one cache pool, print nothing")
+    ap.add_argument("--ncu-batch", type=int, default=0,
+                    help="profiling mode: only the first B slots of the workload (a smaller capture)")
+    ap.add_argument("--ncu-window", type=int, default=0, help="profiling mode: sliding window W")
     args = ap.parse_args()
     if args.ncu_launches:
-        return profile_launches(args.config, args.ncu_launches)
+        return profile_launches(args.config, args.ncu_launches, args.ncu_batch, args.ncu_window)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
@@ -498,6 +565,10 @@ def main():
     ftd.load_library()
     stream = torch.cuda.Stream(device=device)
     peaks = load_peaks()
+    # the isolated steps' predecessor: a device copy of FLUSH_BYTES (> 2x L2 of traffic)
+    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device),
+             torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device))
+    flush[0].fill_(1)
 
     # ---- headline: the named workload, K timed steps ----
     sampler = ClockSampler(gpu_id_for(local))
@@ -513,8 +584,6 @@ def main():
     value = units / (max_ms * 1e-3) / 1e9
     per = r["per_us"]
     kern_us = r["total_ms"] * 1e3 / args.steps
-    achieved = by["total"] / (kern_us * 1e-6) / 1e9
-    traffic = load_traffic(w.name)
     line = dict(
         metric=METRIC, value=value, unit="GB/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
         ms_per_step=max_ms / args.steps, us_per_step=max_ms / args.steps * 1e3,
@@ -525,25 +594,30 @@ def main():
                     cache_dtype=w.cache_dtype, qkv_dtype=w.qkv_dtype, context_tokens=by["ctx"],
                     kv_bytes_per_step=by["kv"], l2="caches rotated over %d pools of %.0f MB each (> L2 129 MB)"
                     % (len(pools), by["kv"] / 1e6), parallelism=f"replicas x{world}"),
-        roofline=dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
-                      frac=achieved / peaks["hbm_gbs"], traffic=traffic,
-                      peak_source=f"{peaks['source']} (STREAM-style copy)", kernel=kernel_name(w),
-                      bytes_per_launch=by["total"], launch_us=kern_us),
         gpu_launches=int(r["launches"]), clocks=clocks)
+    if rank == 0 and args.isolated > 0:
+        # the headline's isolated steps, after its timed region (outside the clock window)
+        step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+        r["isolated_us"] = run_isolated(step, pools, inp, args.isolated, stream, flush)
+        step.close()
+    line["roofline"] = roofline(w, by, r, kern_us, peaks)
     del pools
 
     if rank == 0 and not args.no_extras:
         # ---- end to end through the host-buffer entry point ----
         line["e2e"] = e2e_leg(w, lens, by, device, stream, min(args.steps, 2000))
-        # ---- every large workload of the suite, same protocol ----
+        # ---- every large workload of the suite, same protocol, each with its roofline ----
         per_cfg = {}
         for name in ("7b", "13b", "70b", "int8", "tiny"):
             if name == w.name:
-                per_cfg[name] = dict(us=line["us_per_step"], gbs=value / world, frac=value / world / peaks["hbm_gbs"])
+                per_cfg[name] = dict(us=line["us_per_step"], gbs=value / world, frac=value / world / peaks["hbm_gbs"],
+                                     kv_mb=by["kv"] / 1e6, roofline=line["roofline"])
                 continue
-            w2, _, by2, pools2, _, r2, us2 = measure_config(name, 1000, 50, 99, device, stream)
+            w2, _, by2, pools2, _, r2, us2 = measure_config(name, 1000, 50, 99, device, stream, flush=flush,
+                                                            isolated=args.isolated)
             per_cfg[name] = dict(us=us2, us_median=float(np.median(r2["per_us"])), gbs=by2["kv"] / us2 / 1e3,
-                                 frac=by2["kv"] / us2 / 1e3 / peaks["hbm_gbs"], kv_mb=by2["kv"] / 1e6)
+                                 frac=by2["kv"] / us2 / 1e3 / peaks["hbm_gbs"], kv_mb=by2["kv"] / 1e6,
+                                 roofline=roofline(w2, by2, r2, us2, peaks))
             del pools2
             torch.cuda.empty_cache()
         line["per_config"] = per_cfg
@@ -578,17 +652,21 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def profile_launches(name, n):
-    """N plain launches of one workload on one cache pool (for ncu captures of a single launch)."""
+def profile_launches(name, n, batch=0, window=0):
+    """N plain launches of one workload on one cache pool (for ncu captures of a single launch);
+    batch > 0 keeps only the workload's first slots (their seeded lengths), for a smaller capture."""
     import torch
     import decode_step_masked_gb300 as ftd
     w = WORKLOADS[name]
     lens = gen_seq_lens(w)
+    if batch:
+        w = w.with_(B=batch)
+        lens = lens[:batch]
     device = torch.device("cuda", 0)
     ftd.build_library()
     kc, vc, sc = make_pools(w, 1, 5, device)[0]
     inp = make_step_inputs(w, lens, 5, device)
-    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, window=window)
     for _ in range(n):
         step(inp["q"], inp["k_new"], inp["v_new"], inp["seq_lens"], inp["out"], bias=inp["bias"], k_cache=kc,
              v_cache=vc, scales=sc)

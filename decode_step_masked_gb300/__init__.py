@@ -27,12 +27,13 @@ FTD_ERR_DEVICE_TIMEOUT = 6
 FTD_ERR_BAD_PAGE = 7
 
 FTD_F32, FTD_F16, FTD_BF16, FTD_I8 = 0, 1, 2, 3
+FTD_KERNEL_AUTO, FTD_KERNEL_CUDA_CORE = 0, 1
 DTYPES = {"f32": FTD_F32, "f16": FTD_F16, "bf16": FTD_BF16, "i8": FTD_I8}
 
 # Symbols include/ftd.h declares; the loader checks each one is exported.
 EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_current", "ftd_decode_mha_paged",
            "ftd_decode_mha_host", "ftd_get_error", "ftd_destroy", "ftd_status_str", "ftd_last_error",
-           "ftd_kernel_launches", "ftd_decode_mha_noalloc")
+           "ftd_kernel_launches", "ftd_decode_mha_noalloc", "ftd_debug_stall_next")
 
 
 class FtdConfig(ctypes.Structure):
@@ -40,7 +41,8 @@ class FtdConfig(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("max_len", ctypes.c_int), ("qkv_dtype", ctypes.c_int),
                 ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("out_dtype", ctypes.c_int), ("window", ctypes.c_int), ("page_size", ctypes.c_int),
-                ("num_pages", ctypes.c_int), ("q_len", ctypes.c_int)]
+                ("num_pages", ctypes.c_int), ("q_len", ctypes.c_int), ("kernel", ctypes.c_int),
+                ("wait_limit_us", ctypes.c_int)]
 
 
 class FtdError(RuntimeError):
@@ -89,6 +91,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ftd_kernel_launches.restype = ctypes.c_uint64
     lib.ftd_decode_mha_noalloc.argtypes = [ctypes.POINTER(FtdConfig)] + [P] * 11
     lib.ftd_decode_mha_noalloc.restype = I
+    lib.ftd_debug_stall_next.argtypes = [P, I]
+    lib.ftd_debug_stall_next.restype = I
     if path == LIB:
         _lib = lib
     return lib
@@ -157,6 +161,11 @@ def ftd_decode_mha_noalloc(cfg: FtdConfig, q, k_new, v_new, qkv_bias, k_cache, v
                                                                            device_err, stream))
 
 
+def ftd_debug_stall_next(ctx, calls: int) -> int:
+    """Test hook: the next ``calls`` decode calls withhold one tile copy (bounded-wait error path)."""
+    return load_library().ftd_debug_stall_next(ctypes.c_void_p(ctx), int(calls))
+
+
 def ftd_get_error(ctx) -> int:
     return load_library().ftd_get_error(ctypes.c_void_p(ctx))
 
@@ -180,11 +189,11 @@ class DecodeStep:
 
     def __init__(self, max_batch, n_q_heads, n_kv_heads, head_dim, max_len, qkv_dtype="bf16",
                  cache_dtype="bf16", softmax_scale=0.0, stream: Optional[int] = None, out_dtype="f32",
-                 window=0, page_size=0, num_pages=0, q_len=1):
+                 window=0, page_size=0, num_pages=0, q_len=1, kernel=FTD_KERNEL_AUTO, wait_limit_us=0):
         import torch
         self.cfg = FtdConfig(max_batch, n_q_heads, n_kv_heads, head_dim, max_len, DTYPES[qkv_dtype],
                              DTYPES[cache_dtype], float(softmax_scale), DTYPES[out_dtype], int(window),
-                             int(page_size), int(num_pages), int(q_len))
+                             int(page_size), int(num_pages), int(q_len), int(kernel), int(wait_limit_us))
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         st, ctx = ftd_init(self.cfg, s)
         check(st)

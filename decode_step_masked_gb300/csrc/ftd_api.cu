@@ -13,8 +13,10 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "../../include/ftd.h"
 #include "ftd_decode_splitk.cuh"
@@ -25,7 +27,11 @@ namespace {
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
-std::atomic<ftd_ctx*> g_current{nullptr};  // the most recently initialised live context
+// Live contexts in the order they were initialised; the last one is the current
+// context of ftd_decode_mha_current.  The lock also covers that call's launch,
+// so ftd_destroy cannot free a context under it.
+std::mutex g_live_mutex;
+std::vector<ftd_ctx*> g_live;
 
 ftd_status fail(ftd_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 ftd_status fail(ftd_status s, const char* fmt, ...) {
@@ -103,7 +109,7 @@ namespace ftd {
 // rows (blocks of 4 fill half of an 8-column block, since the MMA needs N >= 16
 // with the hi/lo split).  INT8 caches with head_dim 128 and a multiple of 8
 // query rows per kv head use its INT8 variant, in blocks of 8.
-// FTD_FORCE_CUDA_CORE=1 in the environment selects the CUDA-core kernel instead.
+// cfg.kernel == FTD_KERNEL_CUDA_CORE selects the CUDA-core kernel instead.
 // Internal to the library (hidden), shared by ftd_init and the no-allocation
 // entry point; tki.fn is null when the CUDA-core kernel runs.
 __attribute__((visibility("hidden"))) TcChoice choose_tc(const ftd_config& c) {
@@ -111,8 +117,7 @@ __attribute__((visibility("hidden"))) TcChoice choose_tc(const ftd_config& c) {
     r.nhb = 1;
     r.qblk = 8;
     const int rows_q = (c.q_len > 1 ? c.q_len : 1) * (c.n_q_heads / c.n_kv_heads);
-    const char* force = getenv("FTD_FORCE_CUDA_CORE");
-    const bool forced = force && force[0] == '1';
+    const bool forced = c.kernel == FTD_KERNEL_CUDA_CORE;
     const bool want_tc = (c.cache_dtype == FTD_F16 || c.cache_dtype == FTD_BF16) && c.head_dim == 128 &&
                          rows_q % 4 == 0 && !forced;
     const bool want_tc_i8 = c.cache_dtype == FTD_I8 && c.head_dim == 128 && rows_q % 8 == 0 && !forced;
@@ -128,6 +133,120 @@ __attribute__((visibility("hidden"))) TcChoice choose_tc(const ftd_config& c) {
 __attribute__((visibility("hidden"))) bool encode_tc_cache_map(CUtensorMap* map, void* base, ftd_dtype dt,
                                                                size_t rows) {
     return encode_cache_map(map, base, dt, rows);
+}
+
+// Checks of a configuration shared by every entry point that takes one (ftd_init
+// and the no-allocation entry point), and the kernel plan it implies.  On failure
+// the message goes to msg.
+__attribute__((visibility("hidden"))) ftd_status plan_config(const ftd_config& c, Plan* pl, char* msg, size_t n) {
+    auto bad = [&](ftd_status st, const char* fmt, auto... a) {
+        snprintf(msg, n, fmt, a...);
+        return st;
+    };
+    if (c.max_batch < 1 || c.max_batch > kMaxBatch)
+        return bad(FTD_ERR_INVALID_ARG, "max_batch %d outside 1..%d", c.max_batch, kMaxBatch);
+    if (c.n_kv_heads < 1 || c.n_q_heads < c.n_kv_heads || c.n_q_heads % c.n_kv_heads != 0)
+        return bad(FTD_ERR_INVALID_ARG, "n_q_heads %d must be a positive multiple of n_kv_heads %d", c.n_q_heads,
+                   c.n_kv_heads);
+    if (c.max_len < 16 || c.max_len % 16 != 0)
+        return bad(FTD_ERR_INVALID_ARG, "max_len %d must be a positive multiple of 16", c.max_len);
+    if (c.head_dim <= 0) return bad(FTD_ERR_INVALID_ARG, "head_dim %d", c.head_dim);
+    if (c.head_dim != 64 && c.head_dim != 128)
+        return bad(FTD_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", c.head_dim);
+    if (c.qkv_dtype != FTD_F32 && c.qkv_dtype != FTD_F16 && c.qkv_dtype != FTD_BF16)
+        return bad(FTD_ERR_UNSUPPORTED, "qkv_dtype %d (F32, F16 or BF16)", static_cast<int>(c.qkv_dtype));
+    if (c.cache_dtype != FTD_F32 && c.cache_dtype != FTD_F16 && c.cache_dtype != FTD_BF16 &&
+        c.cache_dtype != FTD_I8)
+        return bad(FTD_ERR_UNSUPPORTED, "cache_dtype %d", static_cast<int>(c.cache_dtype));
+    if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale))
+        return bad(FTD_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
+    if (c.out_dtype != FTD_F32 && c.out_dtype != FTD_F16 && c.out_dtype != FTD_BF16)
+        return bad(FTD_ERR_UNSUPPORTED, "out_dtype %d (F32, F16 or BF16)", static_cast<int>(c.out_dtype));
+    if (c.window < 0) return bad(FTD_ERR_INVALID_ARG, "window %d must be >= 0", c.window);
+    if (c.q_len < 0 || c.q_len > kMaxQLen)
+        return bad(FTD_ERR_INVALID_ARG, "q_len %d outside 0..%d", c.q_len, kMaxQLen);
+    const bool paged = c.page_size != 0;
+    if (paged && (c.page_size < 128 || (c.page_size & (c.page_size - 1)) != 0 || c.num_pages < 1))
+        return bad(FTD_ERR_INVALID_ARG, "page_size %d must be a power of two >= 128 with num_pages %d >= 1",
+                   c.page_size, c.num_pages);
+    if (c.kernel != FTD_KERNEL_AUTO && c.kernel != FTD_KERNEL_CUDA_CORE)
+        return bad(FTD_ERR_INVALID_ARG, "kernel %d (FTD_KERNEL_AUTO or FTD_KERNEL_CUDA_CORE)", c.kernel);
+    if (c.wait_limit_us < 0) return bad(FTD_ERR_INVALID_ARG, "wait_limit_us %d must be >= 0", c.wait_limit_us);
+
+    const int g = c.n_q_heads / c.n_kv_heads;
+    const int nq = c.q_len > 1 ? c.q_len : 1;
+    const int rows_q = nq * g;  // query rows per kv head: every new token's heads of the group
+    int G = 8;
+    while (rows_q % G) G >>= 1;
+    KernelInfo ki{};
+    switch (c.cache_dtype) {
+        case FTD_F32: ki = select_f32(c.head_dim, G); break;
+        case FTD_F16: ki = select_f16(c.head_dim, G); break;
+        case FTD_BF16: ki = select_bf16(c.head_dim, G); break;
+        case FTD_I8: ki = select_i8(c.head_dim, G); break;
+    }
+    if (!ki.fn) return bad(FTD_ERR_UNSUPPORTED, "no kernel for this configuration");
+    const size_t Hkv = static_cast<size_t>(c.n_kv_heads);
+    const size_t rows = paged ? static_cast<size_t>(c.num_pages) * Hkv * c.page_size
+                              : static_cast<size_t>(c.max_batch) * Hkv * c.max_len;
+    if (rows >= (static_cast<size_t>(1) << 31)) return bad(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit row indices");
+    const TcChoice tcc = choose_tc(c);
+    // the kernel's tile space (tiles of T rows per segment) and its weighted length (a few
+    // tiles more per segment) are indexed with 32-bit integers
+    const int T = tcc.tki.fn ? tc::TM : ki.T;
+    const long long nhb = tcc.tki.fn ? tcc.nhb : rows_q / G;
+    const long long segs = static_cast<long long>(c.max_batch) * c.n_kv_heads * nhb;
+    const long long tiles = segs * ((c.max_len + T - 1) / T);
+    if (tiles + 8 * segs >= (1LL << 31)) return bad(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit tile indices");
+    pl->G = G;
+    pl->nhb = rows_q / G;
+    pl->ki = ki;
+    pl->tcc = tcc;
+    pl->rows = rows;
+    return FTD_OK;
+}
+
+// Pointer checks of a decode call, shared by every decode entry point.  Device
+// pointers: caches, scales (INT8) and out 16-byte aligned; q, k_new, v_new and the
+// bias aligned to their element size; seq_lens 4-byte aligned.
+__attribute__((visibility("hidden"))) ftd_status check_pointers(const ftd_config& c, const void* q, const void* k_new,
+                                                                const void* v_new, const void* bias,
+                                                                const int32_t* seq_lens, const void* k_cache,
+                                                                const void* v_cache, const float* scales,
+                                                                const void* out, char* msg, size_t n) {
+    if (!q || !k_new || !v_new || !seq_lens || !out || !k_cache || !v_cache) {
+        snprintf(msg, n, "q, k_new, v_new, seq_lens, out and the caches must be non-NULL");
+        return FTD_ERR_INVALID_ARG;
+    }
+    const bool i8 = c.cache_dtype == FTD_I8;
+    if (i8 && !scales) {
+        snprintf(msg, n, "an INT8 cache needs its scales");
+        return FTD_ERR_INVALID_ARG;
+    }
+    if (!aligned16(k_cache) || !aligned16(v_cache) || (i8 && !aligned16(scales)) || !aligned16(out)) {
+        snprintf(msg, n, "caches, scales and out must be 16-byte aligned");
+        return FTD_ERR_INVALID_ARG;
+    }
+    const uintptr_t qmask = static_cast<uintptr_t>(elem_bytes(c.qkv_dtype) - 1);
+    if ((reinterpret_cast<uintptr_t>(q) & qmask) || (reinterpret_cast<uintptr_t>(k_new) & qmask) ||
+        (reinterpret_cast<uintptr_t>(v_new) & qmask) || (reinterpret_cast<uintptr_t>(bias) & qmask) ||
+        (reinterpret_cast<uintptr_t>(seq_lens) & 3u)) {
+        snprintf(msg, n, "q, k_new, v_new, bias, seq_lens must be naturally aligned");
+        return FTD_ERR_INVALID_ARG;
+    }
+    return FTD_OK;
+}
+
+// Pipeline wait limit in SM cycles: wait_limit_us at the device's peak SM clock, or the default.
+__attribute__((visibility("hidden"))) long long wait_cycles_for(const ftd_config& c, int dev) {
+    if (c.wait_limit_us <= 0) return kWaitLimitCycles;
+    int khz = 0;
+    if (cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess || khz <= 0) {
+        cudaGetLastError();
+        khz = 2100000;
+    }
+    const long long cyc = static_cast<long long>(c.wait_limit_us) * (khz / 1000);
+    return cyc < kWaitLimitCycles ? cyc : kWaitLimitCycles;
 }
 
 // Internal to the library (hidden): used by the no-allocation entry point so its
@@ -176,6 +295,8 @@ struct ftd_ctx {
     bool paged = false;
     int pages_per_seq = 0;
     cudaStream_t last_stream = nullptr;
+    long long wait_cycles = 0;  // limit of the kernels' pipeline waits
+    int stall_calls = 0;        // ftd_debug_stall_next: calls left that withhold a copy
 };
 
 extern "C" {
@@ -204,52 +325,14 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     *out = nullptr;
     if (!cfg) return fail(FTD_ERR_INVALID_ARG, "ftd_init: cfg is NULL");
     const ftd_config c = *cfg;
-    if (c.max_batch < 1 || c.max_batch > ftd::kMaxBatch)
-        return fail(FTD_ERR_INVALID_ARG, "max_batch %d outside 1..%d", c.max_batch, ftd::kMaxBatch);
-    if (c.n_kv_heads < 1 || c.n_q_heads < c.n_kv_heads || c.n_q_heads % c.n_kv_heads != 0)
-        return fail(FTD_ERR_INVALID_ARG, "n_q_heads %d must be a positive multiple of n_kv_heads %d",
-                    c.n_q_heads, c.n_kv_heads);
-    if (c.max_len < 16 || c.max_len % 16 != 0)
-        return fail(FTD_ERR_INVALID_ARG, "max_len %d must be a positive multiple of 16", c.max_len);
-    if (c.head_dim <= 0) return fail(FTD_ERR_INVALID_ARG, "head_dim %d", c.head_dim);
-    if (c.head_dim != 64 && c.head_dim != 128)
-        return fail(FTD_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", c.head_dim);
-    if (c.qkv_dtype != FTD_F32 && c.qkv_dtype != FTD_F16 && c.qkv_dtype != FTD_BF16)
-        return fail(FTD_ERR_UNSUPPORTED, "qkv_dtype %d (F32, F16 or BF16)", static_cast<int>(c.qkv_dtype));
-    if (c.cache_dtype != FTD_F32 && c.cache_dtype != FTD_F16 && c.cache_dtype != FTD_BF16 &&
-        c.cache_dtype != FTD_I8)
-        return fail(FTD_ERR_UNSUPPORTED, "cache_dtype %d", static_cast<int>(c.cache_dtype));
-    if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale))
-        return fail(FTD_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
-    if (c.out_dtype != FTD_F32 && c.out_dtype != FTD_F16 && c.out_dtype != FTD_BF16)
-        return fail(FTD_ERR_UNSUPPORTED, "out_dtype %d (F32, F16 or BF16)", static_cast<int>(c.out_dtype));
-    if (c.window < 0) return fail(FTD_ERR_INVALID_ARG, "window %d must be >= 0", c.window);
-    if (c.q_len < 0 || c.q_len > ftd::kMaxQLen)
-        return fail(FTD_ERR_INVALID_ARG, "q_len %d outside 0..%d", c.q_len, ftd::kMaxQLen);
+    ftd::Plan plan{};
+    char msg[256];
+    const ftd_status pst = ftd::plan_config(c, &plan, msg, sizeof msg);
+    if (pst != FTD_OK) return fail(pst, "%s", msg);
     const bool paged = c.page_size != 0;
-    if (paged && (c.page_size < 128 || (c.page_size & (c.page_size - 1)) != 0 || c.num_pages < 1))
-        return fail(FTD_ERR_INVALID_ARG, "page_size %d must be a power of two >= 128 with num_pages %d >= 1",
-                    c.page_size, c.num_pages);
-
-    const int g = c.n_q_heads / c.n_kv_heads;
     const int nq = c.q_len > 1 ? c.q_len : 1;
-    const int rows_q = nq * g;  // query rows per kv head: every new token's heads of the group
-    int G = 8;
-    while (rows_q % G) G >>= 1;
-    const int nhb = rows_q / G;
-
-    ftd::KernelInfo ki{};
-    switch (c.cache_dtype) {
-        case FTD_F32: ki = ftd::select_f32(c.head_dim, G); break;
-        case FTD_F16: ki = ftd::select_f16(c.head_dim, G); break;
-        case FTD_BF16: ki = ftd::select_bf16(c.head_dim, G); break;
-        case FTD_I8: ki = ftd::select_i8(c.head_dim, G); break;
-    }
-    if (!ki.fn) return fail(FTD_ERR_UNSUPPORTED, "no kernel for this configuration");
-
-    const long long tiles_per_seq = (c.max_len + ki.T - 1) / ki.T;
-    const long long max_tiles = static_cast<long long>(c.max_batch) * c.n_kv_heads * nhb * tiles_per_seq;
-    if (max_tiles >= (1LL << 31)) return fail(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit tile indices");
+    const int G = plan.G, nhb = plan.nhb;
+    const ftd::KernelInfo ki = plan.ki;
 
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -260,15 +343,13 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
 
     const int grid = sms;  // one persistent CTA per SM
-    const size_t B = c.max_batch, Hq = c.n_q_heads, Hkv = c.n_kv_heads, D = c.head_dim, L = c.max_len;
+    const size_t B = c.max_batch, Hq = c.n_q_heads, Hkv = c.n_kv_heads, D = c.head_dim;
     // cache rows of D elements: [B][Hkv][Lmax] contiguous, or [num_pages][Hkv][page_size] paged
-    const size_t rows = paged ? static_cast<size_t>(c.num_pages) * Hkv * c.page_size : B * Hkv * L;
-    if (rows >= (static_cast<size_t>(1) << 31))
-        return fail(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit row indices");
+    const size_t rows = plan.rows;
     const size_t cache_bytes = rows * D * elem_bytes(c.cache_dtype);
     const size_t scale_bytes = c.cache_dtype == FTD_I8 ? 2 * rows * sizeof(float) : 0;
 
-    const ftd::TcChoice tcc = ftd::choose_tc(c);
+    const ftd::TcChoice tcc = plan.tcc;
     const ftd::TcKernelInfo tki = tcc.tki;
     const int tc_nhb = tcc.nhb, tc_qblk = tcc.qblk;
     if (tki.fn) {
@@ -304,6 +385,7 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     ctx->paged = paged;
     ctx->pages_per_seq = paged ? (c.max_len + c.page_size - 1) / c.page_size : 0;
     ctx->n_counters = n_seg;
+    ctx->wait_cycles = ftd::wait_cycles_for(c, dev);
 
     size_t off = 0;
     auto carve = [&](size_t bytes) {
@@ -347,7 +429,10 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
         return cuda_fail(e, "cudaMemsetAsync of the cache pool");
     }
     *out = ctx;
-    g_current.store(ctx);
+    {
+        std::lock_guard<std::mutex> lock(g_live_mutex);
+        g_live.push_back(ctx);
+    }
     return FTD_OK;
 }
 
@@ -381,20 +466,14 @@ static cudaError_t launch_overlapped(const void* fn, int grid, int threads, int 
 static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                 const void* bias, void* k_cache, void* v_cache, const int32_t* block_table,
                                 const int32_t* seq_lens, float* scales, void* out, cudaStream_t stream) {
-    if (!q || !k_new || !v_new || !seq_lens || !out)
-        return fail(FTD_ERR_INVALID_ARG, "q, k_new, v_new, seq_lens and out must be non-NULL");
     if (!k_cache) k_cache = ctx->k_cache;
     if (!v_cache) v_cache = ctx->v_cache;
     const bool i8 = ctx->cfg.cache_dtype == FTD_I8;
     if (i8 && !scales) scales = ctx->scales;
-    if (!aligned16(k_cache) || !aligned16(v_cache) || (i8 && !aligned16(scales)) || !aligned16(out))
-        return fail(FTD_ERR_INVALID_ARG, "caches, scales and out must be 16-byte aligned");
-    const int qeb = elem_bytes(ctx->cfg.qkv_dtype);
-    const uintptr_t qmask = static_cast<uintptr_t>(qeb - 1);
-    if ((reinterpret_cast<uintptr_t>(q) & qmask) || (reinterpret_cast<uintptr_t>(k_new) & qmask) ||
-        (reinterpret_cast<uintptr_t>(v_new) & qmask) || (reinterpret_cast<uintptr_t>(bias) & qmask) ||
-        (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-        return fail(FTD_ERR_INVALID_ARG, "q, k_new, v_new, bias, seq_lens must be naturally aligned");
+    char msg[160];
+    const ftd_status cst = ftd::check_pointers(ctx->cfg, q, k_new, v_new, bias, seq_lens, k_cache, v_cache, scales,
+                                               out, msg, sizeof msg);
+    if (cst != FTD_OK) return fail(cst, "%s", msg);
 
     const ftd_config& c = ctx->cfg;
     ftd::DecodeParams p{};
@@ -430,6 +509,12 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     p.page_shift = 0;
     while (ctx->paged && (1 << p.page_shift) < c.page_size) ++p.page_shift;
     p.num_pages = c.num_pages;
+    p.wait_cycles = ctx->wait_cycles;
+    p.stall = 0;
+    if (ctx->stall_calls > 0) {
+        p.stall = 1;
+        --ctx->stall_calls;
+    }
 
     cudaError_t e;
     if (ctx->use_tc) {
@@ -471,7 +556,8 @@ ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const 
 ftd_status ftd_decode_mha_current(const void* q, const void* k_new, const void* v_new, const void* qkv_bias,
                                   void* k_cache, void* v_cache, const int32_t* seq_lens, float* scales, void* out,
                                   void* stream) {
-    ftd_ctx* ctx = g_current.load();
+    std::lock_guard<std::mutex> lock(g_live_mutex);  // ftd_destroy waits until the launch is done
+    ftd_ctx* ctx = g_live.empty() ? nullptr : g_live.back();
     if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_current: no context (ftd_init first)");
     return ftd_decode_mha(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out, stream);
 }
@@ -581,10 +667,24 @@ ftd_status ftd_get_error(ftd_ctx* ctx) {
     return fail(FTD_ERR_SEQ_OVERFLOW, "some seq_lens[b] + q_len > max_len; those slots were skipped");
 }
 
+ftd_status ftd_debug_stall_next(ftd_ctx* ctx, int calls) {
+    g_last_error.clear();
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_debug_stall_next: ctx is NULL");
+    if (calls < 0) return fail(FTD_ERR_INVALID_ARG, "ftd_debug_stall_next: calls %d must be >= 0", calls);
+    ctx->stall_calls = calls;
+    return FTD_OK;
+}
+
 void ftd_destroy(ftd_ctx* ctx) {
     if (!ctx) return;
-    ftd_ctx* expected = ctx;
-    g_current.compare_exchange_strong(expected, nullptr);
+    {
+        std::lock_guard<std::mutex> lock(g_live_mutex);
+        for (size_t i = 0; i < g_live.size(); ++i)
+            if (g_live[i] == ctx) {
+                g_live.erase(g_live.begin() + static_cast<long>(i));
+                break;
+            }
+    }
     cudaDeviceSynchronize();
     cudaFree(ctx->pool);
     delete ctx;

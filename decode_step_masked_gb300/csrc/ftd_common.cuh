@@ -20,8 +20,13 @@ constexpr uint32_t kErrBadPage = 4u;
 // Most new tokens per slot in one step (speculative verification runs).
 constexpr int kMaxQLen = 64;
 
-// A wait on a copy gives up after this many SM clock cycles (about 2 s).
+// Default limit of a pipeline wait (a wait on a copy, an MMA or another role of
+// the block), in SM clock cycles: about 2 s.  A context can set a shorter one.
 constexpr long long kWaitLimitCycles = 4000000000LL;
+// Limit of a drain wait after an abort (the copies and MMAs a block still has in
+// flight before it exits).  It never takes the context's shorter pipeline limit:
+// a bulk copy must not land in shared memory after the block has left.
+constexpr long long kDrainLimitCycles = 4000000000LL;
 
 constexpr int kMaxBatch = 1024;
 constexpr int kWarps = 8;               // warps per CTA, each an independent worker
@@ -55,6 +60,8 @@ struct DecodeParams {
     // block_table[b * pages_per_seq + i] is the page of positions [i*page_size, (i+1)*page_size)
     const int32_t* block_table;  // nullptr: contiguous [B][Hkv][Lmax][D] cache
     int pages_per_seq, page_shift, num_pages;  // page_size = 1 << page_shift
+    long long wait_cycles;  // limit of a pipeline wait (kWaitLimitCycles unless the context sets one)
+    int stall;              // test hook: block 0 never issues its first tile copy (see ftd_debug_stall_next)
 };
 
 // First visible position of a slot with L cached tokens (the window start).
@@ -169,6 +176,11 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Invalidate a barrier whose phases are all complete, so it can be initialised again.
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -232,13 +244,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of a barrier; after kWaitLimitCycles raise the
+// Wait for phase `parity` of a barrier; after `limit` SM cycles raise the
 // timeout bit and return false instead of spinning forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t* err, long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             atomicOr(err, kErrTimeout);
             return false;
         }

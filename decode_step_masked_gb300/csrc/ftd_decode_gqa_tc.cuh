@@ -231,13 +231,15 @@ __device__ __forceinline__ bool bar_any(int id, int n, bool pred) {
     return r != 0;
 }
 
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t* err, volatile int* abort_flag) {
+// Bounded pipeline wait (`limit` SM cycles) that also gives up as soon as
+// another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t* err, volatile int* abort_flag,
+                                              long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             atomicOr(err, kErrTimeout);
             *abort_flag = 1;
             return false;
@@ -440,22 +442,24 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
     constexpr bool kPasses = !MQ && G >= 16;
     const int np = kPasses ? p.nhb : 1;
     const int spp = kPasses ? p.Hkv : p.Hkv * p.nhb;
-    if (warp == 0) build_prefix(p, TM, spp, LY::ALPHA, P, VP, Ls, lane);
+    bool ovf = false;
+    if (warp == 0) ovf = build_prefix(p, TM, spp, LY::ALPHA, P, VP, Ls, lane);
     fence_mbar_init();
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // The split depends only on the lengths, which no launch of this library writes,
-    // so it runs before the wait on the previous launch, and a block that starts
-    // while the previous step drains warms L2 with its first tiles (contiguous
-    // caches).  Reads of the caches and writes of shared outputs come after the wait.
+    // The split depends only on the lengths, so it runs before the wait on the
+    // previous launch, and a block that starts while the previous step drains
+    // warms L2 with its first tiles (contiguous caches).  After the wait the
+    // lengths are checked again (lengths_changed).  Reads of the caches and
+    // writes of shared outputs come after the wait.
     const long long W = gridDim.x;
     const int wid = blockIdx.x;
     const PassSplit<LY::ALPHA> split{P, VP, p.B, spp, np, static_cast<int>(W)};
-    const int t_begin = split.begin(wid);
-    const int n_my = split.begin(wid + 1) - t_begin;
+    int t_begin = split.begin(wid);
+    int n_my = split.begin(wid + 1) - t_begin;
     if (n_my > 0 && tid == 0 && !p.block_table) {
         Cursor c = locate_pass(t_begin, P, p.B, spp, np);
         for (int k = 0; k < min(NS, n_my); ++k) {
@@ -473,70 +477,118 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
     grid_dep_wait();    // inputs, caches and outputs may be in use by the previous launch
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
 
+    // ---- TMA producer state (thread 0) ----
+    // Test hook (DecodeParams::stall): block 0 never issues its first tile, so the
+    // bounded waits of its consumers run out and the abort path runs.
+    const bool withhold0 = p.stall && blockIdx.x == 0;
+    Cursor pcu{};        // the producer's cursor: the next tile to issue
+    PageCursor pages;
+    const uint64_t l2pol = l2_stream_policy();
+    // Issue tile k at pcu (waiting for its stage to be free from the third tile on)
+    // and advance; false when the wait gave up.
+    auto produce = [&](int k) -> bool {
+        const int s = k % NS;
+        // the tile's address first: a block-table load then overlaps the wait for a free stage
+        const int kvh = pcu.seg / p.nhb;
+        const int t0 = (window_start(Ls[pcu.b], p.window) / TM + pcu.tile) * TM;
+        long long rb = cache_row(p, pcu.b, kvh, t0, pages.page(p, pcu.b, t0));
+        if (rb < 0) {  // bad page: flag it and read row 0 instead (the slot's output is undefined)
+            atomicOr(p.err, kErrBadPage);
+            rb = 0;
+        }
+        const int row0 = static_cast<int>(rb);
+        if constexpr (I8) {
+            // raw stage: K and V codes (one 128 x 128 B box each) and the scales
+            // of the rows before the new tokens
+            const int s8 = k & 1;
+            if (k >= 2 && !tc::wait_or_abort(bar(kBarEmpty8 + s8), ((k >> 1) - 1) & 1, p.err, abort_flag, p.wait_cycles))
+                return false;
+            const int n_cache = min(TM, max(0, Ls[pcu.b] - t0));
+            const uint32_t sb = static_cast<uint32_t>((n_cache * 4 + 15) & ~15);
+            unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
+            const uint32_t fb = bar(kBarFull8 + s8);
+            if (!(withhold0 && k == 0)) {
+                mbar_arrive_expect_tx(fb, 2 * TM * D + 2 * sb);
+                tc::tma_load_2d(smem_addr(st8), &tmk, 0, row0, fb, l2pol);
+                tc::tma_load_2d(smem_addr(st8 + TM * D), &tmv, 0, row0, fb, l2pol);
+                if (sb) {
+                    bulk_g2s_hint(smem_addr(st8 + 2 * TM * D), p.k_scales + rb, sb, fb, l2pol);
+                    bulk_g2s_hint(smem_addr(st8 + 2 * TM * D + TM * 4), p.v_scales + rb, sb, fb, l2pol);
+                }
+            }
+        } else {
+            if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag, p.wait_cycles))
+                return false;
+            const uint32_t st = smem_addr(stages + s * tc::STAGE);
+            if (!(withhold0 && k == 0)) {
+                mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
+                tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s), l2pol);
+                tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
+                tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
+                tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
+            }
+        }
+        if (k + 1 < n_my) advance_pass(pcu, P, p.B, spp, np);
+        return true;
+    };
+    // The first stages' worth of tiles (no stage to wait for) are issued at once; the
+    // lengths are checked again while they are in flight.
+    constexpr int kFirst = I8 ? 2 : NS;
+    int prod_k = 0;      // tiles the producer got to (issued or withheld)
+    auto start = [&]() {
+        prod_k = 0;
+        if (tid != 0 || n_my <= 0) return;
+        pcu = locate_pass(t_begin, P, p.B, spp, np);
+        for (; prod_k < min(kFirst, n_my); ++prod_k) produce(prod_k);
+    };
+    start();
+    if (lengths_changed(p, Ls)) {
+        // (rare) the plan was built from stale lengths: let the copies issued from it
+        // land, reset the barriers, rebuild the plan from the lengths now visible, start again
+        bool failed = false;
+        if (tid == 0) {
+            for (int kk = 0; kk < prod_k; ++kk) {
+                if (withhold0 && kk == 0) continue;
+                failed |= !mbar_wait_bounded(bar((I8 ? kBarFull8 + (kk & 1) : kBarFull + kk % NS)), 0u, p.err,
+                                             kDrainLimitCycles);
+            }
+        }
+        if (__syncthreads_or(failed)) {
+            // a copy did not land in time: leave, with the error raised and TMEM freed
+            if (warp == 1)
+                asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LY::TMEM_COLS));
+            return;
+        }
+        if (tid == 0) {
+            for (int i = 0; i < kNumBars; ++i) {
+                mbar_inval(bar(i));
+                mbar_init(bar(i), 1);
+            }
+        }
+        fence_mbar_init();
+        if (warp == 0) ovf = build_prefix(p, TM, spp, LY::ALPHA, P, VP, Ls, lane);
+        __syncthreads();
+        t_begin = split.begin(wid);
+        n_my = split.begin(wid + 1) - t_begin;
+        pages = PageCursor{};
+        start();
+    }
+    if (ovf && warp == 0 && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
+
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (P[b + 1] == P[b]) {
             zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
         }
     }
 
+    int last_bar = -1;   // MMA issuer (warp 1, lane 0): barrier and phase of its latest commit,
+    uint32_t last_par = 0;  // which completes once every MMA issued before it has
     if (n_my > 0) {
         if (warp == 0) {
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
-                Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
-                PageCursor pages;
-                const uint64_t l2pol = l2_stream_policy();
-                int k = 0;
-                for (; k < n_my; ++k) {
-                    const int s = k % NS;
-                    // the tile's address first: a block-table load then overlaps the wait for a free stage
-                    const int kvh = cu.seg / p.nhb;
-                    const int t0 = (window_start(Ls[cu.b], p.window) / TM + cu.tile) * TM;
-                    long long rb = cache_row(p, cu.b, kvh, t0, pages.page(p, cu.b, t0));
-                    if (rb < 0) {  // bad page: flag it and read row 0 instead (the slot's output is undefined)
-                        atomicOr(p.err, kErrBadPage);
-                        rb = 0;
-                    }
-                    const int row0 = static_cast<int>(rb);
-                    if constexpr (I8) {
-                        // raw stage: K and V codes (one 128 x 128 B box each) and the scales
-                        // of the rows before the new tokens
-                        const int s8 = k & 1;
-                        if (k >= 2 && !tc::wait_or_abort(bar(kBarEmpty8 + s8), ((k >> 1) - 1) & 1, p.err, abort_flag))
-                            break;
-                        const int n_cache = min(TM, max(0, Ls[cu.b] - t0));
-                        const uint32_t sb = static_cast<uint32_t>((n_cache * 4 + 15) & ~15);
-                        unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
-                        const uint32_t fb = bar(kBarFull8 + s8);
-                        mbar_arrive_expect_tx(fb, 2 * TM * D + 2 * sb);
-                        tc::tma_load_2d(smem_addr(st8), &tmk, 0, row0, fb, l2pol);
-                        tc::tma_load_2d(smem_addr(st8 + TM * D), &tmv, 0, row0, fb, l2pol);
-                        if (sb) {
-                            bulk_g2s_hint(smem_addr(st8 + 2 * TM * D), p.k_scales + rb, sb, fb, l2pol);
-                            bulk_g2s_hint(smem_addr(st8 + 2 * TM * D + TM * 4), p.v_scales + rb, sb, fb, l2pol);
-                        }
-                    } else {
-                        if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag))
-                            break;
-                        const uint32_t st = smem_addr(stages + s * tc::STAGE);
-                        mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
-                        tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s), l2pol);
-                        tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
-                        tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
-                        tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
-                    }
-                    if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
-                }
-                if (k < n_my) {
-                    // aborted: let the copies already issued land before the block exits
-                    if constexpr (I8) {
-                        for (int kk = max(0, k - 2); kk < k; ++kk)
-                            mbar_wait_bounded(bar(kBarFull8 + (kk & 1)), (kk >> 1) & 1, p.err);
-                    } else {
-                        for (int kk = max(0, k - NS); kk < k; ++kk)
-                            mbar_wait_bounded(bar(kBarFull + kk % NS), (kk / NS) & 1, p.err);
-                    }
-                }
+                for (; prod_k < n_my; ++prod_k)
+                    if (!produce(prod_k)) break;
             }
         } else if (warp == 1) {
             // ------------------------------------------- append + MMA issue
@@ -557,8 +609,8 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
             const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(Qs), 16, 1024);
             const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(Ps), 16, 1024);
             auto issue_pv = [&](int kk) -> bool {
-                bool w = tc::wait_or_abort(bar(kBarPFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
-                if constexpr (I8) w = w && tc::wait_or_abort(bar(kBarFullV + kk % NB), (kk / NB) & 1, p.err, abort_flag);
+                bool w = tc::wait_or_abort(bar(kBarPFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag, p.wait_cycles);
+                if constexpr (I8) w = w && tc::wait_or_abort(bar(kBarFullV + kk % NB), (kk / NB) & 1, p.err, abort_flag, p.wait_cycles);
                 if (__any_sync(FULL, !w)) return false;
                 if (lane == 0) {
                     tc::tc_fence_after();
@@ -572,6 +624,8 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     }
                     tc::mma_commit(bar(kBarOFull + (kk & 1)));
                     tc::mma_commit(bar((I8 ? kBarEmptyV : kBarEmpty) + kk % NB));
+                    last_bar = kBarOFull + (kk & 1);
+                    last_par = (kk >> 1) & 1;
                 }
                 __syncwarp();
                 return true;
@@ -580,7 +634,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                 const int s = k % NB;
                 const bool new_piece = (k == 0) || (cu.tile == 0);
                 if (k > 0 && new_piece && !issue_pv(k - 1)) { ok = false; break; }
-                const bool wf = tc::wait_or_abort(bar(kBarFull + s), (k / NB) & 1, p.err, abort_flag);
+                const bool wf = tc::wait_or_abort(bar(kBarFull + s), (k / NB) & 1, p.err, abort_flag, p.wait_cycles);
                 if (__any_sync(FULL, !wf)) { ok = false; break; }
                 // (INT8: the converting warps append, and the weights of rows outside
                 // the window or past the end are zero, so no staged row needs zeroing)
@@ -651,7 +705,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     __syncwarp();
                 }
                 if (new_piece) {
-                    const bool wq = tc::wait_or_abort(bar(kBarQReady), qcount & 1, p.err, abort_flag);
+                    const bool wq = tc::wait_or_abort(bar(kBarQReady), qcount & 1, p.err, abort_flag, p.wait_cycles);
                     if (__any_sync(FULL, !wq)) { ok = false; break; }
                     ++qcount;
                 }
@@ -666,6 +720,8 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     }
                     tc::mma_commit(bar(kBarSFull + (k & 1)));
                     if constexpr (I8) tc::mma_commit(bar(kBarEmpty + s));  // the K half is read
+                    last_bar = kBarSFull + (k & 1);
+                    last_par = (k >> 1) & 1;
                 }
                 __syncwarp();
                 if (k > 0 && !new_piece && !issue_pv(k - 1)) { ok = false; break; }
@@ -686,7 +742,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
             Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
             for (int k = 0; k < n_my; ++k) {
                 const int s8 = k & 1, sb = k % NB;
-                const bool okf = tc::wait_or_abort(bar(kBarFull8 + s8), (k >> 1) & 1, p.err, abort_flag);
+                const bool okf = tc::wait_or_abort(bar(kBarFull8 + s8), (k >> 1) & 1, p.err, abort_flag, p.wait_cycles);
                 if (tc::bar_any(3, NCV, !okf)) break;
                 unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
                 float* ssc = reinterpret_cast<float*>(st8 + 2 * TM * D);  // [K | V][TM]
@@ -758,7 +814,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     }
                 };
                 bool oke = true;
-                if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmpty + sb), ((k / NB) - 1) & 1, p.err, abort_flag);
+                if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmpty + sb), ((k / NB) - 1) & 1, p.err, abort_flag, p.wait_cycles);
                 // (the barrier also makes the appended rows visible to both warps)
                 if (tc::bar_any(3, NCV, !oke)) break;
                 convert(0);
@@ -769,7 +825,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarFull + sb)) : "memory");
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kBarScale + (k & 3))) : "memory");
                 }
-                if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmptyV + sb), ((k / NB) - 1) & 1, p.err, abort_flag);
+                if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmptyV + sb), ((k / NB) - 1) & 1, p.err, abort_flag, p.wait_cycles);
                 if (tc::bar_any(3, NCV, !oke)) break;
                 convert(1);
                 fence_proxy_async_smem();
@@ -807,7 +863,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
             bool pending = false;
             int piece_first = cu.tile;
             auto acc_o = [&](int kk) -> bool {
-                const bool okw = tc::wait_or_abort(bar(kBarOFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag);
+                const bool okw = tc::wait_or_abort(bar(kBarOFull + (kk & 1)), (kk >> 1) & 1, p.err, abort_flag, p.wait_cycles);
                 if (tc::bar_any(2, SMX, !okw)) return false;
                 tc::tc_fence_after();
                 __syncwarp();
@@ -894,11 +950,11 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     load_q(nx);
                 }
                 // ---- scores of this tile ----
-                bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag);
+                bool oks = tc::wait_or_abort(bar(kBarSFull + (k & 1)), (k >> 1) & 1, p.err, abort_flag, p.wait_cycles);
                 // INT8: the scales of the tile come from the converting warps; waiting on
                 // their publication orders those writes before the reads.  (Slot k % 4 is
                 // published again for tile k + 4 only after this softmax has issued P(k).)
-                if constexpr (I8) oks = oks && tc::wait_or_abort(bar(kBarScale + (k & 3)), (k >> 2) & 1, p.err, abort_flag);
+                if constexpr (I8) oks = oks && tc::wait_or_abort(bar(kBarScale + (k & 3)), (k >> 2) & 1, p.err, abort_flag, p.wait_cycles);
                 if (tc::bar_any(2, SMX, !oks)) break;
                 tc::tc_fence_after();
                 __syncwarp();
@@ -1091,6 +1147,26 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
+    if (*abort_flag) {
+        // Some role gave up (a bounded wait ran out).  Every role has left its loop, so
+        // nothing waits on the pipeline any more; before TMEM is freed and the block
+        // exits, wait (long drain limit) for what is still in flight: the producer's
+        // last stages' worth of copies before tile prod_k (all but a withheld one), and
+        // the MMAs, through the issuer's latest commit.
+        if (warp == 0 && lane == 0) {
+            if constexpr (I8) {
+                for (int kk = max(0, prod_k - 2); kk < prod_k; ++kk)
+                    if (!(withhold0 && kk == 0))
+                        mbar_wait_bounded(bar(kBarFull8 + (kk & 1)), (kk >> 1) & 1, p.err, kDrainLimitCycles);
+            } else {
+                for (int kk = max(0, prod_k - NS); kk < prod_k; ++kk)
+                    if (!(withhold0 && kk == 0))
+                        mbar_wait_bounded(bar(kBarFull + kk % NS), (kk / NS) & 1, p.err, kDrainLimitCycles);
+            }
+        }
+        if (warp == 1 && lane == 0 && last_bar >= 0)
+            mbar_wait_bounded(bar(last_bar), last_par, p.err, kDrainLimitCycles);
+    }
     if (warp == 1) {
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LY::TMEM_COLS));

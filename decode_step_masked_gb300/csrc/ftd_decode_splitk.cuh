@@ -240,9 +240,9 @@ __device__ __forceinline__ void advance(Cursor& cu, const int* P, int segs) {
 // Tiles per slot and their prefixes, computed by one warp: P[b] counts the tiles
 // of the slots before b (segments of T rows, from the tile holding the window start
 // to the tile of position L + nq - 1, times segs), VP[b] the same plus ALPHA per
-// segment, Ls[b] the cached length (-1 for slots without work).  Slots with
-// L + nq > Lmax raise the sticky overflow flag (once, from block 0).
-__device__ __forceinline__ void build_prefix(const DecodeParams& p, int T, int segs, int alpha, int* P, int* VP,
+// segment, Ls[b] the cached length (-1 for slots without work).  Returns, in every
+// lane, whether some slot has L + nq > Lmax (the caller raises the overflow flag).
+__device__ __forceinline__ bool build_prefix(const DecodeParams& p, int T, int segs, int alpha, int* P, int* VP,
                                              int* Ls, int lane) {
     constexpr unsigned FULL = 0xffffffffu;
     int carry = 0, vcarry = 0;
@@ -275,7 +275,24 @@ __device__ __forceinline__ void build_prefix(const DecodeParams& p, int T, int s
         P[0] = 0;
         VP[0] = 0;
     }
-    if (__any_sync(FULL, ovf) && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
+    return __any_sync(FULL, ovf);
+}
+
+// Whether the lengths differ from the ones the split was built from (Ls), by all
+// threads of the block.  The split is built from lengths read before
+// grid_dep_wait, so that a block placed while the previous launch drains can
+// warm L2 with its first tiles; but a preceding kernel's writes are guaranteed
+// visible only after the wait (a kernel that allows an early start, or that
+// ends without a memory flush yet, may still be writing seq_lens).  So after
+// the wait every block reads the lengths again, through L2, and rebuilds the
+// split when any of them changed.
+__device__ __forceinline__ bool lengths_changed(const DecodeParams& p, const int* Ls) {
+    bool changed = false;
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+        const int L = __ldcg(p.seq_lens + b);
+        changed |= ((L >= 0 && L <= p.Lmax - p.nq) ? L : -1) != Ls[b];
+    }
+    return __syncthreads_or(changed) != 0;
 }
 
 // Static split of the tile space over W workers, weighted: a segment boundary inside
@@ -357,21 +374,21 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
 #pragma unroll
         for (int s = 0; s < SPW; ++s) mbar_init(smem_addr(&bars[s]), 1);
     }
-    // The split depends only on the lengths, which no launch of this library
-    // writes, so it is computed before waiting on the previous launch: a block
-    // that starts while the previous step drains then warms L2 with its first
-    // tiles (contiguous caches) instead of idling.  Everything that reads the
-    // caches' contents or writes memory the previous launch uses comes after
-    // the wait.
-    if (warp == 0) build_prefix(p, T, segs, TL::ALPHA, P, VP, Ls, lane);
+    // The split depends only on the lengths, so it is computed before waiting on
+    // the previous launch: a block that starts while the previous step drains
+    // then warms L2 with its first tiles (contiguous caches) instead of idling.
+    // After the wait the lengths are checked again (lengths_changed).  Everything
+    // that reads the caches' contents or writes memory comes after the wait.
+    bool ovf = false;
+    if (warp == 0) ovf = build_prefix(p, T, segs, TL::ALPHA, P, VP, Ls, lane);
     fence_mbar_init();
     __syncthreads();
 
     const long long W = static_cast<long long>(gridDim.x) * TL::WARPS;
     const int wid = blockIdx.x * TL::WARPS + warp;
     const WeightedSplit<TL::ALPHA> split{P, VP, p.B, segs, static_cast<int>(W)};
-    const int t_begin = split.begin(wid);
-    const int n_my = split.begin(wid + 1) - t_begin;
+    int t_begin = split.begin(wid);
+    int n_my = split.begin(wid + 1) - t_begin;
     if (n_my > 0 && lane == 0 && !p.block_table) {
         Cursor c = locate(t_begin, P, p.B, segs);
         for (int k = 0; k < min(SPW, n_my); ++k) {
@@ -389,19 +406,14 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     grid_dep_wait();    // inputs, caches and outputs may be in use by the previous launch
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
 
-    // Slots without work (inactive or overflowing) get a zero output.
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-        if (P[b + 1] == P[b]) {
-            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
-        }
-    }
-    if (n_my <= 0) return;
-
     // ---- bulk copies of one tile (lane 0 only) ----
     // Paged caches: the page of the tile comes from the block table; the entry
     // of the current page is kept and the next page's entry is loaded early.
     PageCursor pages;
     const uint64_t l2pol = l2_stream_policy();
+    // Test hook (DecodeParams::stall): worker 0 never issues its first tile, so its
+    // bounded wait runs out and the abort path runs.
+    const bool stall_me = p.stall && wid == 0;
     auto issue = [&](int s, const Cursor& cu) {
         const int L = Ls[cu.b];
         const int t0 = (window_start(L, p.window) / T + cu.tile) * T;
@@ -452,17 +464,58 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
         }
     };
 
-    Cursor ci = locate(t_begin, P, p.B, segs);
-    Cursor cc = ci;
-    if (!I8) prefetch_segment(ci);  // the first segment's new K/V rows are needed at its last tile
-    const int npre = min(SPW, n_my);
-    for (int k = 0; k < npre; ++k) {
-        if (lane == 0) issue(k, ci);
-        if (k + 1 < n_my) {
-            advance(ci, P, segs);
-            if (!I8 && ci.tile == 0) prefetch_segment(ci);
+    // The first SPW tiles of the plan are issued at once; the lengths are checked
+    // again while they are in flight.  Copy cursor ci, compute cursor cc.
+    Cursor ci{}, cc{};
+    int npre = 0;
+    auto start = [&]() {
+        npre = min(SPW, n_my);
+        if (n_my <= 0) return;
+        ci = locate(t_begin, P, p.B, segs);
+        cc = ci;
+        if (!I8) prefetch_segment(ci);  // the first segment's new K/V rows are needed at its last tile
+        for (int k = 0; k < npre; ++k) {
+            if (lane == 0 && !(stall_me && k == 0)) issue(k, ci);
+            if (k + 1 < n_my) {
+                advance(ci, P, segs);
+                if (!I8 && ci.tile == 0) prefetch_segment(ci);
+            }
+        }
+    };
+    start();
+    if (lengths_changed(p, Ls)) {
+        // (rare) the plan was built from stale lengths: let the copies issued from it
+        // land, reset the barriers, rebuild the plan from the lengths now visible, start again
+        bool failed = false;
+        if (lane == 0)
+            for (int k = 0; k < npre; ++k)
+                if (!(stall_me && k == 0))
+                    failed |= !mbar_wait_bounded(smem_addr(&bars[k]), 0u, p.err, kDrainLimitCycles);
+        if (__syncthreads_or(failed)) return;
+        if (lane == 0) {
+#pragma unroll
+            for (int s = 0; s < SPW; ++s) {
+                mbar_inval(smem_addr(&bars[s]));
+                mbar_init(smem_addr(&bars[s]), 1);
+            }
+        }
+        fence_mbar_init();
+        if (warp == 0) ovf = build_prefix(p, T, segs, TL::ALPHA, P, VP, Ls, lane);
+        __syncthreads();
+        t_begin = split.begin(wid);
+        n_my = split.begin(wid + 1) - t_begin;
+        pages = PageCursor{};
+        start();
+    }
+    if (ovf && warp == 0 && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
+
+    // Slots without work (inactive or overflowing) get a zero output.
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        if (P[b + 1] == P[b]) {
+            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
         }
     }
+    if (n_my <= 0) return;
 
     float qr[G][EPL], o[G][EPL], m[G], l[G];
     int tk[G];  // token of each query row (0 unless several new tokens per step)
@@ -639,7 +692,8 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     for (; k < n_my; ++k) {
         const int s = k % SPW;
         unsigned char* st = wbase + s * STAGE;
-        if (!mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((k / SPW) & 1), p.err)) break;
+        if (!mbar_wait_bounded(smem_addr(&bars[s]), static_cast<uint32_t>((k / SPW) & 1), p.err, p.wait_cycles))
+            break;
         if (pend) {  // the arrival of the piece that ended one tile ago has returned by now
             resolve(pend_ret, pend_cu, pend_tiles);
             pend = false;
@@ -968,12 +1022,15 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     }
 
     if (k < n_my) {
-        // A copy did not arrive in time: the error bit is set.  Wait (bounded)
-        // for the copies this warp still has in flight before leaving, so no
-        // transfer lands in shared memory after the block has exited.
+        // A copy did not arrive in time: the error bit is set.  Wait for the
+        // copies this warp still has in flight before leaving (tiles k .. k +
+        // SPW - 1 were issued, all but a withheld one), with the long drain
+        // limit, so no transfer lands in shared memory after the block has exited.
         const int last_issued = min(n_my, k + SPW) - 1;
         for (int kk = k; kk <= last_issued; ++kk)
-            mbar_wait_bounded(smem_addr(&bars[kk % SPW]), static_cast<uint32_t>((kk / SPW) & 1), p.err);
+            if (!(stall_me && kk == 0))
+                mbar_wait_bounded(smem_addr(&bars[kk % SPW]), static_cast<uint32_t>((kk / SPW) & 1), p.err,
+                                  kDrainLimitCycles);
     }
 }
 

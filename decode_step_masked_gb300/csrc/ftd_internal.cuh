@@ -17,6 +17,27 @@ struct TcChoice {
 };
 TcChoice choose_tc(const ftd_config& c);
 
+// What a valid configuration runs: the CUDA-core kernel's block of G query rows
+// (nhb blocks per kv head) and its instantiation, the tensor-core choice, and
+// the number of cache rows (of head_dim elements) the caches hold.
+struct Plan {
+    int G, nhb;
+    KernelInfo ki;
+    TcChoice tcc;
+    size_t rows;
+};
+// Every check of a configuration (sizes, dtypes, options, 32-bit index bounds);
+// FTD_OK and the plan, or a status and a message in msg.
+ftd_status plan_config(const ftd_config& c, Plan* plan, char* msg, size_t n);
+
+// Null and alignment checks of a decode call's pointers.
+ftd_status check_pointers(const ftd_config& c, const void* q, const void* k_new, const void* v_new, const void* bias,
+                          const int32_t* seq_lens, const void* k_cache, const void* v_cache, const float* scales,
+                          const void* out, char* msg, size_t n);
+
+// Limit of the kernels' pipeline waits in SM cycles (cfg.wait_limit_us, or the default).
+long long wait_cycles_for(const ftd_config& c, int dev);
+
 // Tensor map of a [rows][128] cache view for the tensor-core kernel; false when
 // the driver entry point is missing or the encoding fails.
 bool encode_tc_cache_map(CUtensorMap* map, void* base, ftd_dtype dt, size_t rows);

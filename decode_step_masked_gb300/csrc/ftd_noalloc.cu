@@ -66,45 +66,20 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
     ftd::set_last_error("");
     if (!cfg) return reject(FTD_ERR_INVALID_ARG, "cfg is NULL");
     const ftd_config c = *cfg;
-    if (!q || !k_new || !v_new || !k_cache || !v_cache || !seq_lens || !out)
-        return reject(FTD_ERR_INVALID_ARG, "q, k_new, v_new, k_cache, v_cache, seq_lens and out must be non-NULL");
-    if (c.max_batch < 1 || c.max_batch > ftd::kMaxBatch || c.n_kv_heads < 1 || c.n_q_heads < c.n_kv_heads ||
-        c.n_q_heads % c.n_kv_heads != 0 || c.max_len < 16 || c.max_len % 16 != 0)
-        return reject(FTD_ERR_INVALID_ARG, "bad batch / head / length configuration (same rules as ftd_init)");
-    if (c.head_dim != 64 && c.head_dim != 128) return reject(FTD_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-    if (c.qkv_dtype != FTD_F32 && c.qkv_dtype != FTD_F16 && c.qkv_dtype != FTD_BF16)
-        return reject(FTD_ERR_UNSUPPORTED, "qkv_dtype must be F32, F16 or BF16");
-    if (!(c.softmax_scale >= 0.f) || !std::isfinite(c.softmax_scale))
-        return reject(FTD_ERR_INVALID_ARG, "softmax_scale must be finite and >= 0");
-    if (c.out_dtype != FTD_F32 && c.out_dtype != FTD_F16 && c.out_dtype != FTD_BF16)
-        return reject(FTD_ERR_UNSUPPORTED, "out_dtype must be F32, F16 or BF16");
-    if (c.window < 0) return reject(FTD_ERR_INVALID_ARG, "window must be >= 0");
+    // the same checks and kernel choice as ftd_init and ftd_decode_mha
+    ftd::Plan plan{};
+    char msg[256];
+    ftd_status st = ftd::plan_config(c, &plan, msg, sizeof msg);
+    if (st != FTD_OK) return reject(st, msg);
     if (c.page_size != 0) return reject(FTD_ERR_INVALID_ARG, "paged caches need a context (ftd_init)");
-    if (c.q_len < 0 || c.q_len > ftd::kMaxQLen) return reject(FTD_ERR_INVALID_ARG, "q_len outside 0..64");
+    st = ftd::check_pointers(c, q, k_new, v_new, qkv_bias, seq_lens, k_cache, v_cache, scales, out, msg, sizeof msg);
+    if (st != FTD_OK) return reject(st, msg);
     const bool i8 = c.cache_dtype == FTD_I8;
-    if (i8 && !scales) return reject(FTD_ERR_INVALID_ARG, "an INT8 cache needs its scales");
-    auto a16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (!a16(k_cache) || !a16(v_cache) || !a16(out) || (i8 && !a16(scales)))
-        return reject(FTD_ERR_INVALID_ARG, "caches, scales and out must be 16-byte aligned");
-
     const int g = c.n_q_heads / c.n_kv_heads;
     const int nq = c.q_len > 1 ? c.q_len : 1;
-    int G = 8;
-    while ((nq * g) % G) G >>= 1;
-    const int nhb = nq * g / G;
-    ftd::KernelInfo ki{};
-    switch (c.cache_dtype) {
-        case FTD_F32: ki = ftd::select_f32(c.head_dim, G); break;
-        case FTD_F16: ki = ftd::select_f16(c.head_dim, G); break;
-        case FTD_BF16: ki = ftd::select_bf16(c.head_dim, G); break;
-        case FTD_I8: ki = ftd::select_i8(c.head_dim, G); break;
-        default: return reject(FTD_ERR_UNSUPPORTED, "cache_dtype");
-    }
-    if (!ki.fn) return reject(FTD_ERR_UNSUPPORTED, "no kernel for this configuration");
-    if (static_cast<size_t>(c.max_batch) * c.n_kv_heads * c.max_len >= (static_cast<size_t>(1) << 31))
-        return reject(FTD_ERR_UNSUPPORTED, "cache too large for 32-bit row indices");
-    // the same kernel choice as ftd_init: the tensor-core kernel where it applies
-    const ftd::TcChoice tcc = ftd::choose_tc(c);
+    const int nhb = plan.nhb;
+    const ftd::KernelInfo ki = plan.ki;
+    const ftd::TcChoice tcc = plan.tcc;
     const bool use_tc = tcc.tki.fn != nullptr;
     const void* fn = use_tc ? tcc.tki.fn : ki.fn;
     const int smem = use_tc ? tcc.tki.smem : ki.smem;
@@ -180,6 +155,8 @@ extern "C" ftd_status ftd_decode_mha_noalloc(const ftd_config* cfg, const void* 
     p.out_dtype = static_cast<int>(c.out_dtype);
     p.window = c.window;
     p.nq = nq;
+    p.wait_cycles = ftd::wait_cycles_for(c, dev);
+    p.stall = 0;
 
     cudaError_t e;
     if (use_tc) {

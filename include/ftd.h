@@ -118,7 +118,19 @@ typedef struct {
     int page_size;         /* 0: contiguous cache; else a power of two >= 128 */
     int num_pages;         /* pages in the pool when page_size > 0 */
     int q_len;             /* new tokens per slot per step, 0 or 1 .. 64 (0 = 1) */
+    int kernel;            /* FTD_KERNEL_AUTO (0): the library's choice;
+                              FTD_KERNEL_CUDA_CORE (1): the CUDA-core split-K kernel
+                              for every configuration (the tensor-core kernel is
+                              otherwise taken for head_dim 128 caches whose kv heads
+                              carry a multiple of 4 query rows, 8 for INT8) */
+    int wait_limit_us;     /* 0: a kernel's bounded waits give up after about 2 s;
+                              else after this many microseconds (measured in SM clock
+                              cycles at the device's peak clock), raising
+                              FTD_ERR_DEVICE_TIMEOUT.  The drain of copies still in
+                              flight after such an abort always keeps the 2 s limit. */
 } ftd_config;
+
+enum { FTD_KERNEL_AUTO = 0, FTD_KERNEL_CUDA_CORE = 1 };
 
 typedef struct ftd_ctx ftd_ctx;
 
@@ -136,9 +148,13 @@ typedef struct ftd_ctx ftd_ctx;
 ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out);
 
 /*
- * ftd_cache_ptrs -- device addresses of the context's own pool.
- * Any output pointer may be NULL.  *scales is NULL unless the cache is INT8.
- * The caller may fill the cache (prefill) through these pointers.
+ * ftd_cache_ptrs -- device addresses of the context's own pool: the K and V
+ * caches [B][Hkv][Lmax][D] (pages for a paged context) and the INT8 scale
+ * planes, i.e. the per-sequence cache pointers of the decoding state that
+ * intelliparadigm.com section 3.2 keeps for each request, and the buffer that
+ * framerc.cn section 3.2 pre-allocates once.  Any output pointer may be NULL.
+ * *scales is NULL unless the cache is INT8.  The caller may fill the cache
+ * (prefill) through these pointers.  Returns INVALID_ARG for a NULL ctx.
  */
 ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** scales);
 
@@ -159,9 +175,10 @@ ftd_status ftd_cache_ptrs(ftd_ctx* ctx, void** k_cache, void** v_cache, float** 
  * The kernel is launched with programmatic dependent launch: it may start
  * while the preceding kernel on the stream finishes, if that kernel allows
  * it (this library's decode kernels do, right after their own start).  Before
- * it waits for that kernel it reads only seq_lens (and prefetches cache lines
- * into L2, which is always safe), so a preceding kernel that allows an early
- * start must not write seq_lens after allowing it.
+ * it waits for that kernel it reads only seq_lens, to plan its work and to
+ * prefetch cache lines into L2 (always safe); after the wait it reads seq_lens
+ * again and re-plans if they changed, so a preceding kernel may write seq_lens
+ * (for example the caller's seq_lens += accepted kernel).
  * A paged context (page_size > 0) is refused with INVALID_ARG.
  */
 ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
@@ -171,9 +188,11 @@ ftd_status ftd_decode_mha(ftd_ctx* ctx, const void* q, const void* k_new, const 
 /*
  * ftd_decode_mha_current -- ftd_decode_mha with the specified ten-argument
  * signature (no context handle): it runs on the most recently initialised
- * context that has not been destroyed, and returns FTD_ERR_INVALID_ARG when
- * there is none.  For a process that holds one context; with several, pass
- * the handle to ftd_decode_mha instead.
+ * context that has not been destroyed (destroying it makes the one initialised
+ * before it current again), and returns FTD_ERR_INVALID_ARG when there is
+ * none.  It holds a library lock while it launches, so an ftd_destroy in
+ * another thread waits for it.  For a process that holds one context; with
+ * several, pass the handle to ftd_decode_mha instead.
  */
 ftd_status ftd_decode_mha_current(const void* q, const void* k_new, const void* v_new, const void* qkv_bias,
                                   void* k_cache, void* v_cache, const int32_t* seq_lens, float* scales,
@@ -207,7 +226,8 @@ ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, 
 
 /*
  * ftd_decode_mha_host -- the same step for callers whose per-step inputs live
- * in host memory.  q, k_new, v_new, qkv_bias (nullable), seq_lens and out are
+ * in host memory (the host input-id update, kernel launches and device-to-host
+ * read of the output that one decode step makes in lmnt.cn section 3.3).  q, k_new, v_new, qkv_bias (nullable), seq_lens and out are
  * HOST pointers; the caches stay on the device as in ftd_decode_mha (NULL =
  * the pool).  When every one of them is pinned, GPU-addressable memory
  * (cudaHostAlloc / cudaHostRegister; 16-byte aligned, seq_lens 4-byte) the
@@ -224,13 +244,20 @@ ftd_status ftd_decode_mha_host(ftd_ctx* ctx, const void* q, const void* k_new, c
 
 /*
  * ftd_get_error -- synchronise the stream of the context's last call, then
- * read and clear the sticky device error word.  Returns FTD_OK,
+ * read and clear the sticky device error word.  A sequence that outgrows the
+ * pre-allocated length is an error the caller must see, not a silent
+ * overwrite (framerc.cn section 3.2; lmnt.cn section 5.2); the kernels skip
+ * such a slot and set the word instead of trapping.  Returns FTD_OK,
  * FTD_ERR_SEQ_OVERFLOW, FTD_ERR_BAD_PAGE, FTD_ERR_DEVICE_TIMEOUT or
- * FTD_ERR_CUDA (the most serious first when several bits are set).
+ * FTD_ERR_CUDA (the most serious first when several bits are set).  After a
+ * timeout it also resets the split-K counters, so the next call starts clean.
  */
 ftd_status ftd_get_error(ftd_ctx* ctx);
 
-/* ftd_destroy -- free the pool (synchronises the device first).  NULL is a no-op. */
+/* ftd_destroy -- free the pool (synchronises the device first).  NULL is a
+ * no-op.  The context must not be in use by another thread's call; if it is
+ * the current context of ftd_decode_mha_current, the most recently initialised
+ * of the remaining live contexts becomes current. */
 void ftd_destroy(ftd_ctx* ctx);
 
 /* ftd_status_str -- static name of a status code. */
@@ -242,6 +269,17 @@ const char* ftd_last_error(void);
 /* ftd_kernel_launches -- number of kernels this library has launched in this
  * process (every decode call adds one; host-side failures add none). */
 uint64_t ftd_kernel_launches(void);
+
+/*
+ * ftd_debug_stall_next -- test hook for the bounded-wait error path; the pages
+ * have no counterpart.  The next `calls` decode calls on ctx withhold the first
+ * tile copy of block 0, so that block's waits run out after the context's
+ * wait_limit_us, it drains what it has in flight and returns, and
+ * ftd_get_error reports FTD_ERR_DEVICE_TIMEOUT (and resets the counters).
+ * Outputs of such a call are undefined.  Nothing faults and nothing hangs:
+ * every wait is bounded.  calls = 0 cancels.
+ */
+ftd_status ftd_debug_stall_next(ftd_ctx* ctx, int calls);
 
 /* Size of the fixed device array that ftd_decode_mha_noalloc uses as scratch. */
 #define FTD_NOALLOC_SCRATCH_BYTES (8u << 20)
@@ -272,10 +310,13 @@ uint64_t ftd_kernel_launches(void);
  * call (a context caches them), so its results are ftd_decode_mha's bytes.
  * Its split-K partials, counters and error word live in one static device
  * array of FTD_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the
- * library holds until the process exits.  A configuration that needs more
- * (max_batch * n_kv_heads * heads-per-kv-block slots plus 8 per SM, each of
- * about head_dim * 4 bytes per query head of a block) is rejected with
- * FTD_ERR_INVALID_ARG and a message in ftd_last_error().
+ * library holds until the process exits.  A configuration that needs more is
+ * rejected with FTD_ERR_INVALID_ARG, and ftd_last_error() gives the bytes it
+ * needs.  The need is one partial slot per segment (max_batch * n_kv_heads *
+ * query-row blocks per kv head) plus, per SM, one slot per worker: the CUDA-core
+ * kernel's warps per block (8, or 12 for INT8 caches with blocks of at most 2
+ * query rows), or 1 for the tensor-core kernel; a slot holds (2 + head_dim)
+ * floats per query row of a block, plus counters and the error word.
  * The first call on each device does a one-time set-up with that device
  * current (it looks up the array's device address and raises the kernel's
  * shared-memory limit); make that first call before any stream capture.

@@ -28,19 +28,12 @@ def host(t, like):
 
 
 def make_step(w, softmax_scale=0.0, force_cuda_core=False, **opts):
-    """A library context; force_cuda_core selects the CUDA-core kernel for grouped caches.
-    opts: out_dtype, window, page_size, num_pages (the config's option fields)."""
-    import os
-    old = os.environ.get("FTD_FORCE_CUDA_CORE")
-    os.environ["FTD_FORCE_CUDA_CORE"] = "1" if force_cuda_core else "0"
-    try:
-        return ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, softmax_scale,
-                              **opts)
-    finally:
-        if old is None:
-            del os.environ["FTD_FORCE_CUDA_CORE"]
-        else:
-            os.environ["FTD_FORCE_CUDA_CORE"] = old
+    """A library context; force_cuda_core selects the CUDA-core kernel for grouped caches
+    (the config's kernel field).  opts: out_dtype, window, page_size, num_pages, q_len,
+    wait_limit_us (the config's option fields)."""
+    kernel = ftd.FTD_KERNEL_CUDA_CORE if force_cuda_core else ftd.FTD_KERNEL_AUTO
+    return ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, softmax_scale,
+                          kernel=kernel, **opts)
 
 
 TORCH_OUT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
@@ -207,3 +200,39 @@ def rising_scores(w, inp, rise_log2=40.0, seed=5):
     k = 0.3 * k + ramp[None, None, :, None] * u[None, :, None, :]
     return dict(inp, q=to_storage(q.astype(np.float32), w.qkv_dtype),
                 k_cache=to_storage(k.astype(np.float32), w.cache_dtype))
+
+
+def rising_scores_i8(w, inp, rise_log2=40.0, seed=5):
+    """rising_scores for an INT8 cache: the keys' history rows (positions before each slot's
+    length) become 0.3 x the dequantised key plus the same ramp along u, and are quantised
+    again per (slot, kv head, position) row with the scale max|k| / 127.  Rows from the
+    length on keep their fill (code 127 with a NaN scale)."""
+    rng = np.random.default_rng(seed)
+    D, g = w.D, w.Hq // w.Hkv
+    u = rng.standard_normal((w.Hkv, D))
+    u /= np.linalg.norm(u, axis=1, keepdims=True)
+    A = 12.0
+    sq = rise_log2 * np.sqrt(D) / (A * np.log2(np.e))
+    q = _from_storage(inp["q"], w.qkv_dtype).astype(np.float64)
+    lead = q.shape[:-2]
+    heads = np.repeat(u, g, axis=0)
+    q = sq * np.broadcast_to(heads, lead + heads.shape) + 0.1 * q
+    codes = inp["k_cache"].copy()
+    scales = inp["scales"].copy()
+    ramp = A * np.arange(w.Lmax, dtype=np.float64) / w.Lmax
+    for b, L in enumerate(np.asarray(inp["seq_lens"])):
+        n = int(min(max(L, 0), w.Lmax))
+        if n == 0:
+            continue
+        k = codes[b, :, :n].astype(np.float64) * scales[0, b, :, :n, None].astype(np.float64)
+        k = 0.3 * k + ramp[None, :n, None] * u[:, None, :]
+        s = (np.max(np.abs(k), axis=-1) / 127.0).astype(np.float32)
+        codes[b, :, :n] = np.clip(np.rint(k / s[..., None].astype(np.float64)), -127, 127).astype(np.int8)
+        scales[0, b, :, :n] = s
+    return dict(inp, q=to_storage(q.astype(np.float32), w.qkv_dtype), k_cache=codes, scales=scales)
+
+
+def scale_q(w, inp, factor):
+    """The same inputs with the query multiplied by ``factor`` (stored again in the qkv dtype)."""
+    q = _from_storage(inp["q"], w.qkv_dtype) * np.float32(factor)
+    return dict(inp, q=to_storage(q, w.qkv_dtype))

@@ -43,7 +43,7 @@ def test_status_strings(lib):
 def cfg(**kw):
     base = dict(max_batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, max_len=256,
                 qkv_dtype=ftd.FTD_BF16, cache_dtype=ftd.FTD_BF16, softmax_scale=0.0,
-                out_dtype=ftd.FTD_F32, window=0, page_size=0, num_pages=0, q_len=0)
+                out_dtype=ftd.FTD_F32, window=0, page_size=0, num_pages=0, q_len=0, kernel=0, wait_limit_us=0)
     base.update(kw)
     return ftd.FtdConfig(*[base[f] for f, _ in ftd.FtdConfig._fields_])
 
@@ -72,6 +72,11 @@ def cfg(**kw):
     (dict(page_size=384, num_pages=8), ftd.FTD_ERR_INVALID_ARG),
     (dict(q_len=-1), ftd.FTD_ERR_INVALID_ARG),
     (dict(q_len=65), ftd.FTD_ERR_INVALID_ARG),
+    (dict(kernel=2), ftd.FTD_ERR_INVALID_ARG),
+    (dict(kernel=-1), ftd.FTD_ERR_INVALID_ARG),
+    (dict(wait_limit_us=-5), ftd.FTD_ERR_INVALID_ARG),
+    # rows fit 32 bits (1024 x 1 x 2^20) but the tile space of 4096 query rows per kv head does not
+    (dict(max_batch=1024, n_q_heads=64, n_kv_heads=1, max_len=1 << 20, q_len=64), ftd.FTD_ERR_UNSUPPORTED),
 ])
 def test_init_rejects_bad_config(lib, kw, status):
     st, ctx = ftd.ftd_init(cfg(**kw))
@@ -90,6 +95,7 @@ def test_null_arguments(lib):
     assert ftd.ftd_decode_mha_paged(0, 16, 16, 16, 0, 16, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_get_error(0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_cache_ptrs(0)[0] == ftd.FTD_ERR_INVALID_ARG
+    assert ftd.ftd_debug_stall_next(0, 1) == ftd.FTD_ERR_INVALID_ARG
     ftd.ftd_destroy(0)  # no-op
     # without a live context the handle-free entry point refuses (no context exists on a CPU host)
     assert ftd.ftd_decode_mha_current(16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
@@ -118,6 +124,27 @@ def test_noalloc_rejects_paged_and_bad_options(lib):
         st = ftd.ftd_decode_mha_noalloc(cfg(**kw), 16, 16, 16, 0, 16, 16, 16, 0, 16, 0, 0)
         assert st in (ftd.FTD_ERR_INVALID_ARG, ftd.FTD_ERR_UNSUPPORTED), kw
         assert ftd.ftd_last_error() != ""
+
+
+def test_noalloc_applies_the_context_paths_checks(lib):
+    """The no-allocation entry point makes ftd_init's and ftd_decode_mha's checks: the 32-bit
+    tile-space bound and the natural alignment of every pointer, before any device work."""
+    huge = cfg(max_batch=1024, n_q_heads=64, n_kv_heads=1, max_len=1 << 20, q_len=64)
+    assert ftd.ftd_decode_mha_noalloc(huge, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0, 0) == ftd.FTD_ERR_UNSUPPORTED
+    assert "tile indices" in ftd.ftd_last_error()
+    ok = dict(q=16, k_new=16, v_new=16, bias=0, k_cache=256, v_cache=512, seq_lens=16, scales=0, out=1024)
+    for name, bad in (("q", 17), ("k_new", 33), ("v_new", 49), ("bias", 3), ("seq_lens", 18), ("k_cache", 264),
+                      ("v_cache", 520), ("out", 1032)):
+        a = dict(ok, **{name: bad})
+        st = ftd.ftd_decode_mha_noalloc(cfg(), a["q"], a["k_new"], a["v_new"], a["bias"], a["k_cache"],
+                                        a["v_cache"], a["seq_lens"], a["scales"], a["out"], 0, 0)
+        assert st == ftd.FTD_ERR_INVALID_ARG, name
+        assert "aligned" in ftd.ftd_last_error(), name
+    i8 = cfg(cache_dtype=ftd.FTD_I8, qkv_dtype=ftd.FTD_F16)
+    st = ftd.ftd_decode_mha_noalloc(i8, 16, 16, 16, 0, 256, 512, 16, 0, 1024, 0, 0)
+    assert st == ftd.FTD_ERR_INVALID_ARG and "scales" in ftd.ftd_last_error()
+    st = ftd.ftd_decode_mha_noalloc(i8, 16, 16, 16, 0, 256, 512, 16, 8, 1024, 0, 0)
+    assert st == ftd.FTD_ERR_INVALID_ARG and "aligned" in ftd.ftd_last_error()
 
 
 def test_missing_library_fails_loudly(tmp_path):

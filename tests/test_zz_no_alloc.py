@@ -152,3 +152,47 @@ def test_noalloc_int8_grouped_runs_the_tensor_core_kernel():
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
     assert np.array_equal(caches[0][0], caches[1][0]) and np.array_equal(caches[0][1], caches[1][1])
     assert np.array_equal(caches[0][2].view(np.uint32), caches[1][2].view(np.uint32))
+
+
+@pytest.mark.parametrize("cache", ["bf16", "i8"])
+def test_noalloc_matches_the_oracle_with_and_without_an_error_word(cache):
+    """Against the float64 oracle (not only against ftd_decode_mha), two calls in a row: the first
+    with an error word, the second with device_err NULL (its overflow bit is dropped, the
+    overflowing slot still gets a zero output and an untouched cache)."""
+    import oracle
+    import torch
+    from tests.gpu_util import TOL_MAXABS_I8, assert_same_bytes
+    qkv = "f16" if cache == "i8" else "bf16"
+    w = Workload("noalloc", B=5, Hq=16, Hkv=2, D=128, Lmax=1024, qkv_dtype=qkv, cache_dtype=cache,
+                 bias_std=0.1, scale_range=(0.01, 0.05), seed=26)
+    inp = gen_all(w, seed=26, seq_lens=np.array([1000, 1024, 3, 511, -1], np.int32), fill_beyond="nan")
+    ref = oracle.load().decode_step(w, inp, nthreads=8)
+    dt = ftd.DTYPES
+    cfg = ftd.FtdConfig(w.B, w.Hq, w.Hkv, w.D, w.Lmax, dt[qkv], dt[cache], 0.0)
+    s = torch.cuda.current_stream().cuda_stream
+    q, kn, vn, bias, sl = (dev(inp[k]) for k in ("q", "k_new", "v_new", "bias", "seq_lens"))
+    for call, with_err in enumerate((True, False)):
+        kc, vc = dev(inp["k_cache"]), dev(inp["v_cache"])
+        sc = dev(inp["scales"]) if cache == "i8" else None
+        out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        st = ftd.ftd_decode_mha_noalloc(cfg, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), bias.data_ptr(),
+                                        kc.data_ptr(), vc.data_ptr(), sl.data_ptr(),
+                                        0 if sc is None else sc.data_ptr(), out.data_ptr(),
+                                        err.data_ptr() if with_err else 0, s)
+        assert st == ftd.FTD_OK, ftd.ftd_last_error()
+        torch.cuda.synchronize()
+        assert int(err.item()) == (1 if with_err else 0), f"call {call}: error word"
+        got = out.double().cpu().numpy()
+        assert np.all(np.isfinite(got)), f"call {call}"
+        d = np.max(np.abs(got - ref["out"]))
+        if cache == "i8":
+            assert d <= TOL_MAXABS_I8, f"call {call}: max-abs {d:.3e}"
+        else:
+            assert d <= TOL_MAXABS, f"call {call}: max-abs {d:.3e}"
+            assert np.linalg.norm(got - ref["out"]) / np.linalg.norm(ref["out"]) <= TOL_RELL2, f"call {call}"
+        assert not got[1].any() and not got[4].any(), f"call {call}: overflowing / inactive slots"
+        kh = kc.cpu().numpy()
+        assert_same_bytes(kh.view(ref["k_cache"].dtype), ref["k_cache"], f"call {call}: K cache")
+        if cache == "i8":
+            assert_same_bytes(sc.cpu().numpy(), ref["scales"], f"call {call}: scales")
