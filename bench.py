@@ -12,9 +12,10 @@ cache from HBM.  The default workload is the largest one, the 13B-shaped
 ragged continuous batch.  Rank 0 prints one JSON line.
 
 Every workload is timed two ways: back to back (graph-replayed steps; each
-step may start while the previous one drains), and isolated (each step follows
-a 320 MB device copy on the same stream, as a decode step follows the
-projection kernels in a model, so it starts cold, with nothing of it in L2).
+step may start while the previous one drains), and isolated (each step follows,
+on the same stream, a projection-shaped GEMM that streams 285 MB of bf16
+weights, as a decode step follows the projection kernels in a model: it starts
+cold, with nothing of it in L2 and no early start).
 
 With ``--gpus N`` under torchrun every rank runs an independent replica (its
 own batch; the decode step needs no collective), ``value`` is the aggregate of
@@ -177,7 +178,8 @@ def n_pools_for(w, kv_bytes):
     return int(max(2, min(4, np.ceil(300e6 / kv_bytes) + 1)))
 
 
-FLUSH_BYTES = 160 << 20  # each isolated step follows a copy of this many bytes (320 MB of traffic)
+# each isolated step follows a GEMM [16 x 8192] . [8192 x 17408] of bf16: 285 MB of weights (> 2x L2)
+FLUSH_GEMM = (16, 8192, 17408)
 
 
 def decode_call(step, pools, inp, stream):
@@ -198,23 +200,35 @@ def decode_call(step, pools, inp, stream):
     return one
 
 
+def make_flush(device):
+    """The isolated steps' predecessor: a GEMM X . W (cuBLAS, bf16) whose weights W exceed
+    2x L2, the shape of a decode step's projection; returns a function that issues it."""
+    import torch
+    m, k, n = FLUSH_GEMM
+    g = torch.Generator(device=device)
+    g.manual_seed(7)
+    x = torch.randn((m, k), device=device, generator=g).to(torch.bfloat16)
+    wt = torch.randn((k, n), device=device, generator=g).to(torch.bfloat16)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+    return lambda: torch.matmul(x, wt, out=y)
+
+
 def run_isolated(step, pools, inp, n, stream, flush):
-    """n steps, each preceded on the same stream by a device copy larger than 2x L2
-    (flush = (src, dst) byte tensors).  The copy is not a decode launch, so the step
-    cannot overlap a previous step, and it evicts the step's inputs from L2.  Each
-    step is timed alone with CUDA events recorded right before and after it.
-    Returns the per-step times in µs."""
+    """n steps, each preceded on the same stream by the projection-shaped GEMM of
+    make_flush(): it streams more than 2x L2 of weights, so the step starts with
+    nothing of its own in L2, and it is not a decode launch, so the step cannot
+    overlap a previous step.  Each step is timed alone with CUDA events recorded
+    right before and after it.  Returns the per-step times in µs."""
     import torch
     import decode_step_masked_gb300 as ftd
     one = decode_call(step, pools, inp, stream)
-    src, dst = flush
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     with torch.cuda.stream(stream):
         for i in range(3):  # warm-up
-            dst.copy_(src)
+            flush()
             one(i)
         for i, (e0, e1) in enumerate(evs):
-            dst.copy_(src)
+            flush()
             e0.record(stream)
             one(i)
             e1.record(stream)
@@ -527,7 +541,9 @@ def roofline(w, by, r, us, peaks, q_len=1):
     if iso is not None and len(iso):
         med = float(np.median(iso))
         d.update(isolated_us=med, isolated_p99_us=float(np.percentile(iso, 99)), isolated_steps=len(iso),
-                 isolated_frac=by["total"] / (med * 1e-6) / 1e9 / peaks["hbm_gbs"])
+                 isolated_frac=by["total"] / (med * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                 isolated_after="bf16 GEMM %dx%dx%d (%.0f MB of weights), events around the step alone"
+                 % (FLUSH_GEMM + (FLUSH_GEMM[1] * FLUSH_GEMM[2] * 2 / 1e6,)))
     return d
 
 
@@ -565,10 +581,7 @@ def main():
     ftd.load_library()
     stream = torch.cuda.Stream(device=device)
     peaks = load_peaks()
-    # the isolated steps' predecessor: a device copy of FLUSH_BYTES (> 2x L2 of traffic)
-    flush = (torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device),
-             torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device))
-    flush[0].fill_(1)
+    flush = make_flush(device)  # the isolated steps' predecessor
 
     # ---- headline: the named workload, K timed steps ----
     sampler = ClockSampler(gpu_id_for(local))

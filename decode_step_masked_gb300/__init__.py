@@ -33,7 +33,8 @@ DTYPES = {"f32": FTD_F32, "f16": FTD_F16, "bf16": FTD_BF16, "i8": FTD_I8}
 # Symbols include/ftd.h declares; the loader checks each one is exported.
 EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_current", "ftd_decode_mha_paged",
            "ftd_decode_mha_host", "ftd_get_error", "ftd_destroy", "ftd_status_str", "ftd_last_error",
-           "ftd_kernel_launches", "ftd_decode_mha_noalloc", "ftd_debug_stall_next")
+           "ftd_kernel_launches", "ftd_decode_mha_noalloc", "ftd_debug_stall_next",
+           "ftd_debug_late_lengths")
 
 
 class FtdConfig(ctypes.Structure):
@@ -93,6 +94,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ftd_decode_mha_noalloc.restype = I
     lib.ftd_debug_stall_next.argtypes = [P, I]
     lib.ftd_debug_stall_next.restype = I
+    lib.ftd_debug_late_lengths.argtypes = [P, P, I, I, P]
+    lib.ftd_debug_late_lengths.restype = I
     if path == LIB:
         _lib = lib
     return lib
@@ -164,6 +167,11 @@ def ftd_decode_mha_noalloc(cfg: FtdConfig, q, k_new, v_new, qkv_bias, k_cache, v
 def ftd_debug_stall_next(ctx, calls: int) -> int:
     """Test hook: the next ``calls`` decode calls withhold one tile copy (bounded-wait error path)."""
     return load_library().ftd_debug_stall_next(ctypes.c_void_p(ctx), int(calls))
+
+
+def ftd_debug_late_lengths(src, dst, n: int, delay_us: int, stream) -> int:
+    """Test hook: a kernel that lets the next launch start at once and copies n lengths src -> dst late."""
+    return load_library().ftd_debug_late_lengths(src, dst, int(n), int(delay_us), stream)
 
 
 def ftd_get_error(ctx) -> int:

@@ -381,8 +381,23 @@ struct PassSplit {
 // For INT8 caches kBarFull / kBarEmpty guard the K halves of the converted
 // operand stages, kBarFullV / kBarEmptyV their V halves, kBarFull8 / kBarEmpty8
 // the raw stages, and kBarScale the four scale slots.
+// kBarDrain takes the MMA issuer's last commit, which completes once every MMA it issued has.
 enum : int { kBarFull = 0, kBarEmpty = 3, kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarQReady = 12,
-             kBarFull8 = 13, kBarEmpty8 = 15, kBarFullV = 17, kBarEmptyV = 19, kBarScale = 21, kNumBars = 25 };
+             kBarFull8 = 13, kBarEmpty8 = 15, kBarFullV = 17, kBarEmptyV = 19, kBarScale = 21, kBarDrain = 25,
+             kNumBars = 26 };
+// after the barriers: the TMEM base, the abort flag, the merge broadcast and the re-planning counter
+static_assert(kNumBars * 8 + 16 <= 256, "misc area");
+
+// After an abort (a cold path, kept out of line like replan so it leaves the code
+// of the streaming loops as it is): wait (long drain limit) for the producer's copies still in flight,
+// the last `stages` tiles before tile k_end (a withheld tile 0 excepted), on the full
+// barriers full0 + kk % stages, phase (kk / stages) & 1.
+static __device__ __noinline__ void tc_drain_copies(uint32_t full0, int stages, int k_end, bool withheld0, uint32_t* err) {
+    for (int kk = max(0, k_end - stages); kk < k_end; ++kk)
+        if (!(withheld0 && kk == 0))
+            mbar_wait_bounded(full0 + 8u * static_cast<uint32_t>(kk % stages), static_cast<uint32_t>((kk / stages) & 1),
+                              err, kDrainLimitCycles);
+}
 
 // MQ: several new tokens per slot (q_len > 1), so the columns of S carry
 // their own causal limits; without it every column shares one row range.
@@ -418,6 +433,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + LY::OFF_MISC + kNumBars * 8);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + LY::OFF_MISC + kNumBars * 8 + 4);
     int* bcast = reinterpret_cast<int*>(smem + LY::OFF_MISC + kNumBars * 8 + 8);
+    int* rv = reinterpret_cast<int*>(smem + LY::OFF_MISC + kNumBars * 8 + 12);  // re-planning meeting counter
     int* P = reinterpret_cast<int*>(smem + LY::OFF_PREFIX);
     int* Ls = P + (kMaxBatch + 1);
     int* VP = LY::HAVE_VP ? Ls + kMaxBatch : P;
@@ -428,6 +444,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) mbar_init(bar(i), 1);
         *abort_flag = 0;
+        *rv = 0;
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
@@ -476,102 +493,17 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
     }
     grid_dep_wait();    // inputs, caches and outputs may be in use by the previous launch
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
-
-    // ---- TMA producer state (thread 0) ----
-    // Test hook (DecodeParams::stall): block 0 never issues its first tile, so the
-    // bounded waits of its consumers run out and the abort path runs.
-    const bool withhold0 = p.stall && blockIdx.x == 0;
-    Cursor pcu{};        // the producer's cursor: the next tile to issue
-    PageCursor pages;
-    const uint64_t l2pol = l2_stream_policy();
-    // Issue tile k at pcu (waiting for its stage to be free from the third tile on)
-    // and advance; false when the wait gave up.
-    auto produce = [&](int k) -> bool {
-        const int s = k % NS;
-        // the tile's address first: a block-table load then overlaps the wait for a free stage
-        const int kvh = pcu.seg / p.nhb;
-        const int t0 = (window_start(Ls[pcu.b], p.window) / TM + pcu.tile) * TM;
-        long long rb = cache_row(p, pcu.b, kvh, t0, pages.page(p, pcu.b, t0));
-        if (rb < 0) {  // bad page: flag it and read row 0 instead (the slot's output is undefined)
-            atomicOr(p.err, kErrBadPage);
-            rb = 0;
-        }
-        const int row0 = static_cast<int>(rb);
-        if constexpr (I8) {
-            // raw stage: K and V codes (one 128 x 128 B box each) and the scales
-            // of the rows before the new tokens
-            const int s8 = k & 1;
-            if (k >= 2 && !tc::wait_or_abort(bar(kBarEmpty8 + s8), ((k >> 1) - 1) & 1, p.err, abort_flag, p.wait_cycles))
-                return false;
-            const int n_cache = min(TM, max(0, Ls[pcu.b] - t0));
-            const uint32_t sb = static_cast<uint32_t>((n_cache * 4 + 15) & ~15);
-            unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
-            const uint32_t fb = bar(kBarFull8 + s8);
-            if (!(withhold0 && k == 0)) {
-                mbar_arrive_expect_tx(fb, 2 * TM * D + 2 * sb);
-                tc::tma_load_2d(smem_addr(st8), &tmk, 0, row0, fb, l2pol);
-                tc::tma_load_2d(smem_addr(st8 + TM * D), &tmv, 0, row0, fb, l2pol);
-                if (sb) {
-                    bulk_g2s_hint(smem_addr(st8 + 2 * TM * D), p.k_scales + rb, sb, fb, l2pol);
-                    bulk_g2s_hint(smem_addr(st8 + 2 * TM * D + TM * 4), p.v_scales + rb, sb, fb, l2pol);
-                }
-            }
-        } else {
-            if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag, p.wait_cycles))
-                return false;
-            const uint32_t st = smem_addr(stages + s * tc::STAGE);
-            if (!(withhold0 && k == 0)) {
-                mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
-                tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s), l2pol);
-                tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
-                tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
-                tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
-            }
-        }
-        if (k + 1 < n_my) advance_pass(pcu, P, p.B, spp, np);
-        return true;
-    };
-    // The first stages' worth of tiles (no stage to wait for) are issued at once; the
-    // lengths are checked again while they are in flight.
-    constexpr int kFirst = I8 ? 2 : NS;
-    int prod_k = 0;      // tiles the producer got to (issued or withheld)
-    auto start = [&]() {
-        prod_k = 0;
-        if (tid != 0 || n_my <= 0) return;
-        pcu = locate_pass(t_begin, P, p.B, spp, np);
-        for (; prod_k < min(kFirst, n_my); ++prod_k) produce(prod_k);
-    };
-    start();
-    if (lengths_changed(p, Ls)) {
-        // (rare) the plan was built from stale lengths: let the copies issued from it
-        // land, reset the barriers, rebuild the plan from the lengths now visible, start again
-        bool failed = false;
-        if (tid == 0) {
-            for (int kk = 0; kk < prod_k; ++kk) {
-                if (withhold0 && kk == 0) continue;
-                failed |= !mbar_wait_bounded(bar((I8 ? kBarFull8 + (kk & 1) : kBarFull + kk % NS)), 0u, p.err,
-                                             kDrainLimitCycles);
-            }
-        }
-        if (__syncthreads_or(failed)) {
-            // a copy did not land in time: leave, with the error raised and TMEM freed
-            if (warp == 1)
-                asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(LY::TMEM_COLS));
-            return;
-        }
-        if (tid == 0) {
-            for (int i = 0; i < kNumBars; ++i) {
-                mbar_inval(bar(i));
-                mbar_init(bar(i), 1);
-            }
-        }
-        fence_mbar_init();
-        if (warp == 0) ovf = build_prefix(p, TM, spp, LY::ALPHA, P, VP, Ls, lane);
-        __syncthreads();
+    if (lengths_changed(p, Ls, lane)) {
+        // (rare) the lengths changed after this block read them: the warps meet, warp 0
+        // rebuilds the split from the lengths now visible, they meet again.  If the
+        // warps disagree (the lengths changed while the step ran) the meeting gives up:
+        // the warp then skips its role, and the others' bounded waits run out.
+        const int r = replan(p, TM, spp, LY::ALPHA, P, VP, Ls, rv);
+        const bool ok = r >= 0;
+        ovf = r > 0;
         t_begin = split.begin(wid);
-        n_my = split.begin(wid + 1) - t_begin;
-        pages = PageCursor{};
-        start();
+        n_my = ok ? split.begin(wid + 1) - t_begin : 0;
+        if (!ok) *abort_flag = 1;
     }
     if (ovf && warp == 0 && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
 
@@ -581,14 +513,65 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
         }
     }
 
-    int last_bar = -1;   // MMA issuer (warp 1, lane 0): barrier and phase of its latest commit,
-    uint32_t last_par = 0;  // which completes once every MMA issued before it has
+    // Test hook (DecodeParams::stall): block 0 never issues its first tile, so the
+    // bounded waits of its consumers run out and the abort path runs.
+    const bool withhold0 = p.stall && blockIdx.x == 0;
+    int prod_k = 0;  // producer (warp 0, lane 0): tiles it got to (issued or withheld)
     if (n_my > 0) {
         if (warp == 0) {
             // ------------------------------------------------ TMA producer
             if (lane == 0) {
-                for (; prod_k < n_my; ++prod_k)
-                    if (!produce(prod_k)) break;
+                Cursor cu = locate_pass(t_begin, P, p.B, spp, np);
+                PageCursor pages;
+                const uint64_t l2pol = l2_stream_policy();
+                int k = 0;
+                if (withhold0) {  // tile 0 is never issued
+                    if (n_my > 1) advance_pass(cu, P, p.B, spp, np);
+                    k = 1;
+                }
+                for (; k < n_my; ++k) {
+                    const int s = k % NS;
+                    // the tile's address first: a block-table load then overlaps the wait for a free stage
+                    const int kvh = cu.seg / p.nhb;
+                    const int t0 = (window_start(Ls[cu.b], p.window) / TM + cu.tile) * TM;
+                    long long rb = cache_row(p, cu.b, kvh, t0, pages.page(p, cu.b, t0));
+                    if (rb < 0) {  // bad page: flag it and read row 0 instead (the slot's output is undefined)
+                        atomicOr(p.err, kErrBadPage);
+                        rb = 0;
+                    }
+                    const int row0 = static_cast<int>(rb);
+                    if constexpr (I8) {
+                        // raw stage: K and V codes (one 128 x 128 B box each) and the scales
+                        // of the rows before the new tokens
+                        const int s8 = k & 1;
+                        if (k >= 2 && !tc::wait_or_abort(bar(kBarEmpty8 + s8), ((k >> 1) - 1) & 1, p.err, abort_flag,
+                                                         p.wait_cycles))
+                            break;
+                        const int n_cache = min(TM, max(0, Ls[cu.b] - t0));
+                        const uint32_t sb = static_cast<uint32_t>((n_cache * 4 + 15) & ~15);
+                        unsigned char* st8 = stages8 + s8 * round_up(tc::STAGE8, 1024);
+                        const uint32_t fb = bar(kBarFull8 + s8);
+                        mbar_arrive_expect_tx(fb, 2 * TM * D + 2 * sb);
+                        tc::tma_load_2d(smem_addr(st8), &tmk, 0, row0, fb, l2pol);
+                        tc::tma_load_2d(smem_addr(st8 + TM * D), &tmv, 0, row0, fb, l2pol);
+                        if (sb) {
+                            bulk_g2s_hint(smem_addr(st8 + 2 * TM * D), p.k_scales + rb, sb, fb, l2pol);
+                            bulk_g2s_hint(smem_addr(st8 + 2 * TM * D + TM * 4), p.v_scales + rb, sb, fb, l2pol);
+                        }
+                    } else {
+                        if (k >= NS && !tc::wait_or_abort(bar(kBarEmpty + s), ((k / NS) - 1) & 1, p.err, abort_flag,
+                                                          p.wait_cycles))
+                            break;
+                        const uint32_t st = smem_addr(stages + s * tc::STAGE);
+                        mbar_arrive_expect_tx(bar(kBarFull + s), tc::STAGE);
+                        tc::tma_load_2d(st, &tmk, 0, row0, bar(kBarFull + s), l2pol);
+                        tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kBarFull + s), l2pol);
+                        tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kBarFull + s), l2pol);
+                        tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kBarFull + s), l2pol);
+                    }
+                    if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
+                }
+                prod_k = k;
             }
         } else if (warp == 1) {
             // ------------------------------------------- append + MMA issue
@@ -624,8 +607,6 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     }
                     tc::mma_commit(bar(kBarOFull + (kk & 1)));
                     tc::mma_commit(bar((I8 ? kBarEmptyV : kBarEmpty) + kk % NB));
-                    last_bar = kBarOFull + (kk & 1);
-                    last_par = (kk >> 1) & 1;
                 }
                 __syncwarp();
                 return true;
@@ -720,14 +701,15 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     }
                     tc::mma_commit(bar(kBarSFull + (k & 1)));
                     if constexpr (I8) tc::mma_commit(bar(kBarEmpty + s));  // the K half is read
-                    last_bar = kBarSFull + (k & 1);
-                    last_par = (k >> 1) & 1;
                 }
                 __syncwarp();
                 if (k > 0 && !new_piece && !issue_pv(k - 1)) { ok = false; break; }
                 if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
             }
             if (ok) issue_pv(n_my - 1);
+            // one last commit: it completes once every MMA issued above has (the drain after an abort)
+            if (lane == 0) tc::mma_commit(bar(kBarDrain));
+            __syncwarp();
         } else if (I8 && ((warp >= 2 && warp < 4) || warp >= 4 + 4 * SH)) {
             // ------------------------------------- INT8: append and fp16 conversion
             // Warps 2-3 and 12-19 take the raw stages in order.  In a tile holding
@@ -1147,25 +1129,14 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
-    if (*abort_flag) {
+    if (*abort_flag && n_my > 0) {
         // Some role gave up (a bounded wait ran out).  Every role has left its loop, so
         // nothing waits on the pipeline any more; before TMEM is freed and the block
-        // exits, wait (long drain limit) for what is still in flight: the producer's
-        // last stages' worth of copies before tile prod_k (all but a withheld one), and
-        // the MMAs, through the issuer's latest commit.
-        if (warp == 0 && lane == 0) {
-            if constexpr (I8) {
-                for (int kk = max(0, prod_k - 2); kk < prod_k; ++kk)
-                    if (!(withhold0 && kk == 0))
-                        mbar_wait_bounded(bar(kBarFull8 + (kk & 1)), (kk >> 1) & 1, p.err, kDrainLimitCycles);
-            } else {
-                for (int kk = max(0, prod_k - NS); kk < prod_k; ++kk)
-                    if (!(withhold0 && kk == 0))
-                        mbar_wait_bounded(bar(kBarFull + kk % NS), (kk / NS) & 1, p.err, kDrainLimitCycles);
-            }
-        }
-        if (warp == 1 && lane == 0 && last_bar >= 0)
-            mbar_wait_bounded(bar(last_bar), last_par, p.err, kDrainLimitCycles);
+        // exits, wait for what is still in flight: the producer's copies, and the MMAs,
+        // through the issuer's last commit.
+        if (warp == 0 && lane == 0)
+            tc_drain_copies(I8 ? bar(kBarFull8) : bar(kBarFull), I8 ? 2 : NS, prod_k, withhold0, p.err);
+        if (warp == 1 && lane == 0) mbar_wait_bounded(bar(kBarDrain), 0u, p.err, kDrainLimitCycles);
     }
     if (warp == 1) {
         __syncwarp();

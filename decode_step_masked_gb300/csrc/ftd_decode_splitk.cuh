@@ -90,6 +90,7 @@ struct Tiling {
     static_assert(D % 16 == 0 && (EPL == 4 || EPL == 8), "head_dim 64 or 128");
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(G * RB <= 16 && R % RB == 0, "reduce-scatter batch");
+    static_assert(((HAVE_VP ? 3 : 2) * kMaxBatch + 3) * 4 <= PREFIX_BYTES, "room for the re-planning counter");
 };
 
 // ------------------------------------------------ shared-memory row access
@@ -278,21 +279,64 @@ __device__ __forceinline__ bool build_prefix(const DecodeParams& p, int T, int s
     return __any_sync(FULL, ovf);
 }
 
-// Whether the lengths differ from the ones the split was built from (Ls), by all
-// threads of the block.  The split is built from lengths read before
-// grid_dep_wait, so that a block placed while the previous launch drains can
-// warm L2 with its first tiles; but a preceding kernel's writes are guaranteed
-// visible only after the wait (a kernel that allows an early start, or that
-// ends without a memory flush yet, may still be writing seq_lens).  So after
-// the wait every block reads the lengths again, through L2, and rebuilds the
-// split when any of them changed.
-__device__ __forceinline__ bool lengths_changed(const DecodeParams& p, const int* Ls) {
+// Whether the lengths differ from the ones the split was built from (Ls).  The
+// split is built from lengths read before grid_dep_wait, so that a block placed
+// while the previous launch drains can warm L2 with its first tiles; but a
+// preceding kernel's writes are guaranteed visible only after the wait (a kernel
+// that allows an early start, or that has ended without its writes landing yet,
+// may still be writing seq_lens).  So after the wait every warp reads all the
+// lengths again, through L2, and votes.  All warps read the same final values,
+// so they reach the same answer without waiting for one another.
+__device__ __forceinline__ bool lengths_changed(const DecodeParams& p, const int* Ls, int lane) {
     bool changed = false;
-    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+    for (int b = lane; b < p.B; b += 32) {
         const int L = __ldcg(p.seq_lens + b);
         changed |= ((L >= 0 && L <= p.Lmax - p.nq) ? L : -1) != Ls[b];
     }
-    return __syncthreads_or(changed) != 0;
+    return __any_sync(0xffffffffu, changed);
+}
+
+// Bounded meeting of the block's nwarps warps on the re-planning path: lane 0 of
+// each warp adds 1 to the shared counter *ctr and waits until it reaches target.
+// Shared-memory writes a warp made before the call are visible to every warp after
+// it.  Returns false, with the timeout bit raised, when some warp has not come
+// within `limit` cycles: that happens only if the warps disagreed about the
+// lengths (they changed while the step ran), and it must not hang the block.
+__device__ __forceinline__ bool warp_rendezvous(int* ctr, int target, long long limit, uint32_t* err, int lane) {
+    __syncwarp();
+    bool ok = true;
+    if (lane == 0) {
+        __threadfence_block();
+        atomicAdd(ctr, 1);
+        const long long t0 = clock64();
+        while (*static_cast<volatile int*>(ctr) < target) {
+            if (clock64() - t0 > limit) {
+                atomicOr(err, kErrTimeout);
+                ok = false;
+                break;
+            }
+        }
+        __threadfence_block();
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok;
+}
+
+// Re-planning after the lengths changed (lengths_changed), by every warp of the
+// block: the warps meet (bounded), warp 0 rebuilds the prefixes from the lengths
+// now visible, they meet again.  Returns -1 when a meeting gave up (the warps
+// disagreed), else whether some slot overflows (meaningful in warp 0).  The
+// tensor-core kernel calls it out of line, which keeps its streaming loops' code
+// as it was; the CUDA-core kernel measured faster with the same steps inline.
+static __device__ __noinline__ int replan(const DecodeParams& p, int T, int segs, int alpha, int* P, int* VP, int* Ls,
+                                          int* rv) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = static_cast<int>(blockDim.x) / 32;
+    if (!warp_rendezvous(rv, nw, p.wait_cycles, p.err, lane)) return -1;
+    bool ovf = false;
+    if (warp == 0) ovf = build_prefix(p, T, segs, alpha, P, VP, Ls, lane);
+    if (!warp_rendezvous(rv, 2 * nw, p.wait_cycles, p.err, lane)) return -1;
+    return ovf ? 1 : 0;
 }
 
 // Static split of the tile space over W workers, weighted: a segment boundary inside
@@ -361,6 +405,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     int* P = reinterpret_cast<int*>(smem);  // [B + 1] tile prefix over slots
     int* Ls = P + (kMaxBatch + 1);          // [B] cached length, -1 when the slot has no work
     int* VP = TL::HAVE_VP ? Ls + kMaxBatch : P;  // [B + 1] weighted prefix: tiles + ALPHA per segment
+    int* rv = P + (TL::HAVE_VP ? 3 : 2) * kMaxBatch + 2;  // re-planning meeting counter (prefix slack)
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hr = lane >> 4, c = lane & 15;
@@ -374,6 +419,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
 #pragma unroll
         for (int s = 0; s < SPW; ++s) mbar_init(smem_addr(&bars[s]), 1);
     }
+    if (threadIdx.x == 0) *rv = 0;
     // The split depends only on the lengths, so it is computed before waiting on
     // the previous launch: a block that starts while the previous step drains
     // then warms L2 with its first tiles (contiguous caches) instead of idling.
@@ -405,6 +451,24 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     }
     grid_dep_wait();    // inputs, caches and outputs may be in use by the previous launch
     grid_dep_launch();  // the next step may take SMs as this grid's blocks finish
+    if (lengths_changed(p, Ls, lane)) {
+        // (rare) the lengths changed after this block read them: the warps meet, warp 0
+        // rebuilds the split from the lengths now visible, they meet again
+        if (!warp_rendezvous(rv, TL::WARPS, p.wait_cycles, p.err, lane)) return;
+        if (warp == 0) ovf = build_prefix(p, T, segs, TL::ALPHA, P, VP, Ls, lane);
+        if (!warp_rendezvous(rv, 2 * TL::WARPS, p.wait_cycles, p.err, lane)) return;
+        t_begin = split.begin(wid);
+        n_my = split.begin(wid + 1) - t_begin;
+    }
+    if (ovf && warp == 0 && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
+
+    // Slots without work (inactive or overflowing) get a zero output.
+    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
+        if (P[b + 1] == P[b]) {
+            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
+        }
+    }
+    if (n_my <= 0) return;
 
     // ---- bulk copies of one tile (lane 0 only) ----
     // Paged caches: the page of the tile comes from the block table; the entry
@@ -464,58 +528,17 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
         }
     };
 
-    // The first SPW tiles of the plan are issued at once; the lengths are checked
-    // again while they are in flight.  Copy cursor ci, compute cursor cc.
-    Cursor ci{}, cc{};
-    int npre = 0;
-    auto start = [&]() {
-        npre = min(SPW, n_my);
-        if (n_my <= 0) return;
-        ci = locate(t_begin, P, p.B, segs);
-        cc = ci;
-        if (!I8) prefetch_segment(ci);  // the first segment's new K/V rows are needed at its last tile
-        for (int k = 0; k < npre; ++k) {
-            if (lane == 0 && !(stall_me && k == 0)) issue(k, ci);
-            if (k + 1 < n_my) {
-                advance(ci, P, segs);
-                if (!I8 && ci.tile == 0) prefetch_segment(ci);
-            }
-        }
-    };
-    start();
-    if (lengths_changed(p, Ls)) {
-        // (rare) the plan was built from stale lengths: let the copies issued from it
-        // land, reset the barriers, rebuild the plan from the lengths now visible, start again
-        bool failed = false;
-        if (lane == 0)
-            for (int k = 0; k < npre; ++k)
-                if (!(stall_me && k == 0))
-                    failed |= !mbar_wait_bounded(smem_addr(&bars[k]), 0u, p.err, kDrainLimitCycles);
-        if (__syncthreads_or(failed)) return;
-        if (lane == 0) {
-#pragma unroll
-            for (int s = 0; s < SPW; ++s) {
-                mbar_inval(smem_addr(&bars[s]));
-                mbar_init(smem_addr(&bars[s]), 1);
-            }
-        }
-        fence_mbar_init();
-        if (warp == 0) ovf = build_prefix(p, T, segs, TL::ALPHA, P, VP, Ls, lane);
-        __syncthreads();
-        t_begin = split.begin(wid);
-        n_my = split.begin(wid + 1) - t_begin;
-        pages = PageCursor{};
-        start();
-    }
-    if (ovf && warp == 0 && lane == 0 && blockIdx.x == 0) atomicOr(p.err, kErrSeqOverflow);
-
-    // Slots without work (inactive or overflowing) get a zero output.
-    for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-        if (P[b + 1] == P[b]) {
-            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
+    Cursor ci = locate(t_begin, P, p.B, segs);
+    Cursor cc = ci;
+    if (!I8) prefetch_segment(ci);  // the first segment's new K/V rows are needed at its last tile
+    const int npre = min(SPW, n_my);
+    for (int k = 0; k < npre; ++k) {
+        if (lane == 0 && !(stall_me && k == 0)) issue(k, ci);
+        if (k + 1 < n_my) {
+            advance(ci, P, segs);
+            if (!I8 && ci.tile == 0) prefetch_segment(ci);
         }
     }
-    if (n_my <= 0) return;
 
     float qr[G][EPL], o[G][EPL], m[G], l[G];
     int tk[G];  // token of each query row (0 unless several new tokens per step)

@@ -281,6 +281,18 @@ uint64_t ftd_kernel_launches(void);
  */
 ftd_status ftd_debug_stall_next(ftd_ctx* ctx, int calls);
 
+/*
+ * ftd_debug_late_lengths -- test hook for the decode kernels' re-planning path;
+ * the pages have no counterpart.  Launches, on `stream`, one small kernel that
+ * at once allows the next launch on the stream to start (programmatic
+ * dependent launch), waits about delay_us microseconds and then copies n int32
+ * lengths from src to dst (both device pointers).  A decode call issued right
+ * after it on the same stream with seq_lens = dst therefore plans its split
+ * from the old lengths and must notice, after its wait, that they changed.
+ * n is 1 .. 1024 and delay_us 0 .. 1e6; the kernel's wait is bounded by delay_us.
+ */
+ftd_status ftd_debug_late_lengths(const int32_t* src, int32_t* dst, int n, int delay_us, void* stream);
+
 /* Size of the fixed device array that ftd_decode_mha_noalloc uses as scratch. */
 #define FTD_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -75,6 +75,38 @@ def test_lengths_written_right_before_the_step(name):
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
+def test_lengths_written_after_the_step_read_them(name):
+    """The preceding kernel (ftd_debug_late_lengths) lets the step start at once and writes
+    seq_lens only ~50 us later: the step plans from the stale lengths, finds after its wait
+    that they changed, and re-plans.  Result, appended rows and status follow the new lengths."""
+    import torch
+    lens = np.array([1500, 0, 2047, 333, 128, -1], np.int32)
+    w, inp, cc = case(name, lens, seed=53)
+    ref = oracle.load().decode_step(w, inp, nthreads=8)
+    step = make_step(w, force_cuda_core=cc)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        q, kn, vn, bias = (dev(inp[k]) for k in ("q", "k_new", "v_new", "bias"))
+        kc, vc = dev(inp["k_cache"]), dev(inp["v_cache"])
+        sc = dev(inp["scales"]) if inp["scales"] is not None else None
+        stale = dev(np.array([700, -1, 5, 333, 2047, 9], np.int32))  # every slot but one differs
+        new = dev(lens)
+        sl = stale.clone()
+        out = torch.full((w.B, w.Hq, w.D), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        for _ in range(3):
+            sl.copy_(stale)
+            assert ftd.ftd_debug_late_lengths(new.data_ptr(), sl.data_ptr(), w.B, 50, stream.cuda_stream) == 0
+            step(q, kn, vn, sl, out, bias=bias, k_cache=kc, v_cache=vc, scales=sc, stream=stream.cuda_stream)
+    torch.cuda.synchronize()
+    assert step.get_error() == ftd.FTD_OK
+    step.close()
+    assert_close(out.double().cpu().numpy(), ref["out"], i8=w.cache_dtype == "i8", what=name)
+    assert_same_bytes(kc.cpu().numpy().view(ref["k_cache"].dtype), ref["k_cache"], f"{name}: K cache")
+    assert_same_bytes(vc.cpu().numpy().view(ref["v_cache"].dtype), ref["v_cache"], f"{name}: V cache")
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
 def test_timeout_path_reports_and_recovers(name):
     lens = [1800, 40, 1000, 2047]
     w, inp, cc = case(name, lens, seed=52)
