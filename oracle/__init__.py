@@ -70,6 +70,8 @@ class Oracle:
         lib.oracle_quant_i8.argtypes = [P, ctypes.c_int, P, P]
         lib.oracle_attend.restype = None
         lib.oracle_attend.argtypes = [P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_double, P, P]
+        lib.oracle_out_proj.restype = None
+        lib.oracle_out_proj.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
         lib.oracle_decode_step.restype = ctypes.c_int
         lib.oracle_decode_step.argtypes = [ctypes.POINTER(_Cfg), P, P, P, P, P, P, P, P, P,
                                            ctypes.c_int]
@@ -145,6 +147,17 @@ class Oracle:
             lens.ctypes.data, None if sc is None else sc.ctypes.data, out.ctypes.data,
             int(nthreads))
         return dict(out=out, k_cache=kc, v_cache=vc, scales=sc, overflow=bool(ov))
+
+
+    def out_proj(self, x, W):
+        """y [tokens][F] = x . W^T in float64: x is the step's output ([B,Hq,D] or [B,T,Hq,D], as
+        float values), flattened to one row of Hq * D per token; W is [F][Hq * D] (float values)."""
+        W = np.ascontiguousarray(W, np.float64)
+        F, K = W.shape
+        x = np.ascontiguousarray(np.asarray(x, np.float64).reshape(-1, K))
+        y = np.zeros((x.shape[0], F), np.float64)
+        self.lib.oracle_out_proj(x.ctypes.data, W.ctypes.data, x.shape[0], K, F, y.ctypes.data)
+        return y
 
 
 def load(path: Optional[str] = None) -> Oracle:

@@ -136,3 +136,10 @@ def decode_step(w, inp, softmax_scale: float = 0.0, window: int = 0, q_len=None)
     if T == 1:
         out = out[:, 0]
     return dict(out=out, k_cache=kc, v_cache=vc, scales=sc, overflow=overflow)
+
+
+def out_proj(x, W):
+    """The output projection as plain Python loops: y[t][f] = sum_k W[f][k] x[t][k]."""
+    F, K = len(W), len(W[0])
+    rows = [list(map(float, r)) for r in np.asarray(x, np.float64).reshape(-1, K)]
+    return [[math.fsum(float(W[f][k]) * r[k] for k in range(K)) for f in range(F)] for r in rows]

@@ -46,6 +46,11 @@
  *      max(0, L + j + 1 - W)): each draft token sees the cache and the draft
  *      tokens before it, as T single-token steps in a row would.  A slot with
  *      L + T > Lmax is an overflow.
+ *   5. Output projection (lpnh.cn section 2.1: the fused kernels hand their
+ *      result straight to the next projection): oracle_out_proj computes
+ *         y[t][f] = sum_k W[f][k] * x[t][k],
+ *      for the step's output x flattened to one row of Hq * D values per token
+ *      and a weight W laid out as a linear layer's [F][Hq * D], in float64.
  *
  * Plain loops, no blocking, no fusion: a reader can check each line against
  * the formulas above.
@@ -275,4 +280,14 @@ int oracle_decode_step(const oracle_cfg* c, const void* q, const void* k_new, co
     }
     (void)nthreads;
     return overflow;
+}
+
+/* Step 5: y [n_tok][F] = x [n_tok][K] times the transpose of W [F][K], in float64. */
+void oracle_out_proj(const double* x, const double* W, int n_tok, int K, int F, double* y) {
+    for (int t = 0; t < n_tok; ++t)
+        for (int f = 0; f < F; ++f) {
+            double s = 0.0;
+            for (int k = 0; k < K; ++k) s += W[(size_t)f * K + k] * x[(size_t)t * K + k];
+            y[(size_t)t * F + f] = s;
+        }
 }

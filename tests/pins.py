@@ -15,7 +15,9 @@ The facts used:
   * softmax weights summing to one; the large-score limit;
   * GQA: kv head h // group, and equality with MHA on repeated K/V;
   * a pure-Python brute force (``oracle/brute.py``) on tiny decode steps;
-  * a step of T new tokens equals T single-token steps in a row.
+  * a step of T new tokens equals T single-token steps in a row;
+  * the output projection: the brute force on a non-square weight, a weight
+    whose rows are unit vectors (y picks entries of x), linearity in x.
 """
 from __future__ import annotations
 
@@ -309,6 +311,33 @@ def pin_multi_token(o):
             assert np.array_equal(one["out"][b, j], v[kvh]), "window 1 -> the token's own V"
 
 
+def pin_out_proj(o):
+    """The output projection y = x . W^T: equal to the pure-Python loops on a non-square W with
+    distinct entries (a transposed or shifted index fails); W with unit-vector rows picks the
+    entries of x; a zero W row gives zero; linear in x."""
+    rng = np.random.default_rng(31)
+    for n_tok, K, F in ((1, 5, 3), (3, 8, 11), (4, 16, 6)):
+        x = rng.standard_normal((n_tok, K))
+        W = rng.standard_normal((F, K))
+        y = o.out_proj(x, W)
+        assert y.shape == (n_tok, F)
+        assert np.max(np.abs(y - np.array(brute.out_proj(x, W)))) <= 1e-12, (n_tok, K, F)
+        x2 = rng.standard_normal((n_tok, K))
+        assert np.max(np.abs(o.out_proj(x + 2.0 * x2, W) - (y + 2.0 * o.out_proj(x2, W)))) <= 1e-12
+    # unit-vector rows: feature f reads element sel[f] of each token's row
+    K, F = 12, 7
+    sel = np.array([11, 0, 5, 5, 3, 10, 1])
+    W = np.zeros((F, K))
+    W[np.arange(F), sel] = 1.0
+    W[2] = 0.0  # and a zero row
+    x = rng.standard_normal((2, 3, 4))  # [B][Hq][D] flattened to K = 12 per token
+    y = o.out_proj(x, W)
+    flat = x.reshape(2, K)
+    want = flat[:, sel].copy()
+    want[:, 2] = 0.0
+    assert np.array_equal(y, want), "unit-vector rows select entries of the flattened output"
+
+
 ALL_PINS = [pin_bf16_rounding, pin_f16_rounding, pin_quant_i8, pin_attend_closed_forms,
             pin_attend_invariants, pin_brute_force, pin_append_semantics, pin_gqa_mapping,
-            pin_golden, pin_workload_tiny, pin_sliding_window, pin_multi_token]
+            pin_golden, pin_workload_tiny, pin_sliding_window, pin_multi_token, pin_out_proj]

@@ -55,6 +55,12 @@ MUTANTS = {
                                   "return (double)((const int8_t*)cache)[i];")],
     "i8_v_scale_from_k_plane": [("oracle_quant_i8(vf, D, code, &scales[plane + si]);",
                                  "oracle_quant_i8(vf, D, code, &scales[si]);")],
+    "proj_weight_transposed": [("s += W[(size_t)f * K + k] * x[(size_t)t * K + k];",
+                                "s += W[(size_t)k * F + f] * x[(size_t)t * K + k];")],
+    "proj_reversed_k_of_x": [("s += W[(size_t)f * K + k] * x[(size_t)t * K + k];",
+                              "s += W[(size_t)f * K + k] * x[(size_t)t * K + (K - 1 - k)];")],
+    "proj_drops_last_k": [("for (int k = 0; k < K; ++k) s += W", "for (int k = 0; k < K - 1; ++k) s += W")],
+    "proj_output_transposed": [("y[(size_t)t * F + f] = s;", "y[(size_t)f * n_tok + t] = s;")],
 }
 
 
