@@ -53,7 +53,8 @@ KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
 OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("13b", dict(page_size=256)),
                 ("70b", dict(out_dtype="bf16")), ("70b", dict(window=1024)), ("70b", dict(page_size=256)),
                 ("int8", dict(page_size=256)), ("7b", dict(q_len=4)), ("7b", dict(q_len=8)),
-                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)), ("mqa", {}), ("70b_i8", {})]
+                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)), ("mqa", {}), ("70b_i8", {}),
+                ("7b", dict(proj_dim=4096)), ("13b", dict(proj_dim=5120)), ("70b", dict(proj_dim=8192))]
 
 
 def kernel_name(w, q_len=1) -> str:
@@ -65,10 +66,11 @@ def kernel_name(w, q_len=1) -> str:
 
 
 # ---------------------------------------------------------------- workload
-def step_bytes(w, lens, window=0, out_dtype="f32", q_len=1) -> dict:
+def step_bytes(w, lens, window=0, out_dtype="f32", q_len=1, proj_dim=0) -> dict:
     """Algorithmic bytes of one step: each visible cached K/V row once per kv head
     (with a window, only rows some new token still sees), plus the q_len appended
-    rows per slot."""
+    rows per slot; with an output projection, also its weight W_o [proj_dim][Hq D]
+    read once, the hi / lo operand planes written and read, and y written."""
     lens = np.asarray(lens, np.int64)
     T = max(1, int(q_len))
     act = (lens >= 0) & (lens + T <= w.Lmax)
@@ -84,7 +86,12 @@ def step_bytes(w, lens, window=0, out_dtype="f32", q_len=1) -> dict:
     scale_rw = 8 * w.Hkv * ctx if w.cache_dtype == "i8" else 0
     small = ((w.B * w.Hq * w.D + 2 * w.B * w.Hkv * w.D) * qeb * T + 4 * w.B
              + EB[out_dtype] * w.B * T * w.Hq * w.D)
-    return dict(kv=kv_read + kv_write + scale_rw, total=kv_read + kv_write + scale_rw + small, ctx=ctx)
+    proj = 0
+    if proj_dim:
+        K, tok = w.Hq * w.D, w.B * T
+        proj = proj_dim * K * qeb + 2 * 2 * tok * K * qeb + tok * proj_dim * EB[out_dtype]
+    return dict(kv=kv_read + kv_write + scale_rw, total=kv_read + kv_write + scale_rw + small + proj, ctx=ctx,
+                proj=proj)
 
 
 def kernel_hash() -> str:
@@ -153,7 +160,7 @@ def make_pools(w, npools, seed, device, page_size=0):
     return pools
 
 
-def make_step_inputs(w, lens, seed, device, out_dtype="f32", q_len=1):
+def make_step_inputs(w, lens, seed, device, out_dtype="f32", q_len=1, proj_dim=0):
     import torch
     g = torch.Generator(device=device)
     g.manual_seed(seed + 1000)
@@ -168,7 +175,12 @@ def make_step_inputs(w, lens, seed, device, out_dtype="f32", q_len=1):
     sl = torch.from_numpy(np.asarray(lens, np.int32)).to(device)
     odt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[out_dtype]
     out = torch.empty((w.B,) + tok + (w.Hq, w.D), dtype=odt, device=device)
-    return dict(q=q, k_new=kn, v_new=vn, bias=bias, seq_lens=sl, out=out)
+    d = dict(q=q, k_new=kn, v_new=vn, bias=bias, seq_lens=sl, out=out)
+    if proj_dim:  # W_o ~ N(0, 1/K) in the qkv dtype, y in the out dtype
+        K = w.Hq * w.D
+        d["w_o"] = (torch.randn((proj_dim, K), device=device, generator=g) / K ** 0.5).to(dt)
+        d["y"] = torch.empty((w.B,) + tok + (proj_dim,), dtype=odt, device=device)
+    return d
 
 
 def n_pools_for(w, kv_bytes):
@@ -195,6 +207,9 @@ def decode_call(step, pools, inp, stream):
                 stream.cuda_stream)
         if inp.get("block_table") is not None:
             ftd.check(ftd.ftd_decode_mha_paged(step.ctx, *common, inp["block_table"].data_ptr(), *tail))
+        elif inp.get("w_o") is not None:
+            ftd.check(ftd.ftd_decode_mha_proj(step.ctx, *common, *tail[:3], inp["w_o"].data_ptr(),
+                                              inp["y"].data_ptr(), tail[3]))
         else:
             ftd.check(ftd.ftd_decode_mha(step.ctx, *common, *tail))
     return one
@@ -499,7 +514,7 @@ def reference_arm(args):
 
 
 def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", window=0, page_size=0, q_len=1,
-                   flush=None, isolated=0):
+                   flush=None, isolated=0, proj_dim=0):
     """Time one workload; the options select a half-precision output, a sliding
     window, a paged cache (one shuffled block table shared by the rotated pools)
     or several new tokens per slot (the cached lengths drop by q_len - 1 so the
@@ -509,16 +524,16 @@ def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", w
     import decode_step_masked_gb300 as ftd
     w = WORKLOADS[name]
     lens = gen_seq_lens(w) - (q_len - 1)
-    by = step_bytes(w, lens, window, out_dtype, q_len)
+    by = step_bytes(w, lens, window, out_dtype, q_len, proj_dim)
     # rotation is sized on the bytes a step reads (the visible rows), so each pool leaves L2 between reads
     pools = make_pools(w, n_pools_for(w, by["kv"]), seed, device, page_size)
-    inp = make_step_inputs(w, lens, seed, device, out_dtype, q_len)
+    inp = make_step_inputs(w, lens, seed, device, out_dtype, q_len, proj_dim)
     num_pages = 0
     if page_size:
         table, num_pages = page_table(w, page_size, seed)
         inp["block_table"] = torch.from_numpy(table).to(device)
     step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, out_dtype=out_dtype,
-                          window=window, page_size=page_size, num_pages=num_pages, q_len=q_len)
+                          window=window, page_size=page_size, num_pages=num_pages, q_len=q_len, proj_dim=proj_dim)
     r = run_timed(step, w, pools, inp, steps, warmup, stream)
     if isolated and flush is not None:
         r["isolated_us"] = run_isolated(step, pools, inp, isolated, stream, flush)
@@ -561,9 +576,11 @@ def main():
     ap.add_argument("--ncu-batch", type=int, default=0,
                     help="profiling mode: only the first B slots of the workload (a smaller capture)")
     ap.add_argument("--ncu-window", type=int, default=0, help="profiling mode: sliding window W")
+    ap.add_argument("--ncu-proj", type=int, default=0,
+                    help="profiling mode: the step with an output projection to this many features")
     args = ap.parse_args()
     if args.ncu_launches:
-        return profile_launches(args.config, args.ncu_launches, args.ncu_batch, args.ncu_window)
+        return profile_launches(args.config, args.ncu_launches, args.ncu_batch, args.ncu_window, args.ncu_proj)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
@@ -641,6 +658,13 @@ def main():
             key = name + (":" + ",".join(f"{k}={v}" for k, v in kw.items()) if kw else "")
             opts[key] = dict(us=us2, gbs=by2["kv"] / us2 / 1e3, frac=by2["kv"] / us2 / 1e3 / peaks["hbm_gbs"],
                              kv_mb=by2["kv"] / 1e6, kernel=kernel_name(w2, kw.get("q_len", 1)))
+            if kw.get("proj_dim"):
+                # decode step + projection; the projection's share against the plain step's time
+                extra = us2 - per_cfg[name]["us"]
+                opts[key].update(kernel=kernel_name(w2) + " + out_proj_kernel", total_mb=by2["total"] / 1e6,
+                                 gbs=by2["total"] / us2 / 1e3, frac=by2["total"] / us2 / 1e3 / peaks["hbm_gbs"],
+                                 proj_mb=by2["proj"] / 1e6, proj_extra_us=extra,
+                                 proj_gbs=by2["proj"] / extra / 1e3 if extra > 0 else None)
             del pools2
             torch.cuda.empty_cache()
         line["options"] = opts
@@ -665,9 +689,10 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-def profile_launches(name, n, batch=0, window=0):
+def profile_launches(name, n, batch=0, window=0, proj_dim=0):
     """N plain launches of one workload on one cache pool (for ncu captures of a single launch);
-    batch > 0 keeps only the workload's first slots (their seeded lengths), for a smaller capture."""
+    batch > 0 keeps only the workload's first slots (their seeded lengths), for a smaller capture;
+    proj_dim > 0 adds the output projection (ftd_decode_mha_proj: two kernels per step)."""
     import torch
     import decode_step_masked_gb300 as ftd
     w = WORKLOADS[name]
@@ -678,11 +703,16 @@ def profile_launches(name, n, batch=0, window=0):
     device = torch.device("cuda", 0)
     ftd.build_library()
     kc, vc, sc = make_pools(w, 1, 5, device)[0]
-    inp = make_step_inputs(w, lens, 5, device)
-    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, window=window)
+    inp = make_step_inputs(w, lens, 5, device, proj_dim=proj_dim)
+    step = ftd.DecodeStep(w.B, w.Hq, w.Hkv, w.D, w.Lmax, w.qkv_dtype, w.cache_dtype, window=window,
+                          proj_dim=proj_dim)
     for _ in range(n):
-        step(inp["q"], inp["k_new"], inp["v_new"], inp["seq_lens"], inp["out"], bias=inp["bias"], k_cache=kc,
-             v_cache=vc, scales=sc)
+        if proj_dim:
+            step.proj(inp["q"], inp["k_new"], inp["v_new"], inp["seq_lens"], inp["out"], inp["w_o"], inp["y"],
+                      bias=inp["bias"], k_cache=kc, v_cache=vc, scales=sc)
+        else:
+            step(inp["q"], inp["k_new"], inp["v_new"], inp["seq_lens"], inp["out"], bias=inp["bias"], k_cache=kc,
+                 v_cache=vc, scales=sc)
     torch.cuda.synchronize()
     ftd.check(step.get_error())
     step.close()

@@ -34,7 +34,7 @@ DTYPES = {"f32": FTD_F32, "f16": FTD_F16, "bf16": FTD_BF16, "i8": FTD_I8}
 EXPORTS = ("ftd_init", "ftd_cache_ptrs", "ftd_decode_mha", "ftd_decode_mha_current", "ftd_decode_mha_paged",
            "ftd_decode_mha_host", "ftd_get_error", "ftd_destroy", "ftd_status_str", "ftd_last_error",
            "ftd_kernel_launches", "ftd_decode_mha_noalloc", "ftd_debug_stall_next",
-           "ftd_debug_late_lengths")
+           "ftd_debug_late_lengths", "ftd_decode_mha_proj")
 
 
 class FtdConfig(ctypes.Structure):
@@ -43,7 +43,7 @@ class FtdConfig(ctypes.Structure):
                 ("cache_dtype", ctypes.c_int), ("softmax_scale", ctypes.c_float),
                 ("out_dtype", ctypes.c_int), ("window", ctypes.c_int), ("page_size", ctypes.c_int),
                 ("num_pages", ctypes.c_int), ("q_len", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("wait_limit_us", ctypes.c_int)]
+                ("proj_dim", ctypes.c_int), ("wait_limit_us", ctypes.c_int)]
 
 
 class FtdError(RuntimeError):
@@ -80,6 +80,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ftd_decode_mha_current.restype = I
     lib.ftd_decode_mha_paged.argtypes = [P] * 12
     lib.ftd_decode_mha_paged.restype = I
+    lib.ftd_decode_mha_proj.argtypes = [P] * 13
+    lib.ftd_decode_mha_proj.restype = I
     lib.ftd_get_error.argtypes = [P]
     lib.ftd_get_error.restype = I
     lib.ftd_destroy.argtypes = [P]
@@ -150,6 +152,12 @@ def ftd_decode_mha_paged(ctx, q, k_new, v_new, qkv_bias, k_pages, v_pages, block
                                                       block_table, seq_lens, scales, out, stream))
 
 
+def ftd_decode_mha_proj(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out, w_o, y,
+                        stream) -> int:
+    return load_library().ftd_decode_mha_proj(*_ptrs(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens,
+                                                     scales, out, w_o, y, stream))
+
+
 def ftd_decode_mha_host(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, seq_lens, scales, out,
                         stream) -> int:
     return load_library().ftd_decode_mha_host(*_ptrs(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache,
@@ -197,11 +205,12 @@ class DecodeStep:
 
     def __init__(self, max_batch, n_q_heads, n_kv_heads, head_dim, max_len, qkv_dtype="bf16",
                  cache_dtype="bf16", softmax_scale=0.0, stream: Optional[int] = None, out_dtype="f32",
-                 window=0, page_size=0, num_pages=0, q_len=1, kernel=FTD_KERNEL_AUTO, wait_limit_us=0):
+                 window=0, page_size=0, num_pages=0, q_len=1, kernel=FTD_KERNEL_AUTO, wait_limit_us=0, proj_dim=0):
         import torch
         self.cfg = FtdConfig(max_batch, n_q_heads, n_kv_heads, head_dim, max_len, DTYPES[qkv_dtype],
                              DTYPES[cache_dtype], float(softmax_scale), DTYPES[out_dtype], int(window),
-                             int(page_size), int(num_pages), int(q_len), int(kernel), int(wait_limit_us))
+                             int(page_size), int(num_pages), int(q_len), int(kernel), int(proj_dim),
+                             int(wait_limit_us))
         s = torch.cuda.current_stream().cuda_stream if stream is None else stream
         st, ctx = ftd_init(self.cfg, s)
         check(st)
@@ -220,6 +229,14 @@ class DecodeStep:
             raise ValueError("a paged context takes paged(..., block_table, ...)")
         check(ftd_decode_mha(self.ctx, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(bias), _ptr(k_cache),
                              _ptr(v_cache), _ptr(seq_lens), _ptr(scales), _ptr(out), s))
+
+    def proj(self, q, k_new, v_new, seq_lens, out, w_o, y, bias=None, k_cache=None, v_cache=None, scales=None,
+             stream: Optional[int] = None):
+        """The step followed by the output projection y = out . w_o^T (a context with proj_dim)."""
+        import torch
+        s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+        check(ftd_decode_mha_proj(self.ctx, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(bias), _ptr(k_cache),
+                                  _ptr(v_cache), _ptr(seq_lens), _ptr(scales), _ptr(out), _ptr(w_o), _ptr(y), s))
 
     def paged(self, q, k_new, v_new, block_table, seq_lens, out, bias=None, k_pages=None, v_pages=None,
               scales=None, stream: Optional[int] = None):

@@ -22,6 +22,7 @@
 #include "ftd_decode_splitk.cuh"
 #include "ftd_decode_gqa_tc.cuh"
 #include "ftd_internal.cuh"
+#include "ftd_out_proj.cuh"
 
 namespace {
 
@@ -101,6 +102,26 @@ bool encode_cache_map(CUtensorMap* map, void* base, ftd_dtype dt, size_t rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D view [rows][cols] of a half-precision matrix (cols contiguous), read in boxes of
+// 64 columns x box_rows rows with the 128-byte swizzle, rows past the end read as zero:
+// the output projection's weight W [F][K] and its activation planes [tokens][K].
+bool encode_rows_map(CUtensorMap* map, const void* base, bool bf16, size_t rows, size_t cols, int box_rows) {
+    EncodeTiledFn fn = encode_tiled();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+              const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The projection's workspace is one partial slot of ntb x 128 floats per tile and per
+// CTA; configurations that would need more than this are refused.
+constexpr size_t kMaxProjWorkspace = static_cast<size_t>(256) << 20;
+
 }  // namespace
 
 namespace ftd {
@@ -140,7 +161,8 @@ __attribute__((visibility("hidden"))) bool encode_tc_cache_map(CUtensorMap* map,
 // the message goes to msg.
 __attribute__((visibility("hidden"))) ftd_status plan_config(const ftd_config& c, Plan* pl, char* msg, size_t n) {
     auto bad = [&](ftd_status st, const char* fmt, auto... a) {
-        snprintf(msg, n, fmt, a...);
+        if constexpr (sizeof...(a) == 0) snprintf(msg, n, "%s", fmt);
+        else snprintf(msg, n, fmt, a...);
         return st;
     };
     if (c.max_batch < 1 || c.max_batch > kMaxBatch)
@@ -172,6 +194,10 @@ __attribute__((visibility("hidden"))) ftd_status plan_config(const ftd_config& c
     if (c.kernel != FTD_KERNEL_AUTO && c.kernel != FTD_KERNEL_CUDA_CORE)
         return bad(FTD_ERR_INVALID_ARG, "kernel %d (FTD_KERNEL_AUTO or FTD_KERNEL_CUDA_CORE)", c.kernel);
     if (c.wait_limit_us < 0) return bad(FTD_ERR_INVALID_ARG, "wait_limit_us %d must be >= 0", c.wait_limit_us);
+    if (c.proj_dim < 0 || c.proj_dim % 128 != 0 || c.proj_dim > 65536)
+        return bad(FTD_ERR_INVALID_ARG, "proj_dim %d must be 0 or a positive multiple of 128 up to 65536", c.proj_dim);
+    if (c.proj_dim > 0 && c.qkv_dtype != FTD_F16 && c.qkv_dtype != FTD_BF16)
+        return bad(FTD_ERR_UNSUPPORTED, "the output projection needs an F16 or BF16 qkv_dtype (its weight's type)");
 
     const int g = c.n_q_heads / c.n_kv_heads;
     const int nq = c.q_len > 1 ? c.q_len : 1;
@@ -203,6 +229,20 @@ __attribute__((visibility("hidden"))) ftd_status plan_config(const ftd_config& c
     pl->ki = ki;
     pl->tcc = tcc;
     pl->rows = rows;
+    pl->tokens = c.max_batch * nq;
+    pl->ntb = pl->nblk = pl->mtiles = pl->kch = 0;
+    if (c.proj_dim > 0) {
+        if (!encode_tiled()) return bad(FTD_ERR_UNSUPPORTED, "the output projection needs the tensor-map driver entry point");
+        const int t16 = (pl->tokens + 15) / 16 * 16;
+        pl->ntb = t16 < op::kMaxNtb ? t16 : op::kMaxNtb;
+        pl->nblk = (pl->tokens + pl->ntb - 1) / pl->ntb;
+        pl->mtiles = c.proj_dim / op::MT;
+        pl->kch = c.n_q_heads * c.head_dim / op::KCH;
+        const size_t ws = (static_cast<size_t>(pl->nblk) * pl->mtiles + 1024) * pl->ntb * op::MT * sizeof(float);
+        if (ws > kMaxProjWorkspace)
+            return bad(FTD_ERR_UNSUPPORTED, "output projection of %d tokens x %d features needs %zu MB of workspace",
+                       pl->tokens, c.proj_dim, ws >> 20);
+    }
     return FTD_OK;
 }
 
@@ -297,6 +337,19 @@ struct ftd_ctx {
     cudaStream_t last_stream = nullptr;
     long long wait_cycles = 0;  // limit of the kernels' pipeline waits
     int stall_calls = 0;        // ftd_debug_stall_next: calls left that withhold a copy
+    // output projection (proj_dim > 0)
+    ftd::Plan plan{};
+    const void* proj_fn = nullptr;
+    int proj_smem = 0;
+    void* proj_hi = nullptr;    // activation planes [tokens][Hq * D], qkv dtype
+    void* proj_lo = nullptr;
+    float* proj_ws = nullptr;
+    uint32_t* proj_counters = nullptr;
+    size_t n_proj_counters = 0;
+    CUtensorMap tmph;
+    CUtensorMap tmpl;
+    CUtensorMap tmw;
+    const void* tm_w_base = nullptr;
 };
 
 extern "C" {
@@ -395,8 +448,14 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     };
     const size_t o_k = carve(cache_bytes), o_v = carve(cache_bytes), o_s = carve(scale_bytes);
     const size_t o_cnt = carve(n_seg * sizeof(uint32_t)), o_err = carve(sizeof(uint32_t));
+    const bool proj = c.proj_dim > 0;
+    const size_t n_pcnt = proj ? static_cast<size_t>(plan.nblk) * plan.mtiles : 0;
+    const size_t o_pcnt = carve(n_pcnt * sizeof(uint32_t));
     const size_t zero_end = off;  // caches, scales, counters and the error word start at zero
     const size_t o_ws = carve(ws_bytes);
+    const size_t plane_bytes = proj ? static_cast<size_t>(plan.tokens) * Hq * D * 2 : 0;
+    const size_t o_ph = carve(plane_bytes), o_pl = carve(plane_bytes);
+    const size_t o_pws = carve(proj ? (n_pcnt + static_cast<size_t>(grid)) * plan.ntb * ftd::op::MT * sizeof(float) : 0);
     const size_t o_q = carve(ctx->q_bytes), o_kn = carve(ctx->kv_new_bytes), o_vn = carve(ctx->kv_new_bytes);
     const size_t o_b = carve(ctx->bias_bytes), o_l = carve(B * sizeof(int32_t)), o_o = carve(ctx->out_bytes);
     ctx->pool_bytes = off;
@@ -421,6 +480,27 @@ ftd_status ftd_init(const ftd_config* cfg, void* stream, ftd_ctx** out) {
     ctx->st_lens = reinterpret_cast<int32_t*>(base + o_l);
     ctx->st_out = base + o_o;
     ctx->last_stream = static_cast<cudaStream_t>(stream);
+    ctx->plan = plan;
+    if (proj) {
+        ctx->proj_hi = base + o_ph;
+        ctx->proj_lo = base + o_pl;
+        ctx->proj_ws = reinterpret_cast<float*>(base + o_pws);
+        ctx->proj_counters = reinterpret_cast<uint32_t*>(base + o_pcnt);
+        ctx->n_proj_counters = n_pcnt;
+        ctx->proj_fn = ftd::select_proj(c.qkv_dtype == FTD_BF16).fn;
+        ctx->proj_smem = ftd::op::smem_bytes(plan.ntb);
+        const bool bf = c.qkv_dtype == FTD_BF16;
+        // the limit for the largest token block, so contexts of every size can launch the kernel
+        e = cudaFuncSetAttribute(ctx->proj_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ftd::op::kStageBudget + 2048);
+        if (e != cudaSuccess || !encode_rows_map(&ctx->tmph, ctx->proj_hi, bf, plan.tokens, Hq * D, plan.ntb) ||
+            !encode_rows_map(&ctx->tmpl, ctx->proj_lo, bf, plan.tokens, Hq * D, plan.ntb)) {
+            cudaFree(ctx->pool);
+            delete ctx;
+            return e != cudaSuccess ? cuda_fail(e, "cudaFuncSetAttribute (projection kernel)")
+                                    : fail(FTD_ERR_CUDA, "cuTensorMapEncodeTiled failed for the projection planes");
+        }
+    }
 
     e = cudaMemsetAsync(ctx->pool, 0, zero_end, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) {
@@ -465,7 +545,8 @@ static cudaError_t launch_overlapped(const void* fn, int grid, int threads, int 
 
 static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                                 const void* bias, void* k_cache, void* v_cache, const int32_t* block_table,
-                                const int32_t* seq_lens, float* scales, void* out, cudaStream_t stream) {
+                                const int32_t* seq_lens, float* scales, void* out, cudaStream_t stream,
+                                bool proj = false) {
     if (!k_cache) k_cache = ctx->k_cache;
     if (!v_cache) v_cache = ctx->v_cache;
     const bool i8 = ctx->cfg.cache_dtype == FTD_I8;
@@ -510,6 +591,9 @@ static ftd_status launch_decode(ftd_ctx* ctx, const void* q, const void* k_new, 
     while (ctx->paged && (1 << p.page_shift) < c.page_size) ++p.page_shift;
     p.num_pages = c.num_pages;
     p.wait_cycles = ctx->wait_cycles;
+    p.proj_hi = proj ? ctx->proj_hi : nullptr;
+    p.proj_lo = proj ? ctx->proj_lo : nullptr;
+    p.proj_dt = c.qkv_dtype == FTD_BF16 ? ftd::kBF16 : ftd::kF16;
     p.stall = 0;
     if (ctx->stall_calls > 0) {
         p.stall = 1;
@@ -570,6 +654,46 @@ ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, 
     if (!ctx->paged) return fail(FTD_ERR_INVALID_ARG, "the context is not paged (page_size 0)");
     return launch_decode(ctx, q, k_new, v_new, qkv_bias, k_pages, v_pages, block_table, seq_lens, scales, out,
                          static_cast<cudaStream_t>(stream));
+}
+
+ftd_status ftd_decode_mha_proj(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                               const void* qkv_bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
+                               float* scales, void* out, const void* w_o, void* y, void* stream) {
+    g_last_error.clear();
+    if (!ctx) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_proj: ctx is NULL");
+    if (ctx->cfg.proj_dim <= 0) return fail(FTD_ERR_INVALID_ARG, "the context has no output projection (proj_dim 0)");
+    if (ctx->paged) return fail(FTD_ERR_INVALID_ARG, "ftd_decode_mha_proj serves contiguous caches only");
+    if (!w_o || !y || !aligned16(w_o) || !aligned16(y))
+        return fail(FTD_ERR_INVALID_ARG, "w_o and y must be non-NULL and 16-byte aligned");
+    const ftd_config& c = ctx->cfg;
+    const ftd::Plan& pl = ctx->plan;
+    if (ctx->tm_w_base != w_o) {
+        if (!encode_rows_map(&ctx->tmw, w_o, c.qkv_dtype == FTD_BF16, static_cast<size_t>(c.proj_dim),
+                             static_cast<size_t>(c.n_q_heads) * c.head_dim, ftd::op::MT))
+            return fail(FTD_ERR_CUDA, "cuTensorMapEncodeTiled failed for w_o");
+        ctx->tm_w_base = w_o;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const ftd_status st = launch_decode(ctx, q, k_new, v_new, qkv_bias, k_cache, v_cache, nullptr, seq_lens, scales,
+                                        out, s, true);
+    if (st != FTD_OK) return st;
+    ftd::ProjParams pp{};
+    pp.y = y;
+    pp.ws = ctx->proj_ws;
+    pp.counters = ctx->proj_counters;
+    pp.err = ctx->err;
+    pp.tokens = pl.tokens;
+    pp.ntb = pl.ntb;
+    pp.nblk = pl.nblk;
+    pp.mtiles = pl.mtiles;
+    pp.kch = pl.kch;
+    pp.out_dtype = static_cast<int>(c.out_dtype);
+    pp.wait_cycles = ctx->wait_cycles;
+    void* args[] = {&ctx->tmw, &ctx->tmph, &ctx->tmpl, &pp};
+    const cudaError_t e = launch_overlapped(ctx->proj_fn, ctx->grid, ftd::op::kThreads, ctx->proj_smem, args, s);
+    if (e != cudaSuccess) return cuda_fail(e, "projection kernel launch");
+    g_launches.fetch_add(1);
+    return FTD_OK;
 }
 
 // Device address of host pointer p when the GPU can address it (pinned and mapped), else null.
@@ -659,6 +783,8 @@ ftd_status ftd_get_error(ftd_ctx* ctx) {
     if (h & ftd::kErrTimeout) {
         // an abandoned launch may have left segment counters part-way; restart them
         e = cudaMemset(ctx->counters, 0, ctx->n_counters * sizeof(uint32_t));
+        if (e == cudaSuccess && ctx->n_proj_counters)
+            e = cudaMemset(ctx->proj_counters, 0, ctx->n_proj_counters * sizeof(uint32_t));
         if (e != cudaSuccess) return cuda_fail(e, "clearing the split-K counters");
         return fail(FTD_ERR_DEVICE_TIMEOUT, "a decode kernel gave up waiting for a copy");
     }

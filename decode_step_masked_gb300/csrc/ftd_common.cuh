@@ -62,6 +62,12 @@ struct DecodeParams {
     int pages_per_seq, page_shift, num_pages;  // page_size = 1 << page_shift
     long long wait_cycles;  // limit of a pipeline wait (kWaitLimitCycles unless the context sets one)
     int stall;              // test hook: block 0 never issues its first tile copy (see ftd_debug_stall_next)
+    // Output projection (ftd_decode_mha_proj): the final stores also write each output
+    // value, as out holds it, split into a high and a low part of the projection's
+    // operand type (proj_dt, kF16 or kBF16), into two planes laid out like out.
+    void* proj_hi;          // nullptr: no projection
+    void* proj_lo;
+    int proj_dt;
 };
 
 // First visible position of a slot with L cached tokens (the window start).
@@ -139,11 +145,65 @@ __device__ __forceinline__ void st_out4(void* out, size_t i, float a, float b, f
     }
 }
 
+// The value out holds after storing v in out_dtype.
+__device__ __forceinline__ float as_stored(float v, int dt) {
+    if (dt == kF16) return __half2float(__float2half_rn(v));
+    if (dt == kBF16) return __bfloat162float(__float2bfloat16_rn(v));
+    return v;
+}
+
+// x as a high and a low part of type kF16 / kBF16 (x ~ hi + lo, about 16 mantissa bits), as bit patterns.
+__device__ __forceinline__ void split_hilo(float x, int dt, uint16_t& hi, uint16_t& lo) {
+    if (dt == kF16) {
+        const __half h = __float2half_rn(x);
+        hi = __half_as_ushort(h);
+        lo = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+    } else {
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        hi = __bfloat16_as_ushort(h);
+        lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+    }
+}
+
+// Final stores of the step: out, and the projection planes when there is a projection.
+__device__ __forceinline__ void store_out1(const DecodeParams& p, size_t i, float v) {
+    st_out1(p.out, i, v, p.out_dtype);
+    if (p.proj_hi) {
+        uint16_t hi, lo;
+        split_hilo(as_stored(v, p.out_dtype), p.proj_dt, hi, lo);
+        static_cast<uint16_t*>(p.proj_hi)[i] = hi;
+        static_cast<uint16_t*>(p.proj_lo)[i] = lo;
+    }
+}
+
+__device__ __forceinline__ void store_out4(const DecodeParams& p, size_t i, float a, float b, float c, float d) {
+    st_out4(p.out, i, a, b, c, d, p.out_dtype);
+    if (p.proj_hi) {
+        const float v[4] = {a, b, c, d};
+        uint16_t hi[4], lo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) split_hilo(as_stored(v[k], p.out_dtype), p.proj_dt, hi[k], lo[k]);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.proj_hi) + i) =
+            make_uint2(hi[0] | (static_cast<uint32_t>(hi[1]) << 16), hi[2] | (static_cast<uint32_t>(hi[3]) << 16));
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.proj_lo) + i) =
+            make_uint2(lo[0] | (static_cast<uint32_t>(lo[1]) << 16), lo[2] | (static_cast<uint32_t>(lo[3]) << 16));
+    }
+}
+
 // Zero n outputs starting at element i (i and n multiples of 8), by all threads of a block.
 __device__ __forceinline__ void zero_out(void* out, size_t i, int n, int dt) {
     const int eb = dt == kF32 ? 4 : 2;
     uint4* dst = reinterpret_cast<uint4*>(static_cast<unsigned char*>(out) + i * eb);
     for (int k = threadIdx.x; k < n * eb / 16; k += blockDim.x) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// zero_out of the step's outputs: out, and the projection planes when there is a projection.
+__device__ __forceinline__ void zero_outputs(const DecodeParams& p, size_t i, int n) {
+    zero_out(p.out, i, n, p.out_dtype);
+    if (p.proj_hi) {
+        zero_out(p.proj_hi, i, n, kF16);
+        zero_out(p.proj_lo, i, n, kF16);
+    }
 }
 
 // ---------------------------------------------------------------- PTX
@@ -207,6 +267,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 __device__ __forceinline__ uint64_t l2_stream_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// L2 policy for small operands many blocks read (the output projection's
+// activation planes): their lines stay in L2 ahead of streamed data.
+__device__ __forceinline__ uint64_t l2_keep_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 

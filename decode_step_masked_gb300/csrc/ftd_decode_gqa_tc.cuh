@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
 
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (P[b + 1] == P[b]) {
-            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
+            zero_outputs(p, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D);
         }
     }
 
@@ -1056,8 +1056,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
 #pragma unroll
                         for (int jj = 0; jj < GH; ++jj)
                             if (c0 + jj < QB)
-                                st_out1(p.out, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r, o[jj] / lt[jj],
-                                        p.out_dtype);
+                                store_out1(p, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r, o[jj] / lt[jj]);
                     } else {
                         float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
                         if (r == 0) {
@@ -1113,8 +1112,8 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
 #pragma unroll
                             for (int jj = 0; jj < GH; ++jj)
                                 if (c0 + jj < QB)
-                                    st_out1(p.out, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r, Ac[jj] / Ls_[jj],
-                                            p.out_dtype);
+                                    store_out1(p, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r,
+                                               Ac[jj] / Ls_[jj]);
                             if (leader) p.counters[segg] = 0u;
                         }
                         tc::named_bar_sync(1, SMX);

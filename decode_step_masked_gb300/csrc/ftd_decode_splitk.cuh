@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     // Slots without work (inactive or overflowing) get a zero output.
     for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
         if (P[b + 1] == P[b]) {
-            zero_out(p.out, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D, p.out_dtype);
+            zero_outputs(p, static_cast<size_t>(b) * p.nq * p.Hq * D, p.nq * p.Hq * D);
         }
     }
     if (n_my <= 0) return;
@@ -690,11 +690,10 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
             const size_t dst = q_row(p, mc.b, kvh, hb * G + j) * D + lane * DL;
             const float inv = 1.f / Ls_[j];
             if constexpr (DL == 4) {
-                st_out4(p.out, dst, Ac[j][0] * inv, Ac[j][1] * inv, Ac[j][2] * inv, Ac[j][3] * inv,
-                        p.out_dtype);
+                store_out4(p, dst, Ac[j][0] * inv, Ac[j][1] * inv, Ac[j][2] * inv, Ac[j][3] * inv);
             } else {
 #pragma unroll
-                for (int e = 0; e < DL; ++e) st_out1(p.out, dst + e, Ac[j][e] * inv, p.out_dtype);
+                for (int e = 0; e < DL; ++e) store_out1(p, dst + e, Ac[j][e] * inv);
             }
         }
         if (lane == 0) p.counters[segg] = 0u;
@@ -995,8 +994,8 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
                         const size_t dst = q_row(p, cc.b, kvh, hb * G + j) * D + c * EPL;
 #pragma unroll
                         for (int e4 = 0; e4 < EPL / 4; ++e4)
-                            st_out4(p.out, dst + 4 * e4, o[j][4 * e4] * inv, o[j][4 * e4 + 1] * inv,
-                                    o[j][4 * e4 + 2] * inv, o[j][4 * e4 + 3] * inv, p.out_dtype);
+                            store_out4(p, dst + 4 * e4, o[j][4 * e4] * inv, o[j][4 * e4 + 1] * inv,
+                                       o[j][4 * e4 + 2] * inv, o[j][4 * e4 + 3] * inv);
                     }
                 }
             } else {

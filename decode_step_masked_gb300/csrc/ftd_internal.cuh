@@ -25,6 +25,9 @@ struct Plan {
     KernelInfo ki;
     TcChoice tcc;
     size_t rows;
+    // output projection (proj_dim > 0): tokens per step, tokens per block of the
+    // projection kernel, blocks, feature tiles of 128 and K chunks of 64
+    int tokens, ntb, nblk, mtiles, kch;
 };
 // Every check of a configuration (sizes, dtypes, options, 32-bit index bounds);
 // FTD_OK and the plan, or a status and a message in msg.

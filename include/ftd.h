@@ -123,6 +123,9 @@ typedef struct {
                               for every configuration (the tensor-core kernel is
                               otherwise taken for head_dim 128 caches whose kv heads
                               carry a multiple of 4 query rows, 8 for INT8) */
+    int proj_dim;          /* 0: no output projection; F > 0 (a multiple of 128): the
+                              context also serves ftd_decode_mha_proj, y = out . W_o^T
+                              with W_o [F][n_q_heads * head_dim] (F16 / BF16 qkv only) */
     int wait_limit_us;     /* 0: a kernel's bounded waits give up after about 2 s;
                               else after this many microseconds (measured in SM clock
                               cycles at the device's peak clock), raising
@@ -223,6 +226,30 @@ ftd_status ftd_decode_mha_paged(ftd_ctx* ctx, const void* q, const void* k_new, 
                                 const void* qkv_bias, void* k_pages, void* v_pages,
                                 const int32_t* block_table, const int32_t* seq_lens, float* scales,
                                 void* out, void* stream);
+
+/*
+ * ftd_decode_mha_proj -- ftd_decode_mha followed, in the same call and on the
+ * same stream, by the output projection of the step's result (the fused
+ * kernels hand their output straight to the next projection in half
+ * precision, "FasterTransformer practice", lpnh.cn, section 2.1):
+ *     y[b][t][f] = sum_k W_o[f][k] * out[b][t][k],   k < n_q_heads * head_dim,
+ * out taken as stored (its out_dtype) and flattened over heads.  The decode
+ * kernel's final stores also write each output value as a high and a low half
+ * of W_o's type into two planes of the context, so the product keeps about 16
+ * mantissa bits of an fp32 out; a second kernel, a tcgen05 GEMM that reads W_o
+ * once, starts while the decode kernel's last blocks finish (programmatic
+ * dependent launch) and writes y.
+ *   w_o : device [proj_dim][n_q_heads * head_dim] in the qkv dtype (F16 or
+ *         BF16; the layout of a linear layer's weight), 16-byte aligned, read only.
+ *   y   : device [B][T][proj_dim] of out_dtype, 16-byte aligned; every element
+ *         is written (zero for inactive and overflowing slots).
+ * Other arguments as in ftd_decode_mha; out is written as well.  Needs a
+ * context with proj_dim > 0 and a contiguous cache (INVALID_ARG otherwise).
+ * Launches two kernels; no host synchronisation and no allocation.
+ */
+ftd_status ftd_decode_mha_proj(ftd_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                               const void* qkv_bias, void* k_cache, void* v_cache, const int32_t* seq_lens,
+                               float* scales, void* out, const void* w_o, void* y, void* stream);
 
 /*
  * ftd_decode_mha_host -- the same step for callers whose per-step inputs live

@@ -43,7 +43,8 @@ def test_status_strings(lib):
 def cfg(**kw):
     base = dict(max_batch=4, n_q_heads=8, n_kv_heads=2, head_dim=128, max_len=256,
                 qkv_dtype=ftd.FTD_BF16, cache_dtype=ftd.FTD_BF16, softmax_scale=0.0,
-                out_dtype=ftd.FTD_F32, window=0, page_size=0, num_pages=0, q_len=0, kernel=0, wait_limit_us=0)
+                out_dtype=ftd.FTD_F32, window=0, page_size=0, num_pages=0, q_len=0, kernel=0, proj_dim=0,
+                wait_limit_us=0)
     base.update(kw)
     return ftd.FtdConfig(*[base[f] for f, _ in ftd.FtdConfig._fields_])
 
@@ -75,6 +76,9 @@ def cfg(**kw):
     (dict(kernel=2), ftd.FTD_ERR_INVALID_ARG),
     (dict(kernel=-1), ftd.FTD_ERR_INVALID_ARG),
     (dict(wait_limit_us=-5), ftd.FTD_ERR_INVALID_ARG),
+    (dict(proj_dim=-128), ftd.FTD_ERR_INVALID_ARG),
+    (dict(proj_dim=100), ftd.FTD_ERR_INVALID_ARG),
+    (dict(proj_dim=128, qkv_dtype=ftd.FTD_F32), ftd.FTD_ERR_UNSUPPORTED),
     # rows fit 32 bits (1024 x 1 x 2^20) but the tile space of 4096 query rows per kv head does not
     (dict(max_batch=1024, n_q_heads=64, n_kv_heads=1, max_len=1 << 20, q_len=64), ftd.FTD_ERR_UNSUPPORTED),
 ])
@@ -93,6 +97,7 @@ def test_null_arguments(lib):
     assert ftd.ftd_decode_mha(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_decode_mha_host(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_decode_mha_paged(0, 16, 16, 16, 0, 16, 16, 16, 16, 0, 16, 0) == ftd.FTD_ERR_INVALID_ARG
+    assert ftd.ftd_decode_mha_proj(0, 16, 16, 16, 0, 16, 16, 16, 0, 16, 16, 16, 0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_get_error(0) == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_cache_ptrs(0)[0] == ftd.FTD_ERR_INVALID_ARG
     assert ftd.ftd_debug_stall_next(0, 1) == ftd.FTD_ERR_INVALID_ARG
