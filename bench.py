@@ -46,7 +46,8 @@ EB = {"f32": 4, "f16": 2, "bf16": 2, "i8": 1}
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
                   "decode_step_masked_gb300/csrc/ftd_decode_splitk.cuh",
-                  "decode_step_masked_gb300/csrc/ftd_decode_gqa_tc.cuh")
+                  "decode_step_masked_gb300/csrc/ftd_decode_gqa_tc.cuh",
+                  "decode_step_masked_gb300/csrc/ftd_decode_wide_tc.cuh")  # the kernels of the traffic captures
 
 
 # option cases the bench times next to the plain step (half output, window, paged cache)
@@ -62,6 +63,8 @@ def kernel_name(w, q_len=1) -> str:
     rows = max(1, q_len) * w.Hq // w.Hkv
     tc = (w.D == 128
           and ((w.cache_dtype in ("f16", "bf16") and rows % 4 == 0) or (w.cache_dtype == "i8" and rows % 8 == 0)))
+    if tc and w.cache_dtype != "i8" and rows % 32 == 0:
+        return "decode_wide_tc_kernel"
     return "decode_gqa_tc_kernel" if tc else "decode_splitk_kernel"
 
 

@@ -22,6 +22,7 @@
 #include "ftd_decode_splitk.cuh"
 #include "ftd_decode_gqa_tc.cuh"
 #include "ftd_internal.cuh"
+#include "ftd_decode_wide_tc.cuh"
 #include "ftd_out_proj.cuh"
 
 namespace {
@@ -128,7 +129,8 @@ namespace ftd {
 // fp16/bf16 caches with head_dim 128 whose kv heads carry a multiple of 4 query
 // rows (group x new tokens) use the tensor-core kernel, in blocks of 16 or 8
 // rows (blocks of 4 fill half of an 8-column block, since the MMA needs N >= 16
-// with the hi/lo split).  INT8 caches with head_dim 128 and a multiple of 8
+// with the hi/lo split), or its wide variant in blocks of 64 or 32 rows when the
+// rows are a multiple of 32.  INT8 caches with head_dim 128 and a multiple of 8
 // query rows per kv head use its INT8 variant, in blocks of 8.
 // cfg.kernel == FTD_KERNEL_CUDA_CORE selects the CUDA-core kernel instead.
 // Internal to the library (hidden), shared by ftd_init and the no-allocation
@@ -143,9 +145,16 @@ __attribute__((visibility("hidden"))) TcChoice choose_tc(const ftd_config& c) {
                          rows_q % 4 == 0 && !forced;
     const bool want_tc_i8 = c.cache_dtype == FTD_I8 && c.head_dim == 128 && rows_q % 8 == 0 && !forced;
     if ((want_tc || want_tc_i8) && encode_tiled()) {
-        const int Gt = (rows_q % 16 == 0 && !want_tc_i8) ? 16 : 8;
-        r.qblk = rows_q % 8 == 0 ? Gt : 4;
-        r.tki = want_tc_i8 ? select_tc_i8(c.q_len > 1) : select_tc(c.cache_dtype == FTD_BF16, Gt, c.q_len > 1);
+        if (want_tc && rows_q % 32 == 0) {
+            // 32 or more query rows per kv head: the wide kernel, all rows of a block of
+            // 32 or 64 in one pass per tile
+            r.qblk = rows_q % 64 == 0 ? 64 : 32;
+            r.tki = select_wide(c.cache_dtype == FTD_BF16, r.qblk, c.q_len > 1);
+        } else {
+            const int Gt = (rows_q % 16 == 0 && !want_tc_i8) ? 16 : 8;
+            r.qblk = rows_q % 8 == 0 ? Gt : 4;
+            r.tki = want_tc_i8 ? select_tc_i8(c.q_len > 1) : select_tc(c.cache_dtype == FTD_BF16, Gt, c.q_len > 1);
+        }
         r.nhb = rows_q / r.qblk;
     }
     return r;

@@ -116,12 +116,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
 }
 
 // kind::f16 instruction descriptor: fp32 accumulate, A/B bf16 (or fp16), M x N.
-__device__ __forceinline__ uint32_t instr_desc(bool bf16, int M, int N, bool a_mn_major) {
+__device__ __forceinline__ uint32_t instr_desc(bool bf16, int M, int N, bool a_mn_major, bool b_mn_major = false) {
     uint32_t d = 0;
     d |= 1u << 4;                                  // D: f32
     d |= (bf16 ? 1u : 0u) << 7;                    // A type
     d |= (bf16 ? 1u : 0u) << 10;                   // B type
     d |= (a_mn_major ? 1u : 0u) << 15;             // A major-ness
+    d |= (b_mn_major ? 1u : 0u) << 16;             // B major-ness
     d |= static_cast<uint32_t>(N >> 3) << 17;
     d |= static_cast<uint32_t>(M >> 4) << 24;
     return d;

@@ -5,7 +5,7 @@
 #include <cuda.h>
 
 #include "../../include/ftd.h"
-#include "ftd_decode_gqa_tc.cuh"
+#include "ftd_decode_wide_tc.cuh"
 
 namespace ftd {
 // The tensor-core kernel a configuration runs (tki.fn null: the CUDA-core

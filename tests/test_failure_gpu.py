@@ -32,7 +32,8 @@ def _built():
 # name: (cache, qkv, Hq, Hkv, force the CUDA-core kernel)
 CASES = {"tc_bf16": ("bf16", "bf16", 16, 2, False), "splitk_bf16": ("bf16", "bf16", 16, 2, True),
          "splitk_mha_f16": ("f16", "f16", 4, 4, False), "tc_i8": ("i8", "f16", 16, 2, False),
-         "splitk_i8": ("i8", "f16", 4, 4, False)}
+         "splitk_i8": ("i8", "f16", 4, 4, False), "tc_wide_mqa": ("bf16", "bf16", 64, 1, False),
+         "tc_wide_32": ("f16", "f16", 32, 1, False)}
 
 
 def case(name, lens, seed):
