@@ -319,6 +319,75 @@ __device__ __forceinline__ void with_qkv_type(int dt, F&& f) {
     else f(__nv_bfloat16{});
 }
 
+// The q of the block of piece c into Qs (the caller publishes it).  With check, the
+// lengths are read again (lengths_changed) while the q loads are in flight, and q is
+// written only when they are unchanged; returns whether they changed.  Out of line:
+// it runs once per piece, and one copy serves every call site.
+template <typename CT, int G, bool MQ>
+static __device__ __noinline__ bool stage_q_fn(const DecodeParams& p, const Cursor c, int st, unsigned char* Qs,
+                                               const int* Ls, bool check) {
+    bool changed = false;
+    with_qkv_type(p.qkv_dtype, [&](auto tag) {
+        using T = decltype(tag);
+        QRaw<T, G> x;
+        fetch_q<T, G, MQ>(p, c, st, x);
+        if (check) changed = lengths_changed(p, Ls, threadIdx.x & 31);
+        if (!changed) put_q<CT, T, G>(Qs, x, p, st);
+    });
+    return changed;
+}
+
+
+// The append of a segment's last tile, by the issuing warp: the new tokens' K and V
+// rows (rows L - t0 .. of the staged tile, and of the cache when the block is the kv
+// head's first) and zeros in the staged V rows past the end.  Out of line: it runs
+// once per segment.
+template <typename CT>
+static __device__ __noinline__ void append_rows(const DecodeParams& p, unsigned char* st, int b, int seg, int tile,
+                                                int L, int lane) {
+    constexpr int TM = tc::TM, D = tc::D, KB = tc::KB;
+    const int t0 = (window_start(L, p.window) / TM + tile) * TM;
+    const int n_total = min(TM, L + p.nq - t0);
+    const int kvh = seg / p.nhb, hb = seg % p.nhb;
+    const int nz = (TM - n_total) * 8;
+    for (int c = lane; c < 2 * nz; c += 32) {
+        const int box = c / nz, rem = c - box * nz;
+        const int r = n_total + (rem >> 3);
+        *reinterpret_cast<uint4*>(st + 2 * KB + box * KB + r * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    for (int nr = max(0, L - t0); nr < n_total; ++nr) {
+        const int tok = t0 + nr - L, pos = t0 + nr;
+        const bool isv = lane >= 16;
+        const int d0 = (lane & 15) * 8;
+        const void* src = isv ? p.v_new : p.k_new;
+        const size_t si = ((static_cast<size_t>(b) * p.nq + tok) * p.Hkv + kvh) * D + d0;
+        const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + d0;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float x0 = ld_qkv(src, p.qkv_dtype, si + 2 * e);
+            float x1 = ld_qkv(src, p.qkv_dtype, si + 2 * e + 1);
+            if (p.bias) {
+                x0 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e);
+                x1 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e + 1);
+            }
+            const CT y0 = tc::to_ct<CT>(x0), y1 = tc::to_ct<CT>(x1);
+            uint16_t u0, u1;
+            memcpy(&u0, &y0, 2);
+            memcpy(&u1, &y1, 2);
+            w[e] = static_cast<uint32_t>(u0) | (static_cast<uint32_t>(u1) << 16);
+        }
+        const uint4 wv = make_uint4(w[0], w[1], w[2], w[3]);
+        unsigned char* srow =
+            st + (isv ? 2 * KB : 0) + (d0 >> 6) * KB + nr * 128 + ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
+        *reinterpret_cast<uint4*>(srow) = wv;
+        if (hb == 0) {
+            const long long rowg = cache_row(p, b, kvh, pos, page_of(p, b, pos));
+            if (rowg >= 0) *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + (rowg * D + d0) * 2) = wv;
+        }
+    }
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                  "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
@@ -410,30 +479,20 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
     const bool leader = warp == 2 && lane == 0;
     // q of the block's piece at cursor c into Qs (the softmax warps), then QReady for the
     // issuer, which waits for it before the piece's first score MMA
-    auto publish_q = [&](auto tag, const auto& x) {
-        wide::put_q<CT, decltype(tag), G>(Qs, x, p, st);
+    auto publish_q = [&]() {
         fence_proxy_async_smem();
         tc::named_bar_sync(1, SMX);
         if (leader) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kQReady)) : "memory");
     };
     auto stage_q = [&](const Cursor& c) {
-        wide::with_qkv_type(p.qkv_dtype, [&](auto tag) {
-            using T = decltype(tag);
-            wide::QRaw<T, G> x;
-            wide::fetch_q<T, G, MQ>(p, c, st, x);
-            publish_q(tag, x);
-        });
+        wide::stage_q_fn<CT, G, MQ>(p, c, st, Qs, Ls, false);
+        publish_q();
     };
     // the softmax warps fetch the first piece's q (as planned) while the lengths are checked
     bool changed;
     if (warp >= 2 && n_my > 0) {
-        wide::with_qkv_type(p.qkv_dtype, [&](auto tag) {
-            using T = decltype(tag);
-            wide::QRaw<T, G> x;
-            wide::fetch_q<T, G, MQ>(p, locate_pass(t_begin, P, p.B, spp, np), st, x);
-            changed = lengths_changed(p, Ls, lane);
-            if (!changed) publish_q(tag, x);
-        });
+        changed = wide::stage_q_fn<CT, G, MQ>(p, locate_pass(t_begin, P, p.B, spp, np), st, Qs, Ls, true);
+        if (!changed) publish_q();
     } else {
         changed = lengths_changed(p, Ls, lane);
     }
@@ -598,51 +657,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                     __syncwarp();
                 }
                 if (has_new) {
-                    // ---- append the new tokens (rows L - t0 ..) and zero staged V rows past the end ----
-                    const int L = Ls[cu.b];
-                    const int t0 = (window_start(L, p.window) / TM + cu.tile) * TM;
-                    const int n_total = min(TM, L + p.nq - t0);
-                    const int kvh = cu.seg / p.nhb, hb = cu.seg % p.nhb;
-                    unsigned char* st = stages + s * tc::STAGE;
-                    const int nz = (TM - n_total) * 8;
-                    for (int c = lane; c < 2 * nz; c += 32) {
-                        const int box = c / nz, rem = c - box * nz;
-                        const int r = n_total + (rem >> 3);
-                        *reinterpret_cast<uint4*>(st + 2 * KB + box * KB + r * 128 + (rem & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    for (int nr = max(0, L - t0); nr < n_total; ++nr) {
-                        const int tok = t0 + nr - L, pos = t0 + nr;
-                        const bool isv = lane >= 16;
-                        const int d0 = (lane & 15) * 8;
-                        const void* src = isv ? p.v_new : p.k_new;
-                        const size_t si = ((static_cast<size_t>(cu.b) * p.nq + tok) * p.Hkv + kvh) * D + d0;
-                        const size_t bi = static_cast<size_t>(p.Hq + (isv ? p.Hkv : 0) + kvh) * D + d0;
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            float x0 = ld_qkv(src, p.qkv_dtype, si + 2 * e);
-                            float x1 = ld_qkv(src, p.qkv_dtype, si + 2 * e + 1);
-                            if (p.bias) {
-                                x0 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e);
-                                x1 += ld_qkv(p.bias, p.qkv_dtype, bi + 2 * e + 1);
-                            }
-                            const CT y0 = tc::to_ct<CT>(x0), y1 = tc::to_ct<CT>(x1);
-                            uint16_t u0, u1;
-                            memcpy(&u0, &y0, 2);
-                            memcpy(&u1, &y1, 2);
-                            w[e] = static_cast<uint32_t>(u0) | (static_cast<uint32_t>(u1) << 16);
-                        }
-                        const uint4 wv = make_uint4(w[0], w[1], w[2], w[3]);
-                        unsigned char* srow = st + (isv ? 2 * KB : 0) + (d0 >> 6) * KB + nr * 128 +
-                                              ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
-                        *reinterpret_cast<uint4*>(srow) = wv;
-                        if (hb == 0) {
-                            const long long rowg = cache_row(p, cu.b, kvh, pos, page_of(p, cu.b, pos));
-                            if (rowg >= 0)
-                                *reinterpret_cast<uint4*>((isv ? p.v_cache : p.k_cache) + (rowg * D + d0) * 2) = wv;
-                        }
-                    }
+                    wide::append_rows<CT>(p, stages + s * tc::STAGE, cu.b, cu.seg, cu.tile, Ls[cu.b], lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
@@ -845,10 +860,24 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                 };
                 const int ss = kPasses ? kvh : cu.seg, sh_ = kPasses ? hb : 0;
                 const int segg = seg_ordinal(p.B, spp, cu.b, ss, sh_);
+                // the block's final rows go through shared memory (the weights buffer is free once
+                // the piece's last P.V is done) to one compact loop of 16-byte stores
+                auto flush_rows = [&](const float (&v)[GH]) {
+                    float* ostg = reinterpret_cast<float*>(Ps);
+#pragma unroll
+                    for (int jj = 0; jj < GH; ++jj) ostg[(c0 + jj) * D + r] = v[jj];
+                    tc::named_bar_sync(1, SMX);
+#pragma unroll 1
+                    for (int idx = st; idx < QB * (D / 4); idx += SMX) {
+                        const int j = idx / (D / 4), d0 = (idx % (D / 4)) * 4;
+                        const float4 x = *reinterpret_cast<const float4*>(ostg + j * D + d0);
+                        store_out4(p, orow(cu.b, kvh, hb * QB + j) * D + d0, x.x, x.y, x.z, x.w);
+                    }
+                };
                 if (piece_first == 0 && seg_end) {
 #pragma unroll
-                    for (int jj = 0; jj < GH; ++jj)
-                        if (c0 + jj < QB) store_out1(p, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r, o[jj] / ltot(jj));
+                    for (int jj = 0; jj < GH; ++jj) o[jj] /= ltot(jj);
+                    flush_rows(o);
                 } else {
                     float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
                     if (r == 0) {
@@ -930,9 +959,8 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                             tc::named_bar_sync(1, SMX);
                         }
 #pragma unroll
-                        for (int jj = 0; jj < GH; ++jj)
-                            if (c0 + jj < QB)
-                                store_out1(p, orow(cu.b, kvh, hb * QB + c0 + jj) * D + r, o[jj] / mrg[G + c0 + jj]);
+                        for (int jj = 0; jj < GH; ++jj) o[jj] /= mrg[G + c0 + jj];
+                        flush_rows(o);
                         if (leader) p.counters[segg] = 0u;
                     }
                     tc::named_bar_sync(1, SMX);
