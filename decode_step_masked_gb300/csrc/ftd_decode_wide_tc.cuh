@@ -44,10 +44,6 @@ namespace wide {
 constexpr int NS = 2;                       // K / V stages (64 KB each)
 constexpr int SH = 2;                       // softmax groups (G / 2 query rows per thread)
 constexpr int kThreads = 64 + 128 * SH;     // producer and MMA warps, then the softmax warps
-// Tiles kept in flight toward L2 ahead of the 2-stage ring: under a full-GPU stream a
-// tile copy takes several microseconds, longer than two tiles' work, so the producer
-// prefetches K and V of tile k + kAhead into L2 when it issues the copy of K(k).
-constexpr int kAhead = 4;
 // Running reference of a query row before its first visible score: finite, so that
 // s - m needs no test for "no reference yet" (a visible score always passes it by
 // more than 2^8, and a masked one gives exp2(-inf) = 0).
@@ -533,26 +529,6 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                     }
                     return static_cast<int>(rb);
                 };
-                // L2 prefetch of K and V of the tile at cursor c
-                auto prefetch_tile = [&](const Cursor& c, PageCursor& pc) {
-                    const int L = Ls[c.b];
-                    const int t0 = (window_start(L, p.window) / TM + c.tile) * TM;
-                    const int n_cache = min(TM, max(0, L - t0));
-                    const long long rb = cache_row(p, c.b, c.seg / p.nhb, t0, pc.page(p, c.b, t0));
-                    if (n_cache > 0 && rb >= 0) {
-                        bulk_prefetch_l2(p.k_cache + rb * D * 2, static_cast<uint32_t>(n_cache) * D * 2);
-                        bulk_prefetch_l2(p.v_cache + rb * D * 2, static_cast<uint32_t>(n_cache) * D * 2);
-                    }
-                };
-                // the first NS tiles were prefetched before the wait (contiguous caches; only
-                // those, so that the small loads right after the wait are not queued behind
-                // more), tiles NS .. kAhead - 1 are prefetched here
-                Cursor cpf = ck;
-                PageCursor ppf;
-                for (int i = 0; i < min(wide::kAhead, n_my); ++i) {
-                    if (i >= NS) prefetch_tile(cpf, ppf);
-                    if (i + 1 < n_my) advance_pass(cpf, P, p.B, spp, np);
-                }
                 int kk = 0, kv = 0;
                 if (withhold0) {
                     if (n_my > 1) advance_pass(ck, P, p.B, spp, np);
@@ -569,10 +545,6 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                         mbar_arrive_expect_tx(bar(kFullK + s), 2 * KB);
                         tc::tma_load_2d(st, &tmk, 0, row0, bar(kFullK + s), l2pol);
                         tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kFullK + s), l2pol);
-                        if (kk + wide::kAhead < n_my) {
-                            prefetch_tile(cpf, ppf);
-                            if (kk + wide::kAhead + 1 < n_my) advance_pass(cpf, P, p.B, spp, np);
-                        }
                         if (kk + 1 < n_my) advance_pass(ck, P, p.B, spp, np);
                         ++kk;
                     } else {
