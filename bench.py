@@ -54,7 +54,7 @@ KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
 OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("13b", dict(page_size=256)),
                 ("70b", dict(out_dtype="bf16")), ("70b", dict(window=1024)), ("70b", dict(page_size=256)),
                 ("int8", dict(page_size=256)), ("7b", dict(q_len=4)), ("7b", dict(q_len=8)),
-                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)), ("mqa", {}), ("70b_i8", {}),
+                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)),
                 ("7b", dict(proj_dim=4096)), ("13b", dict(proj_dim=5120)), ("70b", dict(proj_dim=8192))]
 
 
@@ -641,7 +641,7 @@ def main():
         line["e2e"] = e2e_leg(w, lens, by, device, stream, min(args.steps, 2000))
         # ---- every large workload of the suite, same protocol, each with its roofline ----
         per_cfg = {}
-        for name in ("7b", "13b", "70b", "int8", "tiny"):
+        for name in ("7b", "13b", "70b", "int8", "mqa", "70b_i8", "tiny"):
             if name == w.name:
                 per_cfg[name] = dict(us=line["us_per_step"], gbs=value / world, frac=value / world / peaks["hbm_gbs"],
                                      kv_mb=by["kv"] / 1e6, roofline=line["roofline"])
