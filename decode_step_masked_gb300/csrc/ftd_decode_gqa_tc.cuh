@@ -27,7 +27,9 @@
 //           the sequence end (so 0 * garbage never reaches the product), then
 //           lane 0 issues the MMAs;
 //   warps 2-3 and 12-19 (INT8 only) the append of quantised rows and the
-//           conversion of the codes into fp16 operand stages;
+//           conversion of the codes to fp16: K straight into TMEM (warps 12-19,
+//           two per TMEM lane quarter; the score MMA reads its A operand there),
+//           V into the V halves of two operand stages;
 //   warps 4.. the online softmax in groups of four warps that split the query
 //           columns: thread i of a group owns row i of S and dimension i of O;
 //           they build Qs, read S from TMEM, keep the running max / sum per
@@ -77,15 +79,21 @@ template <int G, bool I8 = false>
 struct Layout {
     static constexpr int N = 2 * G;                // hi and lo parts
     static constexpr int QS = 2 * N * 128;         // Qs / Ps: 2 k-blocks of N rows x 128 B
-    // operand stages the MMAs read: the TMA ring itself (fp16 / bf16), or two
-    // stages of fp16 codes that warps 2-3 convert from two raw INT8 stages
+    // operand stages the MMAs read: the TMA ring itself (fp16 / bf16), or, for INT8, two
+    // stages whose V half the converting warps widen from two raw stages of codes (the K
+    // operand goes to TMEM).  Measured on the INT8 70B step: V-only stages of 32 KB with
+    // 2 / 3 / 4 raw stages ran 94.7 / 93.8 / 94.0 us, these 64 KB stages with 2 raw stages
+    // 92.6 us, so the stage geometry stays that of the fp16 ring.
     static constexpr int NB = I8 ? 2 : NS;
+    static constexpr int NR = 2;                                            // INT8 raw stages
+    static constexpr int SSTR = STAGE;                                      // operand stage stride
+    static constexpr int VOFF = 2 * KB;                                     // the V half in a stage
     static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_S8 = NB * STAGE;                                // raw INT8 stages
+    static constexpr int OFF_S8 = NB * SSTR;                                 // raw INT8 stages
     // [4][K | V][TM] scales, slot k % 4: the softmax of tile k reads its slot until
     // it publishes P, and the slot is rewritten for tile k + 4 only after the score
     // MMAs of tile k + 2, which follow the P.V issue of tile k
-    static constexpr int OFF_SC = OFF_S8 + (I8 ? 2 * round_up(STAGE8, 1024) : 0);
+    static constexpr int OFF_SC = OFF_S8 + (I8 ? NR * round_up(STAGE8, 1024) : 0);
     static constexpr int OFF_QS = OFF_SC + (I8 ? 4 * 2 * TM * 4 : 0);
     static constexpr int OFF_P = OFF_QS + round_up(QS, 1024);
     static constexpr int OFF_RED = OFF_P + 2 * round_up(QS, 1024);
@@ -98,7 +106,11 @@ struct Layout {
     static constexpr int ALPHA = HAVE_VP ? kAlpha : 0;
     static constexpr int PREFIX_BYTES = ((HAVE_VP ? 3 : 2) * kMaxBatch + 2) * 4;
     static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;  // + alignment slack
-    static constexpr int TMEM_COLS = (4 * N <= 32) ? 32 : (4 * N <= 64 ? 64 : 128);
+    // S (2 x N columns) and O (2 x N); INT8 adds the score MMAs' K operand, widened from
+    // the codes straight into TMEM: two buffers of 64 columns (128 fp16 values per row) at KT
+    static constexpr int KT = 64;
+    static constexpr int TMEM_COLS = I8 ? 256 : ((4 * N <= 32) ? 32 : (4 * N <= 64 ? 64 : 128));
+    static_assert(!I8 || 4 * N <= KT, "INT8: S and O below the K operand buffers");
     static constexpr int OOFF = round_up(2 * G, 4);
     static constexpr int SLOT = OOFF + G * D;
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -133,6 +145,15 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b,
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
         "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1 : 0));
+}
+
+// The same with the A operand in TMEM (row m on lane m, elements k and k + 1 in the low and
+// high halves of column k / 2; checked on the GPU against a CPU product before use).
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc ? 1 : 0));
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -191,6 +212,15 @@ __device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, float (&v)[32]) {
         v[i] = a[i];
         v[16 + i] = b[i];
     }
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
@@ -589,7 +619,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
             // addresses stay below 256 KB, so the field never carries), which keeps
             // the issuing thread's chain per MMA to an add and the MMA itself.
             const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(stages), 16, 1024);
-            const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(stages) + 2 * KB, tc::kVLbo, tc::kVSbo);
+            const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(stages) + LY::VOFF, tc::kVLbo, tc::kVSbo);
             const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(Qs), 16, 1024);
             const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(Ps), 16, 1024);
             auto issue_pv = [&](int kk) -> bool {
@@ -598,7 +628,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                 if (__any_sync(FULL, !w)) return false;
                 if (lane == 0) {
                     tc::tc_fence_after();
-                    const uint64_t va = dv0 + static_cast<uint32_t>((kk % NB) * (tc::STAGE >> 4));
+                    const uint64_t va = dv0 + static_cast<uint32_t>((kk % NB) * (LY::SSTR >> 4));
                     const uint64_t pa = dp0 + static_cast<uint32_t>((kk & 1) * (PSZ >> 4));
 #pragma unroll
                     for (int ks = 0; ks < TM / 16; ++ks) {
@@ -696,9 +726,14 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                     const uint64_t ka = dk0 + static_cast<uint32_t>(s * (tc::STAGE >> 4));
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t a = ka + (((ks >> 2) * KB + (ks & 3) * 32) >> 4);
                         const uint64_t bd = dq0 + (((ks >> 2) * (N * 128) + (ks & 3) * 32) >> 4);
-                        tc::mma_f16(tmem + (k & 1) * N, a, bd, id_s, ks > 0);
+                        if constexpr (I8) {
+                            // K in TMEM buffer s: 16 elements of each row = 8 columns per MMA
+                            tc::mma_f16_ta(tmem + (k & 1) * N, tmem + LY::KT * (1 + s) + ks * 8, bd, id_s, ks > 0);
+                        } else {
+                            const uint64_t a = ka + (((ks >> 2) * KB + (ks & 3) * 32) >> 4);
+                            tc::mma_f16(tmem + (k & 1) * N, a, bd, id_s, ks > 0);
+                        }
                     }
                     tc::mma_commit(bar(kBarSFull + (k & 1)));
                     if constexpr (I8) tc::mma_commit(bar(kBarEmpty + s));  // the K half is read
@@ -768,12 +803,11 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                         }
                     }
                 }
-                // Codes to fp16, one half of the operand stage: half 0 (K) once the score
-                // MMAs of tile k - NB have read it, half 1 (V) once its P.V MMAs have.
-                // Each thread converts 16-code chunks (row r, chunk j) of the half, rows
-                // fastest across the threads: with both layouts swizzled, the eight
-                // rows a quarter-warp touches fall in distinct banks.
-                unsigned char* dst = stages + sb * tc::STAGE;
+                // V codes to the fp16 operand stage sb once the P.V MMAs of tile k - NB have
+                // read it.  Each thread converts 16-code chunks (row r, chunk j), rows fastest
+                // across the threads: with both layouts swizzled, the eight rows a
+                // quarter-warp touches fall in distinct banks.
+                unsigned char* dst = stages + sb * LY::SSTR;
                 // (Not unrolled: with four roles' loops sharing each SM sub-partition's
                 // instruction cache, the unrolled copy stalled on instruction fetch and
                 // cost 30 % of the step.)
@@ -790,7 +824,7 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                         const uint4 h1 = make_uint4(tc::codes_to_h2(a2, 0x4140), tc::codes_to_h2(a2, 0x4342),
                                                     tc::codes_to_h2(a3, 0x4140), tc::codes_to_h2(a3, 0x4342));
                         // fp16 columns 16 j .. 16 j + 15: box j / 4, 16-byte chunks 2 (j % 4) and +1
-                        unsigned char* row = dst + v * 2 * KB + (j >> 2) * KB + r * 128;
+                        unsigned char* row = dst + LY::VOFF + (j >> 2) * KB + r * 128;
                         const int c16 = 2 * (j & 3);
                         *reinterpret_cast<uint4*>(row + ((c16 ^ (r & 7)) << 4)) = h0;
                         *reinterpret_cast<uint4*>(row + (((c16 + 1) ^ (r & 7)) << 4)) = h1;
@@ -800,7 +834,33 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
                 if (k >= NB) oke = tc::wait_or_abort(bar(kBarEmpty + sb), ((k / NB) - 1) & 1, p.err, abort_flag, p.wait_cycles);
                 // (the barrier also makes the appended rows visible to both warps)
                 if (tc::bar_any(3, NCV, !oke)) break;
-                convert(0);
+                if (warp >= 4) {
+                    // K straight into TMEM buffer sb, the score MMAs' A operand: warps 12-19,
+                    // two per TMEM lane quarter, each widening half of its 32 rows' dimensions
+                    tc::tc_fence_after();
+                    const int h = (warp - (4 + 4 * SH)) >> 2, rr = (warp & 3) * 32 + lane;
+                    uint32_t wk[32];
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj) {
+                        const int j = 4 * h + jj;
+                        const uint4 u = *reinterpret_cast<const uint4*>(st8 + rr * D + ((j ^ (rr & 7)) << 4));
+                        const uint32_t a0 = u.x ^ 0x80808080u, a1 = u.y ^ 0x80808080u;
+                        const uint32_t a2 = u.z ^ 0x80808080u, a3 = u.w ^ 0x80808080u;
+                        wk[8 * jj + 0] = tc::codes_to_h2(a0, 0x4140);
+                        wk[8 * jj + 1] = tc::codes_to_h2(a0, 0x4342);
+                        wk[8 * jj + 2] = tc::codes_to_h2(a1, 0x4140);
+                        wk[8 * jj + 3] = tc::codes_to_h2(a1, 0x4342);
+                        wk[8 * jj + 4] = tc::codes_to_h2(a2, 0x4140);
+                        wk[8 * jj + 5] = tc::codes_to_h2(a2, 0x4342);
+                        wk[8 * jj + 6] = tc::codes_to_h2(a3, 0x4140);
+                        wk[8 * jj + 7] = tc::codes_to_h2(a3, 0x4342);
+                    }
+                    const uint32_t ta = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + LY::KT * (1 + sb) + 32 * h;
+                    tc::tmem_st16(ta, wk);
+                    tc::tmem_st16(ta + 16, wk + 16);
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc::tc_fence_before();
+                }
                 for (int i = ct; i < 2 * TM; i += NCV) scl[(k & 3) * 2 * TM + i] = ssc[i];  // K and V scales
                 fence_proxy_async_smem();  // the MMAs read the stage through the async proxy
                 tc::named_bar_sync(3, NCV);
