@@ -41,7 +41,11 @@
 namespace ftd {
 namespace wide {
 
-constexpr int NS = 2;                       // K / V stages (64 KB each)
+constexpr int NS = 2;                       // K slots of the ring (32 KB each)
+// V slots (32 KB each): three where the 32-row block's Q and weight buffers leave room,
+// since the P.V MMAs wait on V copies, which a slot frees only after its P.V MMAs
+constexpr int nsv(int G) { return G == 32 ? 3 : 2; }
+constexpr int kMaxNsv = 3;
 constexpr int SH = 2;                       // softmax groups (G / 2 query rows per thread)
 constexpr int kThreads = 64 + 128 * SH;     // producer and MMA warps, then the softmax warps
 // Running reference of a query row before its first visible score: finite, so that
@@ -54,7 +58,9 @@ struct Layout {
     static constexpr int QS = 2 * (2 * G) * 128;     // Qs: 2 k-blocks (64 dims) of 2G rows (hi, lo) x 128 B
     static constexpr int PS = (2 * G / 64) * tc::KB; // Ps: 64-column atoms of 128 key rows x 128 B
     static constexpr int P_LO = (G / 64) * tc::KB + (G % 64) * 2;  // byte offset of the lo weights (column G)
-    static constexpr int OFF_QS = NS * tc::STAGE;
+    static constexpr int NSV = nsv(G);
+    static constexpr int OFF_V = NS * 2 * tc::KB;                // the V ring after the K ring
+    static constexpr int OFF_QS = OFF_V + NSV * 2 * tc::KB;
     static constexpr int OFF_P = OFF_QS + QS;
     static constexpr int OFF_RED = OFF_P + PS;
     // per warp of a group, per row: max and sum; then the merge's per-row state (running
@@ -84,9 +90,22 @@ struct Layout {
 
 // barriers (count 1 each): the K and V halves of a stage fill and empty separately,
 // K after the score MMA, V after the P.V MMA, so the next tiles' K copies run ahead
-enum : int { kFullK = 0, kEmptyK = NS, kFullV = 2 * NS, kEmptyV = 3 * NS, kSFull = 4 * NS, kPFull = 4 * NS + 2,
-             kOFull = 4 * NS + 3, kOFree = 4 * NS + 4, kQReady = 4 * NS + 5, kDrain = 4 * NS + 6,
-             kNumBarsW = 4 * NS + 7 };
+enum : int { kFullK = 0, kEmptyK = NS, kFullV = 2 * NS, kEmptyV = 2 * NS + kMaxNsv, kSFull = 2 * NS + 2 * kMaxNsv,
+             kPFull = kSFull + 2, kOFull = kSFull + 3, kOFree = kSFull + 4, kQReady = kSFull + 5, kDrain = kSFull + 6,
+             kNumBarsW = kSFull + 7 };
+
+// Whether the phase of the given parity of the barrier has completed, without waiting.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 static_assert(kNumBarsW * 8 + 16 <= 256, "misc area");
 
 // 2^x (PTX ex2.approx.ftz: relative error about 2^-22, results below 2^-126 flush to 0)
@@ -340,12 +359,12 @@ static __device__ __noinline__ bool stage_q_fn(const DecodeParams& p, const Curs
 
 
 // The append of a segment's last tile, by the issuing warp: the new tokens' K and V
-// rows (rows L - t0 .. of the staged tile, and of the cache when the block is the kv
-// head's first) and zeros in the staged V rows past the end.  Out of line: it runs
-// once per segment.
+// rows (rows L - t0 .. of the staged K and V slots, and of the cache when the block is
+// the kv head's first) and zeros in the staged V rows past the end.  Out of line: it
+// runs once per segment.
 template <typename CT>
-static __device__ __noinline__ void append_rows(const DecodeParams& p, unsigned char* st, int b, int seg, int tile,
-                                                int L, int lane) {
+static __device__ __noinline__ void append_rows(const DecodeParams& p, unsigned char* kst, unsigned char* vst, int b,
+                                                int seg, int tile, int L, int lane) {
     constexpr int TM = tc::TM, D = tc::D, KB = tc::KB;
     const int t0 = (window_start(L, p.window) / TM + tile) * TM;
     const int n_total = min(TM, L + p.nq - t0);
@@ -354,7 +373,7 @@ static __device__ __noinline__ void append_rows(const DecodeParams& p, unsigned 
     for (int c = lane; c < 2 * nz; c += 32) {
         const int box = c / nz, rem = c - box * nz;
         const int r = n_total + (rem >> 3);
-        *reinterpret_cast<uint4*>(st + 2 * KB + box * KB + r * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(vst + box * KB + r * 128 + (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     for (int nr = max(0, L - t0); nr < n_total; ++nr) {
         const int tok = t0 + nr - L, pos = t0 + nr;
@@ -379,8 +398,7 @@ static __device__ __noinline__ void append_rows(const DecodeParams& p, unsigned 
             w[e] = static_cast<uint32_t>(u0) | (static_cast<uint32_t>(u1) << 16);
         }
         const uint4 wv = make_uint4(w[0], w[1], w[2], w[3]);
-        unsigned char* srow =
-            st + (isv ? 2 * KB : 0) + (d0 >> 6) * KB + nr * 128 + ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
+        unsigned char* srow = (isv ? vst : kst) + (d0 >> 6) * KB + nr * 128 + ((((d0 & 63) >> 3) ^ (nr & 7)) << 4);
         *reinterpret_cast<uint4*>(srow) = wv;
         if (hb == 0) {
             const long long rowg = cache_row(p, b, kvh, pos, page_of(p, b, pos));
@@ -518,8 +536,10 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
     if (n_my > 0) {
         if (warp == 0) {
             // ------------------------------------------------ TMA producer
-            // K halves run one tile ahead of V halves: K(k) needs only the score MMA of
-            // tile k - 2 to be done, V(k) the P.V MMA of tile k - 2.
+            // Two rings: K(k) may be copied once the score MMA of tile k - NS is done, V(k)
+            // once the P.V MMA of tile k - NSV is.  One thread polls both (test_wait, no
+            // blocking) and issues whichever copy has a free slot; a wait that makes no
+            // progress for the pipeline limit aborts as the other roles' waits do.
             if (lane == 0) {
                 Cursor ck = locate_pass(t_begin, P, p.B, spp, np), cv = ck;
                 PageCursor pk, pv;
@@ -534,36 +554,50 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                     }
                     return static_cast<int>(rb);
                 };
+                constexpr int NSV = LY::NSV;
                 int kk = 0, kv = 0;
                 if (withhold0) {
                     if (n_my > 1) advance_pass(ck, P, p.B, spp, np);
                     kk = 1;
                 }
-                while (kv < n_my) {
-                    if (kk < n_my && kk <= kv + 1) {
+                long long idle0 = clock64();
+                while (kk < n_my || kv < n_my) {
+                    bool did = false;
+                    if (kk < n_my) {
                         const int s = kk % NS;
-                        const int row0 = tile_row(ck, pk);
-                        if (kk >= NS && !tc::wait_or_abort(bar(kEmptyK + s), ((kk / NS) - 1) & 1, p.err, abort_flag,
-                                                           p.wait_cycles))
-                            break;
-                        const uint32_t st = smem_addr(stages + s * tc::STAGE);
-                        mbar_arrive_expect_tx(bar(kFullK + s), 2 * KB);
-                        tc::tma_load_2d(st, &tmk, 0, row0, bar(kFullK + s), l2pol);
-                        tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kFullK + s), l2pol);
-                        if (kk + 1 < n_my) advance_pass(ck, P, p.B, spp, np);
-                        ++kk;
+                        if (kk < NS || wide::mbar_test(bar(kEmptyK + s), ((kk / NS) - 1) & 1)) {
+                            const int row0 = tile_row(ck, pk);
+                            const uint32_t st = smem_addr(stages + s * 2 * KB);
+                            mbar_arrive_expect_tx(bar(kFullK + s), 2 * KB);
+                            tc::tma_load_2d(st, &tmk, 0, row0, bar(kFullK + s), l2pol);
+                            tc::tma_load_2d(st + KB, &tmk, 64, row0, bar(kFullK + s), l2pol);
+                            if (kk + 1 < n_my) advance_pass(ck, P, p.B, spp, np);
+                            ++kk;
+                            did = true;
+                        }
+                    }
+                    if (kv < n_my) {
+                        const int s = kv % NSV;
+                        if (kv < NSV || wide::mbar_test(bar(kEmptyV + s), ((kv / NSV) - 1) & 1)) {
+                            const int row0 = tile_row(cv, pv);
+                            const uint32_t st = smem_addr(stages + LY::OFF_V + s * 2 * KB);
+                            mbar_arrive_expect_tx(bar(kFullV + s), 2 * KB);
+                            tc::tma_load_2d(st, &tmv, 0, row0, bar(kFullV + s), l2pol);
+                            tc::tma_load_2d(st + KB, &tmv, 64, row0, bar(kFullV + s), l2pol);
+                            if (kv + 1 < n_my) advance_pass(cv, P, p.B, spp, np);
+                            ++kv;
+                            did = true;
+                        }
+                    }
+                    if (did) {
+                        idle0 = clock64();
                     } else {
-                        const int s = kv % NS;
-                        const int row0 = tile_row(cv, pv);
-                        if (kv >= NS && !tc::wait_or_abort(bar(kEmptyV + s), ((kv / NS) - 1) & 1, p.err, abort_flag,
-                                                           p.wait_cycles))
+                        if (*abort_flag) break;
+                        if (clock64() - idle0 > p.wait_cycles) {
+                            atomicOr(p.err, kErrTimeout);
+                            *abort_flag = 1;
                             break;
-                        const uint32_t st = smem_addr(stages + s * tc::STAGE);
-                        mbar_arrive_expect_tx(bar(kFullV + s), 2 * KB);
-                        tc::tma_load_2d(st + 2 * KB, &tmv, 0, row0, bar(kFullV + s), l2pol);
-                        tc::tma_load_2d(st + 3 * KB, &tmv, 64, row0, bar(kFullV + s), l2pol);
-                        if (kv + 1 < n_my) advance_pass(cv, P, p.B, spp, np);
-                        ++kv;
+                        }
                     }
                 }
                 prod_kk = kk;
@@ -575,7 +609,8 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
             const uint32_t id_s = tc::instr_desc(BF, TM, G, false);
             const uint32_t id_o = tc::instr_desc(BF, D, G, true, true);
             const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(stages), 16, 1024);
-            const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(stages) + 2 * KB, tc::kVLbo, tc::kVSbo);
+            const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(stages) + LY::OFF_V, tc::kVLbo, tc::kVSbo);
+            constexpr int NSV = LY::NSV;
             const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(Qs), 16, 1024);
             // the weights, MN-major: 64-column atoms of 128 key rows (16 KB apart), 8-row groups 1 KB apart
             const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(Ps), KB, 1024);
@@ -586,7 +621,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
             // P.V of a piece waits until the softmax has read the previous piece's O
             auto issue_pv = [&](int kk) -> bool {
                 bool w = tc::wait_or_abort(bar(kPFull), kk & 1, p.err, abort_flag, p.wait_cycles);
-                w = w && tc::wait_or_abort(bar(kFullV + kk % NS), (kk / NS) & 1, p.err, abort_flag, p.wait_cycles);
+                w = w && tc::wait_or_abort(bar(kFullV + kk % NSV), (kk / NSV) & 1, p.err, abort_flag, p.wait_cycles);
                 const bool first = pv_first[kk & 1];
                 if (first && opieces > 0)
                     w = w && tc::wait_or_abort(bar(kOFree), (opieces - 1) & 1, p.err, abort_flag, p.wait_cycles);
@@ -594,7 +629,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                 if (first) ++opieces;
                 if (lane == 0) {
                     tc::tc_fence_after();
-                    const uint64_t va = dv0 + static_cast<uint32_t>((kk % NS) * (tc::STAGE >> 4));
+                    const uint64_t va = dv0 + static_cast<uint32_t>((kk % NSV) * (2 * KB >> 4));
 #pragma unroll
                     for (int ks = 0; ks < TM / 16; ++ks) {
                         const uint64_t a = va + (ks * 2048 >> 4);
@@ -603,7 +638,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                         tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
                     }
                     tc::mma_commit(bar(kOFull));
-                    tc::mma_commit(bar(kEmptyV + kk % NS));
+                    tc::mma_commit(bar(kEmptyV + kk % NSV));
                 }
                 __syncwarp();
                 return true;
@@ -618,23 +653,24 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                     has_new = Ls[cu.b] < (window_start(Ls[cu.b], p.window) / TM + cu.tile + 1) * TM;
                 const bool patch_v = has_new || (cu.tile == 0 && p.window > 0);  // the V half is written here
                 bool wf = tc::wait_or_abort(bar(kFullK + s), (k / NS) & 1, p.err, abort_flag, p.wait_cycles);
-                if (patch_v) wf = wf && tc::wait_or_abort(bar(kFullV + s), (k / NS) & 1, p.err, abort_flag, p.wait_cycles);
+                if (patch_v) wf = wf && tc::wait_or_abort(bar(kFullV + k % NSV), (k / NSV) & 1, p.err, abort_flag, p.wait_cycles);
                 if (__any_sync(FULL, !wf)) { ok = false; break; }
                 if (cu.tile == 0 && p.window > 0) {
                     // rows of the first tile before the window start get weight 0; zero
                     // their staged V so stale or non-finite history cannot reach O
                     const int nlo = window_start(Ls[cu.b], p.window) % TM;
-                    unsigned char* st = stages + s * tc::STAGE;
+                    unsigned char* vst = stages + LY::OFF_V + (k % NSV) * 2 * KB;
                     for (int c = lane; c < 2 * nlo * 8; c += 32) {
                         const int box = c / (nlo * 8), rem = c - box * nlo * 8;
-                        *reinterpret_cast<uint4*>(st + 2 * KB + box * KB + (rem >> 3) * 128 + (rem & 7) * 16) =
+                        *reinterpret_cast<uint4*>(vst + box * KB + (rem >> 3) * 128 + (rem & 7) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                     }
                     if (nlo > 0) fence_proxy_async_smem();
                     __syncwarp();
                 }
                 if (has_new) {
-                    wide::append_rows<CT>(p, stages + s * tc::STAGE, cu.b, cu.seg, cu.tile, Ls[cu.b], lane);
+                    wide::append_rows<CT>(p, stages + s * 2 * KB, stages + LY::OFF_V + (k % NSV) * 2 * KB, cu.b, cu.seg,
+                                          cu.tile, Ls[cu.b], lane);
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
@@ -645,7 +681,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                 }
                 if (lane == 0) {
                     tc::tc_fence_after();
-                    const uint64_t ka = dk0 + static_cast<uint32_t>(s * (tc::STAGE >> 4));
+                    const uint64_t ka = dk0 + static_cast<uint32_t>(s * (2 * KB >> 4));
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks) {
                         const uint64_t a = ka + (((ks >> 2) * KB + (ks & 3) * 32) >> 4);
@@ -955,7 +991,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
         // a bounded wait ran out: wait (long drain limit) for the copies and MMAs in flight
         if (warp == 0 && lane == 0) {
             tc_drain_copies(bar(kFullK), NS, prod_kk, withhold0, p.err);
-            tc_drain_copies(bar(kFullV), NS, prod_kv, false, p.err);
+            tc_drain_copies(bar(kFullV), LY::NSV, prod_kv, false, p.err);
         }
         if (warp == 1 && lane == 0) mbar_wait_bounded(bar(kDrain), 0u, p.err, kDrainLimitCycles);
     }
