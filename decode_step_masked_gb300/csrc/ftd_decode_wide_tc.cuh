@@ -80,8 +80,7 @@ struct Layout {
     static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;
     // two S buffers (columns 0 and G) and O (column 2G)
     static constexpr int TMEM_COLS = 3 * G <= 128 ? 128 : 256;
-    // split-K partial of a piece: m and l of the G rows, then O transposed (dimension d's G
-    // rows contiguous at OOFF + d G, so each thread moves its rows with 16-byte accesses)
+    // split-K partial of a piece: m and l of the G rows, then O as G rows of D floats
     static constexpr int OOFF = round_up(2 * G, 4);
     static constexpr int SLOT = OOFF + G * tc::D;
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -856,128 +855,122 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                 if (k < n_my) advance_pass(nx, P, p.B, spp, np);
                 if (seg_end && k < n_my) stage_q(nx);
                 // ---- end of the piece: O after its last P.V ----
+                // O goes once through shared memory as rows x D floats (the weights buffer is
+                // free once the piece's last P.V is done); the partial, the merge and the
+                // block's rows then run as short loops of coalesced 16-byte accesses
                 if (!wait_o()) break;
-                float o[GH];
-                ld_rows(2 * G, o);
-                tc::tc_fence_before();
+                float* ostg = reinterpret_cast<float*>(Ps);
+                {
+                    float o[GH];
+                    ld_rows(2 * G, o);
+                    tc::tc_fence_before();
+#pragma unroll
+                    for (int jj = 0; jj < GH; ++jj) ostg[(c0 + jj) * D + r] = o[jj];
+                }
                 {
                     const float v = wide::rows_reduce<GH>(l, lane, add_op);
                     if (lane < GH) red_sum[q4 * G + c0 + lane] = v;
                 }
+                if (r == 0) {
+#pragma unroll
+                    for (int jj = 0; jj < GH; ++jj) mrg[c0 + jj] = m[jj];  // the piece's references
+                }
                 tc::named_bar_sync(1, SMX);
                 // O is read: the next piece's first P.V may overwrite it
                 if (leader) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar(kOFree)) : "memory");
-                auto ltot = [&](int jj) {
-                    const int j = c0 + jj;
-                    return red_sum[j] + red_sum[G + j] + red_sum[2 * G + j] + red_sum[3 * G + j];
-                };
+                if (st < G) mrg[G + st] = red_sum[st] + red_sum[G + st] + red_sum[2 * G + st] + red_sum[3 * G + st];
+                tc::named_bar_sync(1, SMX);
                 const int ss = kPasses ? kvh : cu.seg, sh_ = kPasses ? hb : 0;
                 const int segg = seg_ordinal(p.B, spp, cu.b, ss, sh_);
-                // the block's final rows go through shared memory (the weights buffer is free once
-                // the piece's last P.V is done) to one compact loop of 16-byte stores
-                auto flush_rows = [&](const float (&v)[GH]) {
-                    float* ostg = reinterpret_cast<float*>(Ps);
-#pragma unroll
-                    for (int jj = 0; jj < GH; ++jj) ostg[(c0 + jj) * D + r] = v[jj];
-                    tc::named_bar_sync(1, SMX);
-#pragma unroll 1
-                    for (int idx = st; idx < QB * (D / 4); idx += SMX) {
-                        const int j = idx / (D / 4), d0 = (idx % (D / 4)) * 4;
-                        const float4 x = *reinterpret_cast<const float4*>(ostg + j * D + d0);
-                        store_out4(p, orow(cu.b, kvh, hb * QB + j) * D + d0, x.x, x.y, x.z, x.w);
-                    }
-                };
-                if (piece_first == 0 && seg_end) {
-#pragma unroll
-                    for (int jj = 0; jj < GH; ++jj) o[jj] /= ltot(jj);
-                    flush_rows(o);
-                } else {
+                constexpr int NV4 = G * D / 4 / SMX;  // 16-byte pieces of O per thread
+                float4* o4 = reinterpret_cast<float4*>(ostg);
+                bool fin = piece_first == 0 && seg_end;  // the piece is its whole segment
+                bool merged = false;
+                if (!fin) {
+                    // the partial: m and l of the rows, then O as rows x D
                     float* slot = p.ws + static_cast<size_t>(segg + wid) * LY::SLOT;
-                    if (r == 0) {
-#pragma unroll
-                        for (int jj = 0; jj < GH; jj += 4) {
-                            *reinterpret_cast<float4*>(slot + c0 + jj) = make_float4(m[jj], m[jj + 1], m[jj + 2], m[jj + 3]);
-                            *reinterpret_cast<float4*>(slot + G + c0 + jj) =
-                                make_float4(ltot(jj), ltot(jj + 1), ltot(jj + 2), ltot(jj + 3));
-                        }
-                        // this piece's maxima, in case it is the one that merges
-#pragma unroll
-                        for (int jj = 0; jj < GH; ++jj) mrg[c0 + jj] = m[jj];
+                    if (st < G) {
+                        slot[st] = mrg[st];
+                        slot[G + st] = mrg[G + st];
                     }
 #pragma unroll
-                    for (int jj = 0; jj < GH; jj += 4)
-                        *reinterpret_cast<float4*>(slot + LY::OOFF + r * G + c0 + jj) =
-                            make_float4(o[jj], o[jj + 1], o[jj + 2], o[jj + 3]);
+                    for (int u = 0; u < NV4; ++u)
+                        reinterpret_cast<float4*>(slot + LY::OOFF)[st + u * SMX] = o4[st + u * SMX];
                     tc::named_bar_sync(1, SMX);
                     if (leader) {
                         const uint32_t prev = arrive_acq_rel(&p.counters[segg], static_cast<uint32_t>(ntl));
                         bcast[0] = (prev + ntl == static_cast<uint32_t>(cu.nt)) ? 1 : 0;
                     }
                     tc::named_bar_sync(1, SMX);
-                    if (bcast[0]) {
-                        // the last piece to arrive merges: its own partial from registers, the
-                        // others two at a time, all loads of a step in flight together; thread
-                        // st < G keeps row st's running max and sum and publishes the step's
-                        // factors, which every thread applies to its rows at dimension r
-                        const int wf = split.worker_at(cu.b, ss, sh_, cu.nt, 0);
-                        const int wl = split.worker_at(cu.b, ss, sh_, cu.nt, cu.nt - 1);
-                        if (st < G) mrg[G + st] = red_sum[st] + red_sum[G + st] + red_sum[2 * G + st] + red_sum[3 * G + st];
-                        tc::named_bar_sync(1, SMX);
-                        int w = wf;
-#pragma unroll 1
-                        for (;;) {
-                            int wa = -1, wb = -1;
-                            for (; w <= wl && wb < 0; ++w) {
-                                if (w == wid || !split.has_piece(w, wf, wl)) continue;
-                                if (wa < 0) wa = w;
-                                else wb = w;
-                            }
-                            if (wa < 0) break;
-                            const bool hasb = wb >= 0;
-                            const float* sa = p.ws + static_cast<size_t>(segg + wa) * LY::SLOT;
-                            const float* sb = p.ws + static_cast<size_t>(segg + (hasb ? wb : wa)) * LY::SLOT;
-                            float oa[GH], ob[GH];
-#pragma unroll
-                            for (int jj = 0; jj < GH; jj += 4) {
-                                const float4 va = __ldcg(reinterpret_cast<const float4*>(sa + LY::OOFF + r * G + c0 + jj));
-                                const float4 vb = __ldcg(reinterpret_cast<const float4*>(sb + LY::OOFF + r * G + c0 + jj));
-                                oa[jj] = va.x;
-                                oa[jj + 1] = va.y;
-                                oa[jj + 2] = va.z;
-                                oa[jj + 3] = va.w;
-                                ob[jj] = vb.x;
-                                ob[jj + 1] = vb.y;
-                                ob[jj + 2] = vb.z;
-                                ob[jj + 3] = vb.w;
-                            }
-                            if (st < G) {
-                                const float ma = __ldcg(sa + st), la = __ldcg(sa + G + st);
-                                const float mb = __ldcg(sb + st), lb = __ldcg(sb + G + st);
-                                const float m0 = mrg[st];
-                                const float mn = fmaxf(m0, hasb ? fmaxf(ma, mb) : ma);  // finite: every m >= kMInit
-                                const float f0 = wide::ex2(m0 - mn), fa = wide::ex2(ma - mn);
-                                const float fb = hasb ? wide::ex2(mb - mn) : 0.f;
-                                mrg[st] = mn;
-                                mrg[G + st] = mrg[G + st] * f0 + la * fa + lb * fb;
-                                mrg[2 * G + st] = f0;
-                                mrg[3 * G + st] = fa;
-                                mrg[4 * G + st] = fb;
-                            }
-                            tc::named_bar_sync(1, SMX);
-#pragma unroll
-                            for (int jj = 0; jj < GH; ++jj) {
-                                const int j = c0 + jj;
-                                o[jj] = o[jj] * mrg[2 * G + j] + oa[jj] * mrg[3 * G + j] + ob[jj] * mrg[4 * G + j];
-                            }
-                            tc::named_bar_sync(1, SMX);
-                        }
-#pragma unroll
-                        for (int jj = 0; jj < GH; ++jj) o[jj] /= mrg[G + c0 + jj];
-                        flush_rows(o);
-                        if (leader) p.counters[segg] = 0u;
-                    }
-                    tc::named_bar_sync(1, SMX);
+                    fin = merged = bcast[0] != 0;
                 }
+                if (merged) {
+                    // the last piece to arrive merges the others into its O in shared memory,
+                    // two at a time with all their loads in flight; thread st < G keeps row
+                    // st's running max and sum and publishes the step's factors
+                    const int wf = split.worker_at(cu.b, ss, sh_, cu.nt, 0);
+                    const int wl = split.worker_at(cu.b, ss, sh_, cu.nt, cu.nt - 1);
+                    int w = wf;
+#pragma unroll 1
+                    for (;;) {
+                        int wa = -1, wb = -1;
+                        for (; w <= wl && wb < 0; ++w) {
+                            if (w == wid || !split.has_piece(w, wf, wl)) continue;
+                            if (wa < 0) wa = w;
+                            else wb = w;
+                        }
+                        if (wa < 0) break;
+                        const bool hasb = wb >= 0;
+                        const float* sa = p.ws + static_cast<size_t>(segg + wa) * LY::SLOT;
+                        const float* sb = p.ws + static_cast<size_t>(segg + (hasb ? wb : wa)) * LY::SLOT;
+                        float4 va[NV4], vb[NV4];
+#pragma unroll
+                        for (int u = 0; u < NV4; ++u) {
+                            va[u] = __ldcg(reinterpret_cast<const float4*>(sa + LY::OOFF) + st + u * SMX);
+                            vb[u] = hasb ? __ldcg(reinterpret_cast<const float4*>(sb + LY::OOFF) + st + u * SMX)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                        if (st < G) {
+                            const float ma = __ldcg(sa + st), la = __ldcg(sa + G + st);
+                            const float mb = __ldcg(sb + st), lb = __ldcg(sb + G + st);
+                            const float m0 = mrg[st];
+                            const float mn = fmaxf(m0, hasb ? fmaxf(ma, mb) : ma);  // finite: every m >= kMInit
+                            const float f0 = wide::ex2(m0 - mn), fa = wide::ex2(ma - mn);
+                            const float fb = hasb ? wide::ex2(mb - mn) : 0.f;
+                            mrg[st] = mn;
+                            mrg[G + st] = mrg[G + st] * f0 + la * fa + lb * fb;
+                            mrg[2 * G + st] = f0;
+                            mrg[3 * G + st] = fa;
+                            mrg[4 * G + st] = fb;
+                        }
+                        tc::named_bar_sync(1, SMX);
+#pragma unroll
+                        for (int u = 0; u < NV4; ++u) {
+                            const int idx = st + u * SMX, j = idx / (D / 4);
+                            const float f0 = mrg[2 * G + j], fa = mrg[3 * G + j], fb = mrg[4 * G + j];
+                            float4 x = o4[idx];
+                            x.x = x.x * f0 + va[u].x * fa + vb[u].x * fb;
+                            x.y = x.y * f0 + va[u].y * fa + vb[u].y * fb;
+                            x.z = x.z * f0 + va[u].z * fa + vb[u].z * fb;
+                            x.w = x.w * f0 + va[u].w * fa + vb[u].w * fb;
+                            o4[idx] = x;
+                        }
+                        tc::named_bar_sync(1, SMX);
+                    }
+                }
+                if (fin) {
+                    // the block's rows: O / l, one 16-byte store per 4 dimensions
+#pragma unroll 1
+                    for (int idx = st; idx < QB * (D / 4); idx += SMX) {
+                        const int j = idx / (D / 4), d0 = (idx % (D / 4)) * 4;
+                        const float lj = mrg[G + j];
+                        const float4 x = o4[idx];
+                        store_out4(p, orow(cu.b, kvh, hb * QB + j) * D + d0, x.x / lj, x.y / lj, x.z / lj, x.w / lj);
+                    }
+                    if (merged && leader) p.counters[segg] = 0u;
+                }
+                // the staging buffer and the row state are free for the next piece
+                tc::named_bar_sync(1, SMX);
                 cu = nx;
             }
         }
