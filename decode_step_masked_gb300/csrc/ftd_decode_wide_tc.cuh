@@ -350,6 +350,8 @@ static __device__ __noinline__ bool stage_q_fn(const DecodeParams& p, const Curs
         using T = decltype(tag);
         QRaw<T, G> x;
         fetch_q<T, G, MQ>(p, c, st, x);
+        // the first piece's q loads go out before the producer's first copies (named barrier 3)
+        if (check) asm volatile("bar.arrive 3, %0;" ::"r"(wide::kThreads - 32) : "memory");
         if (check) changed = lengths_changed(p, Ls, threadIdx.x & 31);
         if (!changed) put_q<CT, T, G>(Qs, x, p, st);
     });
@@ -513,6 +515,8 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
         if (!changed) publish_q();
     } else {
         changed = lengths_changed(p, Ls, lane);
+        // the producer issues its first copies once the softmax warps' q loads are out
+        if (warp == 0 && n_my > 0) tc::named_bar_sync(3, wide::kThreads - 32);
     }
     if (changed) {
         // (rare) the lengths changed after this block read them: re-plan, as in the narrow kernel
