@@ -422,7 +422,10 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     if (threadIdx.x == 0) *rv = 0;
     // The split depends only on the lengths, so it is computed before waiting on
     // the previous launch: a block that starts while the previous step drains
-    // then warms L2 with its first tiles (contiguous caches) instead of idling.
+    // then warms L2 with its first tiles (contiguous caches) instead of idling:
+    // each warp's first tile, or, for INT8 caches, as many tiles as it has stages
+    // (measured after a GEMM and back to back: deeper prefetches of the fp16/bf16
+    // tiles queue ahead of the first demand copies and lengthen the step's start).
     // After the wait the lengths are checked again (lengths_changed).  Everything
     // that reads the caches' contents or writes memory comes after the wait.
     bool ovf = false;
@@ -437,7 +440,8 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
     int n_my = split.begin(wid + 1) - t_begin;
     if (n_my > 0 && lane == 0 && !p.block_table) {
         Cursor c = locate(t_begin, P, p.B, segs);
-        for (int k = 0; k < min(SPW, n_my); ++k) {
+        constexpr int NPF = I8 ? SPW : 1;  // tiles prefetched per warp
+        for (int k = 0; k < min(NPF, n_my); ++k) {
             const int L = Ls[c.b];
             const int t0 = (window_start(L, p.window) / T + c.tile) * T;
             const int n_cache = min(T, max(0, L - t0));
@@ -446,7 +450,7 @@ __global__ void __launch_bounds__(Tiling<CT, D, G>::WARPS * 32, 1) decode_splitk
                 bulk_prefetch_l2(p.k_cache + rb * ROW, static_cast<uint32_t>(n_cache) * ROW);
                 bulk_prefetch_l2(p.v_cache + rb * ROW, static_cast<uint32_t>(n_cache) * ROW);
             }
-            if (k + 1 < min(SPW, n_my)) advance(c, P, segs);
+            if (k + 1 < min(NPF, n_my)) advance(c, P, segs);
         }
     }
     grid_dep_wait();    // inputs, caches and outputs may be in use by the previous launch
