@@ -500,15 +500,16 @@ __global__ void __launch_bounds__(tc::threads_for(G, std::is_same_v<CT, int8_t>)
 
     // The split depends only on the lengths, so it runs before the wait on the
     // previous launch, and a block that starts while the previous step drains
-    // warms L2 with its first tiles (contiguous caches).  After the wait the
-    // lengths are checked again (lengths_changed).  Reads of the caches and
-    // writes of shared outputs come after the wait.
+    // warms L2 with its first tiles (contiguous fp16 / bf16 caches; the INT8
+    // variant measured faster without it, back to back and after a GEMM).  After
+    // the wait the lengths are checked again (lengths_changed).  Reads of the
+    // caches and writes of shared outputs come after the wait.
     const long long W = gridDim.x;
     const int wid = blockIdx.x;
     const PassSplit<LY::ALPHA> split{P, VP, p.B, spp, np, static_cast<int>(W)};
     int t_begin = split.begin(wid);
     int n_my = split.begin(wid + 1) - t_begin;
-    if (n_my > 0 && tid == 0 && !p.block_table) {
+    if (!I8 && n_my > 0 && tid == 0 && !p.block_table) {
         Cursor c = locate_pass(t_begin, P, p.B, spp, np);
         for (int k = 0; k < min(NS, n_my); ++k) {
             const int L = Ls[c.b];
