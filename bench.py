@@ -54,7 +54,7 @@ KERNEL_SOURCES = ("decode_step_masked_gb300/csrc/ftd_common.cuh",
 OPTION_CASES = [("13b", dict(out_dtype="bf16")), ("13b", dict(window=1024)), ("13b", dict(page_size=256)),
                 ("70b", dict(out_dtype="bf16")), ("70b", dict(window=1024)), ("70b", dict(page_size=256)),
                 ("int8", dict(page_size=256)), ("7b", dict(q_len=4)), ("7b", dict(q_len=8)),
-                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)),
+                ("70b", dict(q_len=2)), ("70b", dict(q_len=4)), ("70b", dict(ragged=1)),
                 ("7b", dict(proj_dim=4096)), ("13b", dict(proj_dim=5120)), ("70b", dict(proj_dim=8192))]
 
 
@@ -517,15 +517,18 @@ def reference_arm(args):
 
 
 def measure_config(name, steps, warmup, seed, device, stream, out_dtype="f32", window=0, page_size=0, q_len=1,
-                   flush=None, isolated=0, proj_dim=0):
+                   flush=None, isolated=0, proj_dim=0, ragged=0):
     """Time one workload; the options select a half-precision output, a sliding
-    window, a paged cache (one shuffled block table shared by the rotated pools)
-    or several new tokens per slot (the cached lengths drop by q_len - 1 so the
-    step's last position stays where the plain workload's is).  With flush and
+    window, a paged cache (one shuffled block table shared by the rotated pools),
+    several new tokens per slot (the cached lengths drop by q_len - 1 so the
+    step's last position stays where the plain workload's is) or ragged contexts
+    (uniform in 128 .. Lmax, the continuous-batch length mix).  With flush and
     isolated > 0, also time that many isolated steps (run_isolated)."""
     import torch
     import decode_step_masked_gb300 as ftd
     w = WORKLOADS[name]
+    if ragged:
+        w = w.with_(lens=("ctx_uniform", 128, w.Lmax))
     lens = gen_seq_lens(w) - (q_len - 1)
     by = step_bytes(w, lens, window, out_dtype, q_len, proj_dim)
     # rotation is sized on the bytes a step reads (the visible rows), so each pool leaves L2 between reads
