@@ -79,7 +79,11 @@ struct Layout {
     static constexpr int PREFIX_BYTES = ((HAVE_VP ? 3 : 2) * kMaxBatch + 2) * 4;
     static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;
     // two S buffers (columns 0 and G) and O (column 2G)
-    static constexpr int TMEM_COLS = 3 * G <= 128 ? 128 : 256;
+    // 32-row blocks: one P.V MMA per 16 key rows takes the hi and lo weights together (N = 2G)
+    // into two O halves (columns 2G and 3G, summed when O is read), so each V operand is read
+    // from shared memory once and a V slot is free sooner
+    static constexpr bool PVC = G == 32;
+    static constexpr int TMEM_COLS = (PVC ? 4 : 3) * G <= 128 ? 128 : 256;
     // split-K partial of a piece: m and l of the G rows, then O as G rows of D floats
     static constexpr int OOFF = round_up(2 * G, 4);
     static constexpr int SLOT = OOFF + G * tc::D;
@@ -619,7 +623,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
             // that makes no progress for the pipeline limit aborts as the other roles' waits do.
             Cursor cu = locate_pass(t_begin, P, p.B, spp, np);  // the tile of the next score MMA
             const uint32_t id_s = tc::instr_desc(BF, TM, G, false);
-            const uint32_t id_o = tc::instr_desc(BF, D, G, true, true);
+            const uint32_t id_o = tc::instr_desc(BF, D, LY::PVC ? 2 * G : G, true, true);
             const uint64_t dk0 = tc::smem_desc_sw128(smem_addr(stages), 16, 1024);
             const uint64_t dv0 = tc::smem_desc_sw128(smem_addr(stages) + LY::OFF_V, tc::kVLbo, tc::kVSbo);
             constexpr int NSV = LY::NSV;
@@ -707,7 +711,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                                     const uint64_t a = va + (kq * 2048 >> 4);
                                     const uint64_t bh = dp0 + (kq * 2048 >> 4);  // key rows 16 kq .. of the hi weights
                                     tc::mma_f16(tmem + 2 * G, a, bh, id_o, !first || kq > 0);
-                                    tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
+                                    if constexpr (!LY::PVC) tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
                                 }
                                 tc::mma_commit(bar(kOFull));
                                 tc::mma_commit(bar(kEmptyV + kp % NSV));
@@ -952,11 +956,15 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                             put_p8(j8, pq + j8);
                             if (chained) {
                                 // rescale this piece's O (these rows' columns, dimension r)
-                                float o8[8];
-                                wide::tmem_ld_rows<8>(tmem + lane_base + 2 * G + c0 + j8, o8);
 #pragma unroll
-                                for (int i8 = 0; i8 < 8; ++i8) o8[i8] *= alpha[i8];
-                                wide::tmem_st8(tmem + lane_base + 2 * G + c0 + j8, o8);
+                                for (int h = 0; h < (LY::PVC ? 2 : 1); ++h) {  // both O halves
+                                    float o8[8];
+                                    const uint32_t oc = tmem + lane_base + (2 + h) * G + c0 + j8;
+                                    wide::tmem_ld_rows<8>(oc, o8);
+#pragma unroll
+                                    for (int i8 = 0; i8 < 8; ++i8) o8[i8] *= alpha[i8];
+                                    wide::tmem_st8(oc, o8);
+                                }
                             }
                         }
                         if (chained) wide::tmem_st_wait();
@@ -986,6 +994,12 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                 {
                     float o[GH];
                     ld_rows(2 * G, o);
+                    if constexpr (LY::PVC) {
+                        float o2[GH];
+                        ld_rows(3 * G, o2);
+#pragma unroll
+                        for (int jj = 0; jj < GH; ++jj) o[jj] += o2[jj];
+                    }
                     tc::tc_fence_before();
 #pragma unroll
                     for (int jj = 0; jj < GH; ++jj) ostg[(c0 + jj) * D + r] = o[jj];
