@@ -79,10 +79,11 @@ struct Layout {
     static constexpr int PREFIX_BYTES = ((HAVE_VP ? 3 : 2) * kMaxBatch + 2) * 4;
     static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;
     // two S buffers (columns 0 and G) and O (column 2G)
-    // 32-row blocks: one P.V MMA per 16 key rows takes the hi and lo weights together (N = 2G)
-    // into two O halves (columns 2G and 3G, summed when O is read), so each V operand is read
-    // from shared memory once and a V slot is free sooner
-    static constexpr bool PVC = G == 32;
+    // One P.V MMA per 16 key rows takes the hi and lo weights together (N = 2G) into two O
+    // halves (columns 2G and 3G, summed when O is read), so each V operand is read from shared
+    // memory once and a V slot is free sooner (70B-shaped step with 4 new tokens 117.2 -> 104.5
+    // us, multi-query step 47.5 -> 45.8 us)
+    static constexpr bool PVC = true;
     static constexpr int TMEM_COLS = (PVC ? 4 : 3) * G <= 128 ? 128 : 256;
     // split-K partial of a piece: m and l of the G rows, then O as G rows of D floats
     static constexpr int OOFF = round_up(2 * G, 4);
@@ -756,7 +757,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                             const uint64_t a = va + (ks * 2048 >> 4);
                             const uint64_t bh = dp0 + (ks * 2048 >> 4);  // key rows 16 ks .. of the hi weights
                             tc::mma_f16(tmem + 2 * G, a, bh, id_o, !first || ks > 0);
-                            tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
+                            if constexpr (!LY::PVC) tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
                         }
                         tc::mma_commit(bar(kOFull));
                         tc::mma_commit(bar(kEmptyV + kk % NSV));
@@ -837,7 +838,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                 if constexpr (MQ) return q_row(p, b, kvh, qi);
                 return static_cast<size_t>(b) * p.Hq + kvh * p.group + qi;
             };
-            // the owned rows' TMEM columns from column col: S buffer (k & 1) * G, O at 2G
+            // the owned rows' TMEM columns from column col: S buffer (k & 1) * G, O at 2G (and 3G)
             auto ld_rows = [&](uint32_t col, float (&v)[GH]) { wide::tmem_ld_rows<GH>(tmem + lane_base + col + c0, v); };
             // weights of owned rows jj0 .. jj0 + 7 for key row r: hi at column c0 + jj0, lo at G + c0 + jj0
             auto put_p8 = [&](int jj0, const float* pv) {
