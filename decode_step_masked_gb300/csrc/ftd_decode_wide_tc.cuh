@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                             if (lane == 0) {
                                 tc::tc_fence_after();
                                 const uint64_t ka = dk0 + static_cast<uint32_t>(s * (2 * KB >> 4));
-    #pragma unroll
+#pragma unroll
                                 for (int kq = 0; kq < D / 16; ++kq) {
                                     const uint64_t a = ka + (((kq >> 2) * KB + (kq & 3) * 32) >> 4);
                                     const uint64_t bh = dq0 + (((kq >> 2) * (2 * G * 128) + (kq & 3) * 32) >> 4);
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                             if (lane == 0) {
                                 tc::tc_fence_after();
                                 const uint64_t va = dv0 + static_cast<uint32_t>((kp % NSV) * (2 * KB >> 4));
-    #pragma unroll
+#pragma unroll
                                 for (int kq = 0; kq < TM / 16; ++kq) {
                                     const uint64_t a = va + (kq * 2048 >> 4);
                                     const uint64_t bh = dp0 + (kq * 2048 >> 4);  // key rows 16 kq .. of the hi weights
@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                     if (lane == 0) {
                         tc::tc_fence_after();
                         const uint64_t va = dv0 + static_cast<uint32_t>((kk % NSV) * (2 * KB >> 4));
-    #pragma unroll
+#pragma unroll
                         for (int ks = 0; ks < TM / 16; ++ks) {
                             const uint64_t a = va + (ks * 2048 >> 4);
                             const uint64_t bh = dp0 + (ks * 2048 >> 4);  // key rows 16 ks .. of the hi weights
@@ -804,7 +804,7 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
                     if (lane == 0) {
                         tc::tc_fence_after();
                         const uint64_t ka = dk0 + static_cast<uint32_t>(s * (2 * KB >> 4));
-    #pragma unroll
+#pragma unroll
                         for (int ks = 0; ks < D / 16; ++ks) {
                             const uint64_t a = ka + (((ks >> 2) * KB + (ks & 3) * 32) >> 4);
                             const uint64_t bh = dq0 + (((ks >> 2) * (2 * G * 128) + (ks & 3) * 32) >> 4);
