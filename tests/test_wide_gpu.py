@@ -79,6 +79,16 @@ def test_wide_multi_token(Hq, Hkv, T):
     check(w, inp, what=f"wide multi-token {Hq}/{Hkv} T{T}")
 
 
+@pytest.mark.parametrize("Hq,T", [(32, 1), (64, 1), (8, 4)])
+def test_wide_many_short_segments(Hq, T):
+    """200 slots with contexts up to 1000 tokens, some inactive: about five tiles per block,
+    so blocks cross several pieces, and most segments end in a merge of partials."""
+    rng = np.random.default_rng(91)
+    lens = rng.integers(-1, 1000, size=200)
+    w, inp = case("bf16", B=200, Hq=Hq, Hkv=1, Lmax=1024, lens=lens, T=T, seed=92)
+    check(w, inp, what=f"wide short segments Hq{Hq} T{T}")
+
+
 @pytest.mark.parametrize("rise", [20.0, 60.0])
 @pytest.mark.parametrize("Hq,Hkv,T", [(64, 1, 1), (32, 1, 1), (8, 1, 4), (16, 1, 4)])
 def test_wide_rising_scores(Hq, Hkv, T, rise):
@@ -101,12 +111,13 @@ def test_wide_half_output(out_dtype):
     check(w, inp, out_dtype=out_dtype, what=f"wide out {out_dtype}")
 
 
-@pytest.mark.parametrize("T,window", [(1, 0), (4, 0), (4, 200)])
-def test_wide_paged(T, window):
-    """Pages of 128 tokens in shuffled order, new tokens across a page boundary, a window."""
+@pytest.mark.parametrize("rows,T,window", [(64, 1, 0), (64, 4, 0), (64, 4, 200), (32, 1, 0), (32, 4, 200)])
+def test_wide_paged(rows, T, window):
+    """Pages of 128 tokens in shuffled order, new tokens across a page boundary, a window;
+    blocks of 64 and of 32 query rows."""
     import torch
     ps = 128
-    w, inp = case("bf16", B=3, Hq=64 // T, Hkv=1, Lmax=1024, lens=[126, 0, 900], T=T, seed=75)
+    w, inp = case("bf16", B=3, Hq=rows // T, Hkv=1, Lmax=1024, lens=[126, 0, 900], T=T, seed=75)
     table, num_pages, spare = page_layout(w, inp["seq_lens"], ps, spare=2, seed=12, q_len=T)
     ref = oracle.load().decode_step(w, inp, nthreads=8, window=window)
     nan = np.uint16(0x7FC0)
