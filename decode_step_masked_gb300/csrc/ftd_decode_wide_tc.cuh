@@ -78,8 +78,8 @@ struct Layout {
     static constexpr int ALPHA = HAVE_VP ? (G == 64 ? 4 : 1) : 0;
     static constexpr int PREFIX_BYTES = ((HAVE_VP ? 3 : 2) * kMaxBatch + 2) * 4;
     static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;
-    // two S buffers (columns 0 and G) and O (column 2G)
-    // One P.V MMA per 16 key rows takes the hi and lo weights together (N = 2G) into two O
+    // TMEM: two S buffers (columns 0 and G), then O.  One P.V MMA per 16 key rows takes the hi
+    // and lo weights together (N = 2G) into two O
     // halves (columns 2G and 3G, summed when O is read), so each V operand is read from shared
     // memory once and a V slot is free sooner (70B-shaped step with 4 new tokens 117.2 -> 104.5
     // us, multi-query step 47.5 -> 45.8 us)
@@ -613,15 +613,15 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
             }
         } else if (warp == 1) {
             // ------------------------------------------- append + MMA issue
-            // 32-row blocks: the score MMAs and the P.V MMAs are two streams, each in tile order,
-            // issued as their inputs become ready rather than alternately (the 70B-shaped step
-            // with 4 new tokens: 123.7 -> 117.1 us): the score MMA of tile k needs
-            // its K tile, the piece's q (on a piece's first tile) and S buffer k & 1 free (the
-            // softmax is done with tile k - 2); the P.V of tile j needs its weights and its V
-            // tile, and on a piece's first tile the previous piece's O read.  So a late V copy
-            // no longer holds back the next score MMA, and with it the K ring.  The warp tests
-            // the barriers (test_wait, no blocking) and issues whichever stream is ready; a loop
-            // that makes no progress for the pipeline limit aborts as the other roles' waits do.
+            // The score MMAs and the P.V MMAs are two streams, each in tile order, issued as
+            // their inputs become ready rather than alternately (the 70B-shaped step with 4 new
+            // tokens: 123.7 -> 117.1 us).  The score MMA of tile k needs its K tile, the piece's
+            // q (on a piece's first tile) and S buffer k & 1 free (the softmax is done with tile
+            // k - 2); the P.V of tile j needs its weights and its V tile, and on a piece's first
+            // tile the previous piece's O read.  So a late V copy no longer holds back the next
+            // score MMA, and with it the K ring.  The warp tests the barriers (test_wait, no
+            // blocking) and issues whichever stream is ready; a loop that makes no progress for
+            // the pipeline limit aborts as the other roles' waits do.
             Cursor cu = locate_pass(t_begin, P, p.B, spp, np);  // the tile of the next score MMA
             const uint32_t id_s = tc::instr_desc(BF, TM, G, false);
             const uint32_t id_o = tc::instr_desc(BF, D, LY::PVC ? 2 * G : G, true, true);
@@ -631,194 +631,135 @@ __global__ void __launch_bounds__(wide::kThreads, 1)
             const uint64_t dq0 = tc::smem_desc_sw128(smem_addr(Qs), 16, 1024);
             // the weights, MN-major: 64-column atoms of 128 key rows (16 KB apart), 8-row groups 1 KB apart
             const uint64_t dp0 = tc::smem_desc_sw128(smem_addr(Ps), KB, 1024);
-            if constexpr (G == 32) {
-                int qcount = 0, opieces = 0;
-                int ks = 0, kp = 0;   // next score MMA, next P.V
-                uint32_t firsts = 0;  // bit k % 32: the P.V of tile k is the first of its piece
-                long long idle0 = clock64();
-                while (kp < n_my) {
-                    bool did = false;
-                    if (ks < n_my) {
-                        const bool new_piece = (ks == 0) || (cu.tile == 0);
-                        bool has_new = cu.tile == cu.nt - 1;
-                        if constexpr (MQ)
-                            has_new = Ls[cu.b] < (window_start(Ls[cu.b], p.window) / TM + cu.tile + 1) * TM;
-                        const bool patch_v = has_new || (cu.tile == 0 && p.window > 0);  // the V tile is written here
-                        const int s = ks % NS;
-                        // every lane tests (and so acquires) the barriers: the warp writes the
-                        // appended rows into the landed tiles
-                        bool r = wide::mbar_test(bar(kFullK + s), (ks / NS) & 1);
-                        if (r && patch_v) r = wide::mbar_test(bar(kFullV + ks % NSV), (ks / NSV) & 1);
-                        if (r && new_piece) r = wide::mbar_test(bar(kQReady), qcount & 1);
-                        if (r && ks >= 2) r = wide::mbar_test(bar(kSFree + (ks & 1)), ((ks >> 1) - 1) & 1);
-                        if (__all_sync(FULL, r)) {
+            int qcount = 0, opieces = 0;
+            int ks = 0, kp = 0;   // next score MMA, next P.V
+            uint32_t firsts = 0;  // bit k % 32: the P.V of tile k is the first of its piece
+            long long idle0 = clock64();
+            while (kp < n_my) {
+                bool did = false;
+                // 64-row blocks give the P.V MMAs the first turn, 32-row blocks the score MMAs
+                // (multi-query step 45.8 -> 44.6 us; the 70B-shaped step with 4 new tokens kept
+                // the score MMAs first: 117.1 against 118.4 us)
+                if (G == 64 && kp < ks) {
+                    // P.V of tile kp: into O, accumulating after the piece's first tile
+                    const bool first = (firsts >> (kp & 31)) & 1u;
+                    bool r = wide::mbar_test(bar(kPFull), kp & 1);
+                    if (r) r = wide::mbar_test(bar(kFullV + kp % NSV), (kp / NSV) & 1);
+                    if (r && first && opieces > 0) r = wide::mbar_test(bar(kOFree), (opieces - 1) & 1);
+                    if (__all_sync(FULL, r)) {
+                        if (first) ++opieces;
+                        if (lane == 0) {
                             tc::tc_fence_after();
-                            if (cu.tile == 0 && p.window > 0) {
-                                // rows of the first tile before the window start get weight 0; zero
-                                // their staged V so stale or non-finite history cannot reach O
-                                const int nlo = window_start(Ls[cu.b], p.window) % TM;
-                                unsigned char* vst = stages + LY::OFF_V + (ks % NSV) * 2 * KB;
-                                for (int c = lane; c < 2 * nlo * 8; c += 32) {
-                                    const int box = c / (nlo * 8), rem = c - box * nlo * 8;
-                                    *reinterpret_cast<uint4*>(vst + box * KB + (rem >> 3) * 128 + (rem & 7) * 16) =
-                                        make_uint4(0u, 0u, 0u, 0u);
-                                }
-                                if (nlo > 0) fence_proxy_async_smem();
-                                __syncwarp();
-                            }
-                            if (has_new) {
-                                wide::append_rows<CT>(p, stages + s * 2 * KB, stages + LY::OFF_V + (ks % NSV) * 2 * KB, cu.b,
-                                                      cu.seg, cu.tile, Ls[cu.b], lane);
-                                fence_proxy_async_smem();
-                                __syncwarp();
-                            }
-                            if (lane == 0) {
-                                tc::tc_fence_after();
-                                const uint64_t ka = dk0 + static_cast<uint32_t>(s * (2 * KB >> 4));
+                            const uint64_t va = dv0 + static_cast<uint32_t>((kp % NSV) * (2 * KB >> 4));
 #pragma unroll
-                                for (int kq = 0; kq < D / 16; ++kq) {
-                                    const uint64_t a = ka + (((kq >> 2) * KB + (kq & 3) * 32) >> 4);
-                                    const uint64_t bh = dq0 + (((kq >> 2) * (2 * G * 128) + (kq & 3) * 32) >> 4);
-                                    tc::mma_f16(tmem + (ks & 1) * G, a, bh, id_s, kq > 0);
-                                    tc::mma_f16(tmem + (ks & 1) * G, a, bh + (G * 128 >> 4), id_s, true);  // the lo rows
-                                }
-                                tc::mma_commit(bar(kSFull + (ks & 1)));
-                                tc::mma_commit(bar(kEmptyK + s));  // the K tile is read
+                            for (int kq = 0; kq < TM / 16; ++kq) {
+                                const uint64_t a = va + (kq * 2048 >> 4);
+                                const uint64_t bh = dp0 + (kq * 2048 >> 4);  // key rows 16 kq .. (hi, then lo at column G)
+                                tc::mma_f16(tmem + 2 * G, a, bh, id_o, !first || kq > 0);
+                                if constexpr (!LY::PVC) tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
                             }
-                            __syncwarp();
-                            if (new_piece) {
-                                ++qcount;
-                                firsts |= 1u << (ks & 31);
-                            } else {
-                                firsts &= ~(1u << (ks & 31));
-                            }
-                            if (++ks < n_my) advance_pass(cu, P, p.B, spp, np);
-                            did = true;
+                            tc::mma_commit(bar(kOFull));
+                            tc::mma_commit(bar(kEmptyV + kp % NSV));
                         }
-                    }
-                    if (kp < ks) {
-                        // P.V of tile kp: into O, accumulating after the piece's first tile
-                        const bool first = (firsts >> (kp & 31)) & 1u;
-                        bool r = wide::mbar_test(bar(kPFull), kp & 1);
-                        if (r) r = wide::mbar_test(bar(kFullV + kp % NSV), (kp / NSV) & 1);
-                        if (r && first && opieces > 0) r = wide::mbar_test(bar(kOFree), (opieces - 1) & 1);
-                        if (__all_sync(FULL, r)) {
-                            if (first) ++opieces;
-                            if (lane == 0) {
-                                tc::tc_fence_after();
-                                const uint64_t va = dv0 + static_cast<uint32_t>((kp % NSV) * (2 * KB >> 4));
-#pragma unroll
-                                for (int kq = 0; kq < TM / 16; ++kq) {
-                                    const uint64_t a = va + (kq * 2048 >> 4);
-                                    const uint64_t bh = dp0 + (kq * 2048 >> 4);  // key rows 16 kq .. of the hi weights
-                                    tc::mma_f16(tmem + 2 * G, a, bh, id_o, !first || kq > 0);
-                                    if constexpr (!LY::PVC) tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
-                                }
-                                tc::mma_commit(bar(kOFull));
-                                tc::mma_commit(bar(kEmptyV + kp % NSV));
-                            }
-                            __syncwarp();
-                            ++kp;
-                            did = true;
-                        }
-                    }
-                    if (did) {
-                        idle0 = clock64();
-                    } else {
-                        if (*abort_flag) break;
-                        if (clock64() - idle0 > p.wait_cycles) {
-                            if (lane == 0) atomicOr(p.err, kErrTimeout);
-                            *abort_flag = 1;
-                            break;
-                        }
+                        __syncwarp();
+                        ++kp;
+                        did = true;
                     }
                 }
-            } else {
-                // 64-row blocks: the score MMA of tile k, then the P.V of tile k - 1, in turn (measured
-                // faster for them than the two streams: 47.3 against 49.2 us on the multi-query step)
-                int qcount = 0, opieces = 0;
-                bool ok = true;
-                bool pv_first[2] = {true, true};  // whether the P.V of tile k is the first of its piece
-                // P.V of tile kk: into O, accumulating after the piece's first tile; the first
-                // P.V of a piece waits until the softmax has read the previous piece's O
-                auto issue_pv = [&](int kk) -> bool {
-                    bool w = tc::wait_or_abort(bar(kPFull), kk & 1, p.err, abort_flag, p.wait_cycles);
-                    w = w && tc::wait_or_abort(bar(kFullV + kk % NSV), (kk / NSV) & 1, p.err, abort_flag, p.wait_cycles);
-                    const bool first = pv_first[kk & 1];
-                    if (first && opieces > 0)
-                        w = w && tc::wait_or_abort(bar(kOFree), (opieces - 1) & 1, p.err, abort_flag, p.wait_cycles);
-                    if (__any_sync(FULL, !w)) return false;
-                    if (first) ++opieces;
-                    if (lane == 0) {
-                        tc::tc_fence_after();
-                        const uint64_t va = dv0 + static_cast<uint32_t>((kk % NSV) * (2 * KB >> 4));
-#pragma unroll
-                        for (int ks = 0; ks < TM / 16; ++ks) {
-                            const uint64_t a = va + (ks * 2048 >> 4);
-                            const uint64_t bh = dp0 + (ks * 2048 >> 4);  // key rows 16 ks .. of the hi weights
-                            tc::mma_f16(tmem + 2 * G, a, bh, id_o, !first || ks > 0);
-                            if constexpr (!LY::PVC) tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
-                        }
-                        tc::mma_commit(bar(kOFull));
-                        tc::mma_commit(bar(kEmptyV + kk % NSV));
-                    }
-                    __syncwarp();
-                    return true;
-                };
-                for (int k = 0; k < n_my; ++k) {
-                    const int s = k % NS;
-                    const bool new_piece = (k == 0) || (cu.tile == 0);
-                    if (k > 0 && new_piece && !issue_pv(k - 1)) { ok = false; break; }
-                    pv_first[k & 1] = new_piece;
+                if (ks < n_my) {
+                    const bool new_piece = (ks == 0) || (cu.tile == 0);
                     bool has_new = cu.tile == cu.nt - 1;
                     if constexpr (MQ)
                         has_new = Ls[cu.b] < (window_start(Ls[cu.b], p.window) / TM + cu.tile + 1) * TM;
-                    const bool patch_v = has_new || (cu.tile == 0 && p.window > 0);  // the V half is written here
-                    bool wf = tc::wait_or_abort(bar(kFullK + s), (k / NS) & 1, p.err, abort_flag, p.wait_cycles);
-                    if (patch_v) wf = wf && tc::wait_or_abort(bar(kFullV + k % NSV), (k / NSV) & 1, p.err, abort_flag, p.wait_cycles);
-                    if (__any_sync(FULL, !wf)) { ok = false; break; }
-                    if (cu.tile == 0 && p.window > 0) {
-                        // rows of the first tile before the window start get weight 0; zero
-                        // their staged V so stale or non-finite history cannot reach O
-                        const int nlo = window_start(Ls[cu.b], p.window) % TM;
-                        unsigned char* vst = stages + LY::OFF_V + (k % NSV) * 2 * KB;
-                        for (int c = lane; c < 2 * nlo * 8; c += 32) {
-                            const int box = c / (nlo * 8), rem = c - box * nlo * 8;
-                            *reinterpret_cast<uint4*>(vst + box * KB + (rem >> 3) * 128 + (rem & 7) * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        if (nlo > 0) fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    if (has_new) {
-                        wide::append_rows<CT>(p, stages + s * 2 * KB, stages + LY::OFF_V + (k % NSV) * 2 * KB, cu.b, cu.seg,
-                                              cu.tile, Ls[cu.b], lane);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                    }
-                    if (new_piece) {
-                        const bool wq = tc::wait_or_abort(bar(kQReady), qcount & 1, p.err, abort_flag, p.wait_cycles);
-                        if (__any_sync(FULL, !wq)) { ok = false; break; }
-                        ++qcount;
-                    }
-                    if (lane == 0) {
+                    const bool patch_v = has_new || (cu.tile == 0 && p.window > 0);  // the V tile is written here
+                    const int s = ks % NS;
+                    // every lane tests (and so acquires) the barriers: the warp writes the
+                    // appended rows into the landed tiles
+                    bool r = wide::mbar_test(bar(kFullK + s), (ks / NS) & 1);
+                    if (r && patch_v) r = wide::mbar_test(bar(kFullV + ks % NSV), (ks / NSV) & 1);
+                    if (r && new_piece) r = wide::mbar_test(bar(kQReady), qcount & 1);
+                    if (r && ks >= 2) r = wide::mbar_test(bar(kSFree + (ks & 1)), ((ks >> 1) - 1) & 1);
+                    if (__all_sync(FULL, r)) {
                         tc::tc_fence_after();
-                        const uint64_t ka = dk0 + static_cast<uint32_t>(s * (2 * KB >> 4));
-#pragma unroll
-                        for (int ks = 0; ks < D / 16; ++ks) {
-                            const uint64_t a = ka + (((ks >> 2) * KB + (ks & 3) * 32) >> 4);
-                            const uint64_t bh = dq0 + (((ks >> 2) * (2 * G * 128) + (ks & 3) * 32) >> 4);
-                            tc::mma_f16(tmem + (k & 1) * G, a, bh, id_s, ks > 0);
-                            tc::mma_f16(tmem + (k & 1) * G, a, bh + (G * 128 >> 4), id_s, true);  // the lo rows
+                        if (cu.tile == 0 && p.window > 0) {
+                            // rows of the first tile before the window start get weight 0; zero
+                            // their staged V so stale or non-finite history cannot reach O
+                            const int nlo = window_start(Ls[cu.b], p.window) % TM;
+                            unsigned char* vst = stages + LY::OFF_V + (ks % NSV) * 2 * KB;
+                            for (int c = lane; c < 2 * nlo * 8; c += 32) {
+                                const int box = c / (nlo * 8), rem = c - box * nlo * 8;
+                                *reinterpret_cast<uint4*>(vst + box * KB + (rem >> 3) * 128 + (rem & 7) * 16) =
+                                    make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            if (nlo > 0) fence_proxy_async_smem();
+                            __syncwarp();
                         }
-                        tc::mma_commit(bar(kSFull + (k & 1)));
-                        tc::mma_commit(bar(kEmptyK + s));  // the K half is read
+                        if (has_new) {
+                            wide::append_rows<CT>(p, stages + s * 2 * KB, stages + LY::OFF_V + (ks % NSV) * 2 * KB, cu.b,
+                                                  cu.seg, cu.tile, Ls[cu.b], lane);
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        if (lane == 0) {
+                            tc::tc_fence_after();
+                            const uint64_t ka = dk0 + static_cast<uint32_t>(s * (2 * KB >> 4));
+#pragma unroll
+                            for (int kq = 0; kq < D / 16; ++kq) {
+                                const uint64_t a = ka + (((kq >> 2) * KB + (kq & 3) * 32) >> 4);
+                                const uint64_t bh = dq0 + (((kq >> 2) * (2 * G * 128) + (kq & 3) * 32) >> 4);
+                                tc::mma_f16(tmem + (ks & 1) * G, a, bh, id_s, kq > 0);
+                                tc::mma_f16(tmem + (ks & 1) * G, a, bh + (G * 128 >> 4), id_s, true);  // the lo rows
+                            }
+                            tc::mma_commit(bar(kSFull + (ks & 1)));
+                            tc::mma_commit(bar(kEmptyK + s));  // the K tile is read
+                        }
+                        __syncwarp();
+                        if (new_piece) {
+                            ++qcount;
+                            firsts |= 1u << (ks & 31);
+                        } else {
+                            firsts &= ~(1u << (ks & 31));
+                        }
+                        if (++ks < n_my) advance_pass(cu, P, p.B, spp, np);
+                        did = true;
                     }
-                    __syncwarp();
-                    if (k > 0 && !new_piece && !issue_pv(k - 1)) { ok = false; break; }
-                    if (k + 1 < n_my) advance_pass(cu, P, p.B, spp, np);
                 }
-                if (ok) issue_pv(n_my - 1);
+                if (G != 64 && kp < ks) {
+                    // P.V of tile kp: into O, accumulating after the piece's first tile
+                    const bool first = (firsts >> (kp & 31)) & 1u;
+                    bool r = wide::mbar_test(bar(kPFull), kp & 1);
+                    if (r) r = wide::mbar_test(bar(kFullV + kp % NSV), (kp / NSV) & 1);
+                    if (r && first && opieces > 0) r = wide::mbar_test(bar(kOFree), (opieces - 1) & 1);
+                    if (__all_sync(FULL, r)) {
+                        if (first) ++opieces;
+                        if (lane == 0) {
+                            tc::tc_fence_after();
+                            const uint64_t va = dv0 + static_cast<uint32_t>((kp % NSV) * (2 * KB >> 4));
+#pragma unroll
+                            for (int kq = 0; kq < TM / 16; ++kq) {
+                                const uint64_t a = va + (kq * 2048 >> 4);
+                                const uint64_t bh = dp0 + (kq * 2048 >> 4);  // key rows 16 kq .. (hi, then lo at column G)
+                                tc::mma_f16(tmem + 2 * G, a, bh, id_o, !first || kq > 0);
+                                if constexpr (!LY::PVC) tc::mma_f16(tmem + 2 * G, a, bh + (LY::P_LO >> 4), id_o, true);
+                            }
+                            tc::mma_commit(bar(kOFull));
+                            tc::mma_commit(bar(kEmptyV + kp % NSV));
+                        }
+                        __syncwarp();
+                        ++kp;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    idle0 = clock64();
+                } else {
+                    if (*abort_flag) break;
+                    if (clock64() - idle0 > p.wait_cycles) {
+                        if (lane == 0) atomicOr(p.err, kErrTimeout);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
             }
             // one last commit: it completes once every MMA issued above has (the drain after an abort)
             if (lane == 0) tc::mma_commit(bar(kDrain));
