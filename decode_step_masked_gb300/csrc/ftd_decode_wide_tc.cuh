@@ -71,11 +71,11 @@ struct Layout {
     static constexpr int OFF_PREFIX = OFF_MISC + MISC_BYTES;
     static constexpr bool HAVE_VP = OFF_PREFIX + round_up((3 * kMaxBatch + 2) * 4, 128) + 1024 <= 232448;
     // weight of a segment boundary in the static split, in tiles: a piece's end (the next
-    // piece's q, the partial or the merge, the block's rows) costs about four tiles with
-    // 64-row blocks and one with 32-row blocks (measured: boundary weights 1, 2, 3, 4, 6 gave
-    // 62.5 / 61.6 / 58.0 / 56.1 / 56.7 us on the multi-query step; 1, 2, 3 gave 126.9 /
-    // 130.4 / 128.5 us on the 70B-shaped step with 4 new tokens)
-    static constexpr int ALPHA = HAVE_VP ? (G == 64 ? 4 : 1) : 0;
+    // piece's q, the partial or the merge, the block's rows) costs about five tiles with
+    // 64-row blocks and one with 32-row blocks (measured with the current issue order:
+    // boundary weights 3, 4, 5, 6 gave 46.6 / 44.9 / 44.1 / 44.2 us on the multi-query step;
+    // 0, 1, 2, 3 gave 117.7 / 117.1 / 121.7 / 117.9 us on the 70B-shaped step with 4 new tokens)
+    static constexpr int ALPHA = HAVE_VP ? (G == 64 ? 5 : 1) : 0;
     static constexpr int PREFIX_BYTES = ((HAVE_VP ? 3 : 2) * kMaxBatch + 2) * 4;
     static constexpr int SMEM = OFF_PREFIX + round_up(PREFIX_BYTES, 128) + 1024;
     // TMEM: two S buffers (columns 0 and G), then O.  One P.V MMA per 16 key rows takes the hi
