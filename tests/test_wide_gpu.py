@@ -79,14 +79,16 @@ def test_wide_multi_token(Hq, Hkv, T):
     check(w, inp, what=f"wide multi-token {Hq}/{Hkv} T{T}")
 
 
+@pytest.mark.parametrize("window", [0, 300])
 @pytest.mark.parametrize("Hq,T", [(32, 1), (64, 1), (8, 4)])
-def test_wide_many_short_segments(Hq, T):
+def test_wide_many_short_segments(Hq, T, window):
     """200 slots with contexts up to 1000 tokens, some inactive: about five tiles per block,
-    so blocks cross several pieces, and most segments end in a merge of partials."""
+    so blocks cross several pieces, and most segments end in a merge of partials; with a
+    window, most pieces start on a tile whose rows before the window start are zeroed."""
     rng = np.random.default_rng(91)
     lens = rng.integers(-1, 1000, size=200)
     w, inp = case("bf16", B=200, Hq=Hq, Hkv=1, Lmax=1024, lens=lens, T=T, seed=92)
-    check(w, inp, what=f"wide short segments Hq{Hq} T{T}")
+    check(w, inp, window=window, what=f"wide short segments Hq{Hq} T{T} window {window}")
 
 
 @pytest.mark.parametrize("rise", [20.0, 60.0])
